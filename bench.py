@@ -1,0 +1,539 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused cascaded-reduction hot path on GB300.
+
+One step = one pass of every fused kernel over its workload, on inputs
+resident in HBM:
+  decode split-KV, Lk = 32768 (B 32, Hq 32, Hkv 8, d 128, bf16)
+  BERT-style prefill attention (B 8, H 16, L 512, d 64, bf16)
+  MoE gate (8192 x 4096 x 64 experts, top-2)
+  row absmax -> E4M3 -> FP8 GEMM (4096^3)
+  decode split-KV, Lk = 2048
+Each kernel's inputs were last touched one step earlier with >= 4.3 GB
+streamed in between, far more than the 129 MB L2, so every launch starts
+from a cold L2 without an explicit flush.
+
+Metric: the step's roofline time (sum over the kernels of
+max(algorithmic bytes / HBM peak, algorithmic FLOPs / tensor peak)) divided
+by the measured step time, in percent.  Peaks come from MEASURED_PEAKS.json
+when present, else the fallback figures (6.8 TB/s, 1.9 PFLOP/s bf16; FP8 =
+2x bf16).  One JSON line is printed by rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from cascaded_reductions_loop_gb300 import inputs as I  # noqa: E402
+
+METRIC = "fused cascaded-reduction TFLOP/s or HBM GB/s, % of GB300 roofline (1 GPU)"
+UNIT = "% of roofline (step roofline time / measured step time)"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFS = 1900.0
+FALLBACK_BF16_TFS_SUSTAINED = 1700.0
+DOMINANT = "decode_32k"
+
+
+# ------------------------------------------------------------------ peaks
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            hbm = float(d.get("hbm_gbs") or d.get("hbm_GBps") or 0)
+            bf16 = float(d.get("bf16_tflops") or 0)
+            bf16s = float(d.get("bf16_tflops_sustained") or bf16)
+            if hbm > 0 and bf16 > 0:
+                return {"hbm_gbs": hbm, "bf16_tfs": bf16, "bf16_tfs_sustained": bf16s,
+                        "source": "measured"}
+        except (ValueError, OSError):
+            pass
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tfs": FALLBACK_BF16_TFS,
+            "bf16_tfs_sustained": FALLBACK_BF16_TFS_SUSTAINED, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ workload
+
+
+class Op:
+    """One fused call of the step: its algorithmic bytes/FLOPs and a launcher."""
+
+    def __init__(self, name, bytes_, flops, tc_dtype, n_kernels):
+        self.name, self.bytes, self.flops, self.tc_dtype = name, bytes_, flops, tc_dtype
+        self.n_kernels = n_kernels
+
+    def roofline_s(self, peaks):
+        t_mem = self.bytes / (peaks["hbm_gbs"] * 1e9)
+        tc = peaks["bf16_tfs_sustained"] * (2.0 if self.tc_dtype == "fp8" else 1.0)
+        t_tc = self.flops / (tc * 1e12) if self.flops else 0.0
+        return max(t_mem, t_tc)
+
+    def bound(self, peaks):
+        t_mem = self.bytes / (peaks["hbm_gbs"] * 1e9)
+        tc = peaks["bf16_tfs_sustained"] * (2.0 if self.tc_dtype == "fp8" else 1.0)
+        t_tc = self.flops / (tc * 1e12) if self.flops else 0.0
+        return "hbm" if t_mem >= t_tc else "tensor"
+
+
+def decode_op(name, s):
+    kv = 2 * s.B * s.Hkv * s.Lk * s.d * 2
+    qo = 2 * s.B * s.Hq * s.d * 2
+    return Op(name, kv + qo, 4 * s.B * s.Hq * s.Lk * s.d, "bf16", 2)
+
+
+def make_ops():
+    b = I.BERT_PREFILL
+    m = I.MOE_GATE
+    f = I.FP8_GEMM
+    return [
+        decode_op("decode_32k", I.DECODE_32K),
+        Op("bert_prefill", 4 * b.B * b.Hq * b.Lq * b.d * 2, 4 * b.B * b.Hq * b.Lq * b.Lk * b.d,
+           "bf16", 1),
+        Op("moe_gate", m.T * m.D * 2 + m.E * m.D * 2 + m.T * m.k * 8, 2 * m.T * m.D * m.E, "bf16", 1),
+        Op("fp8_gemm", f.M * f.K * 2 + f.N * f.K + f.N * 4 + f.M * f.N * 2, 2 * f.M * f.N * f.K,
+           "fp8", 2),
+        decode_op("decode_2k", I.DECODE_2K),
+    ]
+
+
+def host_inputs():
+    """All step inputs as CPU tensors (seeded), keyed by op name."""
+    q32, k32, v32 = I.decode_inputs(I.DECODE_32K)
+    q2, k2, v2 = I.decode_inputs(I.DECODE_2K)
+    qb, kb, vb = I.attention_inputs(I.BERT_PREFILL)
+    xm, wm = I.moe_inputs(I.MOE_GATE)
+    xf, wqf, swf = I.fp8_inputs(I.FP8_GEMM)
+    return {"decode_32k": [q32, k32, v32], "decode_2k": [q2, k2, v2],
+            "bert_prefill": [qb, kb, vb], "moe_gate": [xm, wm], "fp8_gemm": [xf, wqf, swf]}
+
+
+class Step:
+    """Device buffers and the calls of one step, through the public binding."""
+
+    def __init__(self, rf, dev_inputs):
+        self.rf = rf
+        d = dev_inputs
+        self.inp = d
+        s32, s2, sb, sm, sf = I.DECODE_32K, I.DECODE_2K, I.BERT_PREFILL, I.MOE_GATE, I.FP8_GEMM
+        cuda = torch.device("cuda")
+        self.o32 = torch.empty(s32.B, s32.Hq, s32.d, dtype=torch.bfloat16, device=cuda)
+        self.o2 = torch.empty(s2.B, s2.Hq, s2.d, dtype=torch.bfloat16, device=cuda)
+        self.ws32 = torch.empty(rf.rf_attn_decode_splitkv_workspace_size(
+            s32.B, s32.Hq, s32.Hkv, s32.Lk, s32.d, 0), dtype=torch.uint8, device=cuda)
+        self.ws2 = torch.empty(rf.rf_attn_decode_splitkv_workspace_size(
+            s2.B, s2.Hq, s2.Hkv, s2.Lk, s2.d, 0), dtype=torch.uint8, device=cuda)
+        self.ob = torch.empty(sb.B, sb.Hq, sb.Lq, sb.d, dtype=torch.bfloat16, device=cuda)
+        self.idx = torch.empty(sm.T, sm.k, dtype=torch.int32, device=cuda)
+        self.wts = torch.empty(sm.T, sm.k, dtype=torch.float32, device=cuda)
+        self.y = torch.empty(sf.M, sf.N, dtype=torch.bfloat16, device=cuda)
+        self.wsf = torch.empty(rf.rf_absmax_fp8_gemm_workspace_size(sf.M, sf.N, sf.K),
+                               dtype=torch.uint8, device=cuda)
+        self.calls = {
+            "decode_32k": lambda: rf.rf_attn_decode_splitkv(*d["decode_32k"], self.o32, s32.scale,
+                                                            self.ws32),
+            "bert_prefill": lambda: rf.rf_attn_fwd(*d["bert_prefill"], self.ob, sb.scale),
+            "moe_gate": lambda: rf.rf_moe_gate_topk_softmax(*d["moe_gate"], sm.k, self.idx,
+                                                            self.wts),
+            "fp8_gemm": lambda: rf.rf_absmax_fp8_gemm(*d["fp8_gemm"], self.y, workspace=self.wsf),
+            "decode_2k": lambda: rf.rf_attn_decode_splitkv(*d["decode_2k"], self.o2, s2.scale,
+                                                           self.ws2),
+        }
+        self.outputs = {"decode_32k": [self.o32], "decode_2k": [self.o2],
+                        "bert_prefill": [self.ob], "moe_gate": [self.idx, self.wts],
+                        "fp8_gemm": [self.y]}
+
+
+# ------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ timing
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Maximum of a per-rank float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def traffic_for(kernel_key):
+    """Per-launch DRAM bytes from a committed ncu capture, if the kernel source
+    has not changed since (matched by hash); else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        d = json.load(open(path)).get(kernel_key)
+    except (ValueError, OSError):
+        return None
+    if not d:
+        return None
+    src = os.path.join(ROOT, d["source"])
+    if not os.path.exists(src):
+        return None
+    sha = hashlib.sha1(open(src, "rb").read()).hexdigest()
+    return d["bytes_per_launch"] if sha == d["source_sha1"] else None
+
+
+def run_ours(args, world, rank, local):
+    import cascaded_reductions_loop_gb300 as rf
+
+    torch.cuda.set_device(local)
+    peaks = load_peaks()
+    ops = make_ops()
+    host = host_inputs()
+    dev = {k: [t.cuda() for t in v] for k, v in host.items()}
+    step = Step(rf, dev)
+    stream = torch.cuda.current_stream()
+
+    # warm-up
+    for _ in range(args.warmup):
+        for op in ops:
+            step.calls[op.name]()
+    torch.cuda.synchronize()
+    st = rf.rf_get_device_status()
+    if st != rf.RF_OK:
+        raise RuntimeError(f"device status after warm-up: {rf.rf_status_string(st)}")
+
+    # timed region: K steps, one event pair per fused call
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    n = len(ops)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(args.steps):
+        evs[s][0].record(stream)
+        for i, op in enumerate(ops):
+            step.calls[op.name]()
+            evs[s][i + 1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    st = rf.rf_get_device_status()
+    if st != rf.RF_OK:
+        raise RuntimeError(f"device status after timing: {rf.rf_status_string(st)}")
+
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
+    ms_per_step = total_ms / args.steps
+    per_op_ms = {op.name: statistics.median(evs[s][i].elapsed_time(evs[s][i + 1])
+                                            for s in range(args.steps))
+                 for i, op in enumerate(ops)}
+    roof_s = sum(op.roofline_s(peaks) for op in ops)
+    value = 100.0 * world * roof_s / (ms_per_step * 1e-3)
+
+    rows = {}
+    for op in ops:
+        t = per_op_ms[op.name] * 1e-3
+        r = {"ms": round(per_op_ms[op.name], 5), "bound": op.bound(peaks),
+             "roofline_frac": round(op.roofline_s(peaks) / t, 4)}
+        if op.bound(peaks) == "hbm":
+            r["GBps"] = round(op.bytes / t / 1e9, 1)
+        else:
+            r["TFLOPs"] = round(op.flops / t / 1e12, 1)
+        rows[op.name] = r
+
+    dom = next(op for op in ops if op.name == DOMINANT)
+    dom_t = per_op_ms[DOMINANT] * 1e-3
+    achieved = dom.bytes / dom_t / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": traffic_for("decode_32k"),
+                "kernel": "rf_attn_decode_splitkv at Lk=32768 (partial + merge kernels)",
+                "peak_source": peaks["source"]}
+
+    result = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; shapes of the five named workloads)",
+        "config": {"workload": "decode32k+bert_prefill+moe_gate+fp8_gemm+decode2k",
+                   "decode": "B32 Hq32 Hkv8 d128 Lk {32768, 2048} bf16",
+                   "prefill": "B8 H16 L512 d64 bf16", "moe": "T8192 D4096 E64 top2 bf16",
+                   "fp8": "M=N=K=4096 e4m3 (bf16 X in, bf16 Y out)",
+                   "l2": "no flush: step streams >= 4.6 GB (> 129 MB L2) between reuses",
+                   "parallelism": f"replicas x{world}"},
+        "peaks": {k: peaks[k] for k in ("hbm_gbs", "bf16_tfs", "bf16_tfs_sustained", "source")},
+        "rows": rows,
+        "roofline": roofline,
+        "gpu_launches": args.steps * sum(op.n_kernels for op in ops),
+        "clocks": clk,
+    }
+
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(rf, ops, peaks, host, step, world, args)
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        result["cpu_baseline"] = cpu_baseline(ops, peaks, host, budget_s=args.cpu_budget)
+    return result
+
+
+def run_e2e(rf, ops, peaks, host, step, world, args):
+    """Same metric through the public binding with host buffers: every step
+    copies its inputs from pinned host memory and its results back."""
+    pinned = {k: [t.pin_memory() for t in v] for k, v in host.items()}
+    out_host = {k: [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+                for k, outs in step.outputs.items()}
+    h2d = sum(t.numel() * t.element_size() for v in pinned.values() for t in v)
+    d2h = sum(t.numel() * t.element_size() for v in out_host.values() for t in v)
+    stream = torch.cuda.current_stream()
+
+    def one():
+        for op in ops:
+            for dst, src in zip(step.inp[op.name], pinned[op.name]):
+                dst.copy_(src, non_blocking=True)
+            step.calls[op.name]()
+            for dst, src in zip(out_host[op.name], step.outputs[op.name]):
+                dst.copy_(src, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    k = max(2, min(args.steps, 5))
+    barrier(world)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(k):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b), world) / k
+    roof_s = sum(op.roofline_s(peaks) for op in ops)
+    return {"value": round(100.0 * world * roof_s / (ms * 1e-3), 4), "unit": UNIT,
+            "ms_per_step": round(ms, 3), "steps": k, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+
+def oracle_sample_seconds(host, frac):
+    """Times the fp64 oracle on a bounded sample of every op; returns
+    {op: (seconds, fraction of the op's full work covered)}."""
+    from oracle import attention as A
+    from oracle import fp8_quant_gemm as F
+    from oracle import moe_gate as G
+
+    out = {}
+    rng = np.random.default_rng(0)
+
+    s = I.DECODE_32K
+    q, k, v = host["decode_32k"]
+    nrows = max(1, int(round(frac * s.B * s.Hq)))
+    rows = [(int(b), int(h)) for b, h in zip(rng.integers(0, s.B, nrows), rng.integers(0, s.Hq, nrows))]
+    t = time.perf_counter()
+    A.decode_attention(q, k, v, s.scale, rows=rows)
+    out["decode_32k"] = (time.perf_counter() - t, nrows / (s.B * s.Hq))
+
+    s = I.DECODE_2K
+    q, k, v = host["decode_2k"]
+    nrows = max(1, int(round(frac * 4 * s.B * s.Hq)))
+    rows = [(int(b), int(h)) for b, h in zip(rng.integers(0, s.B, nrows), rng.integers(0, s.Hq, nrows))]
+    t = time.perf_counter()
+    A.decode_attention(q, k, v, s.scale, rows=rows)
+    out["decode_2k"] = (time.perf_counter() - t, nrows / (s.B * s.Hq))
+
+    s = I.BERT_PREFILL
+    q, k, v = host["bert_prefill"]
+    nh = max(1, int(round(frac * 4 * s.B * s.Hq)))
+    t = time.perf_counter()
+    for i in range(nh):
+        b, h = divmod(i % (s.B * s.Hq), s.Hq)
+        A.attention(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1], s.scale)
+    out["bert_prefill"] = (time.perf_counter() - t, nh / (s.B * s.Hq))
+
+    s = I.MOE_GATE
+    x, w = host["moe_gate"]
+    nt = max(1, int(round(frac * 4 * s.T)))
+    t = time.perf_counter()
+    G.moe_gate(x, w, s.k, rows=range(nt))
+    out["moe_gate"] = (time.perf_counter() - t, nt / s.T)
+
+    s = I.FP8_GEMM
+    x, wq, sw = host["fp8_gemm"]
+    nr = max(1, int(round(frac * s.M)))
+    t = time.perf_counter()
+    F.absmax_fp8_gemm(x, wq, sw, rows=range(nr))
+    out["fp8_gemm"] = (time.perf_counter() - t, nr / s.M)
+    return out
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(ops, peaks, host, budget_s=15.0):
+    # calibrate the sample size on a tiny fraction, then size it to the budget
+    frac = 1.0 / 512
+    t0 = time.perf_counter()
+    oracle_sample_seconds(host, frac)
+    cal = time.perf_counter() - t0
+    frac = min(0.25, frac * max(1.0, budget_s / max(cal, 1e-3)))
+    res = oracle_sample_seconds(host, frac)
+    full_s = sum(sec / f for sec, f in res.values())
+    roof_s = sum(op.roofline_s(peaks) for op in ops)
+    return {"value": 100.0 * roof_s / full_s, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "seconds_per_full_step": round(full_s, 2),
+            "sample": (f"{frac:.4f} of each op's rows/heads/tokens (fp64 numpy oracle, BLAS "
+                       f"threads up to the core count); full step extrapolated linearly"),
+            "sample_seconds": round(sum(sec for sec, _ in res.values()), 2)}
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the CPU fp64 oracle as it stands, on the same
+    workload and metric, each step a bounded sample."""
+    if rank != 0:
+        return None
+    peaks = load_peaks()
+    ops = make_ops()
+    host = host_inputs()
+    frac = 1.0 / 1024
+    for _ in range(max(1, min(args.warmup, 1))):
+        oracle_sample_seconds(host, frac)
+    t_full = []
+    for _ in range(args.steps):
+        res = oracle_sample_seconds(host, frac)
+        t_full.append(sum(sec / f for sec, f in res.values()))
+    full_s = statistics.median(t_full)
+    roof_s = sum(op.roofline_s(peaks) for op in ops)
+    value = 100.0 * roof_s / full_s
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(full_s * 1e3, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; shapes of the five named workloads)",
+        "config": {"workload": "decode32k+bert_prefill+moe_gate+fp8_gemm+decode2k",
+                   "parallelism": "CPU oracle, rank 0 only"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"{frac:.5f} of each op's rows/heads/tokens per step, "
+                                   "full step extrapolated linearly"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of CPU oracle work for the cpu_baseline sample")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("note: raising --warmup to 3 (minimum)", file=sys.stderr)
+        args.warmup = 3
+
+    world, rank, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    try:
+        if args.impl == "reference":
+            res = run_reference(args, world, rank)
+        else:
+            res = run_ours(args, world, rank, local)
+        if rank == 0 and res is not None:
+            print(json.dumps(res), flush=True)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,200 @@
+"""Python binding of librf_gb300.so, the fused cascaded-reduction kernels for
+GB300 (sm_103a).
+
+Argument marshalling only: each function below checks tensor shapes and
+dtypes, then calls the C entry point of the same name (declared in
+``include/rf.h``) with raw device pointers and the current torch CUDA
+stream.  Every step of the computation runs in the library's CUDA kernels;
+there is no other implementation behind these names.  If the library is
+missing, importing this package raises: build it with
+``cascaded_reductions_loop_gb300._build.build()``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "RFError", "lib", "rf_status_string", "rf_version", "rf_get_device_status",
+    "rf_attn_fwd", "rf_attn_decode_splitkv", "rf_attn_decode_splitkv_num_splits",
+    "rf_attn_decode_splitkv_workspace_size", "rf_moe_gate_topk_softmax",
+    "rf_absmax_fp8_gemm", "rf_absmax_fp8_gemm_workspace_size", "rf_selftest_wait_timeout",
+    "RF_OK", "RF_ERR_INVALID_ARG", "RF_ERR_UNSUPPORTED", "RF_ERR_WORKSPACE", "RF_ERR_CUDA",
+    "RF_ERR_DEVICE_TIMEOUT", "RF_F32", "RF_BF16",
+]
+
+RF_OK, RF_ERR_INVALID_ARG, RF_ERR_UNSUPPORTED, RF_ERR_WORKSPACE, RF_ERR_CUDA, \
+    RF_ERR_DEVICE_TIMEOUT = range(6)
+RF_F32, RF_BF16 = 0, 1
+
+LIB_PATH = _build.LIB_PATH
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: the CUDA library must be built first "
+        "(cascaded_reductions_loop_gb300._build.build()); there is no fallback path")
+
+_c = ctypes
+_P = _c.c_void_p
+_I = _c.c_int
+_F = _c.c_float
+_Z = _c.c_size_t
+
+lib = _c.CDLL(LIB_PATH)
+
+_SIGS = {
+    "rf_status_string": (_c.c_char_p, [_I]),
+    "rf_version": (_I, []),
+    "rf_get_device_status": (_I, [_P]),
+    "rf_attn_fwd": (_I, [_I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "rf_attn_decode_splitkv_num_splits": (_I, [_I, _I, _I, _I, _I, _I]),
+    "rf_attn_decode_splitkv_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I]),
+    "rf_attn_decode_splitkv": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
+    "rf_moe_gate_topk_softmax": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P]),
+    "rf_absmax_fp8_gemm_workspace_size": (_Z, [_I, _I, _I]),
+    "rf_absmax_fp8_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _Z, _P]),
+    "rf_selftest_wait_timeout": (_I, [_I, _P]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+class RFError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {rf_status_string(status)}")
+
+
+def _check(status: int, where: str) -> None:
+    if status != RF_OK:
+        raise RFError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else _c.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return _c.c_void_p(stream.cuda_stream)
+
+
+def _need(t, dtype, shape, name):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+# ------------------------------------------------------------------ entry points
+
+
+def rf_status_string(status: int) -> str:
+    return lib.rf_status_string(int(status)).decode()
+
+
+def rf_version() -> int:
+    return lib.rf_version()
+
+
+def rf_get_device_status(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device status."""
+    return lib.rf_get_device_status(_stream(stream))
+
+
+def rf_attn_fwd(q, k, v, o, scale: float, causal: int = 0, stream=None) -> None:
+    """Single-segment fused attention.  q, o: [B,H,Lq,d]; k, v: [B,H,Lk,d];
+    all fp32 (exact SIMT path) or all bf16 (tcgen05 path)."""
+    B, H, Lq, d = q.shape
+    Lk = k.shape[2]
+    dt = q.dtype
+    if dt not in (torch.float32, torch.bfloat16):
+        raise ValueError("q must be float32 or bfloat16")
+    _need(q, dt, (B, H, Lq, d), "q")
+    _need(k, dt, (B, H, Lk, d), "k")
+    _need(v, dt, (B, H, Lk, d), "v")
+    _need(o, dt, (B, H, Lq, d), "o")
+    code = RF_F32 if dt == torch.float32 else RF_BF16
+    _check(lib.rf_attn_fwd(code, _ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, Lq, Lk, d,
+                           float(scale), int(causal), _stream(stream)), "rf_attn_fwd")
+
+
+def rf_attn_decode_splitkv_num_splits(B, Hq, Hkv, Lk, d, num_splits=0) -> int:
+    return lib.rf_attn_decode_splitkv_num_splits(B, Hq, Hkv, Lk, d, num_splits)
+
+
+def rf_attn_decode_splitkv_workspace_size(B, Hq, Hkv, Lk, d, num_splits=0) -> int:
+    return lib.rf_attn_decode_splitkv_workspace_size(B, Hq, Hkv, Lk, d, num_splits)
+
+
+def rf_attn_decode_splitkv(q, k, v, o, scale: float, workspace, num_splits: int = 0,
+                           stream=None) -> None:
+    """Multi-segment decode attention.  q, o: [B,Hq,d] bf16; k, v:
+    [B,Hkv,Lk,d] bf16; workspace: a uint8 CUDA tensor of at least
+    rf_attn_decode_splitkv_workspace_size(...) bytes."""
+    B, Hq, d = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    _need(q, torch.bfloat16, (B, Hq, d), "q")
+    _need(k, torch.bfloat16, (B, Hkv, Lk, d), "k")
+    _need(v, torch.bfloat16, (B, Hkv, Lk, d), "v")
+    _need(o, torch.bfloat16, (B, Hq, d), "o")
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.rf_attn_decode_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, Hq, Hkv, Lk, d,
+                                      float(scale), int(num_splits), _ptr(workspace), ws_bytes,
+                                      _stream(stream)), "rf_attn_decode_splitkv")
+
+
+def rf_moe_gate_topk_softmax(x, w_gate, k: int, idx, weights, stream=None) -> None:
+    """Fused MoE gate.  x: [T,D] bf16; w_gate: [E,D] bf16 (expert-major);
+    idx: [T,k] int32 out; weights: [T,k] fp32 out."""
+    T, D = x.shape
+    E = w_gate.shape[0]
+    _need(x, torch.bfloat16, (T, D), "x")
+    _need(w_gate, torch.bfloat16, (E, D), "w_gate")
+    _need(idx, torch.int32, (T, k), "idx")
+    _need(weights, torch.float32, (T, k), "weights")
+    _check(lib.rf_moe_gate_topk_softmax(_ptr(x), _ptr(w_gate), T, D, E, int(k), _ptr(idx),
+                                        _ptr(weights), _stream(stream)),
+           "rf_moe_gate_topk_softmax")
+
+
+def rf_absmax_fp8_gemm_workspace_size(M, N, K) -> int:
+    return lib.rf_absmax_fp8_gemm_workspace_size(M, N, K)
+
+
+def rf_absmax_fp8_gemm(x, wq, sw, y, sx_out=None, xq_out=None, workspace=None,
+                       stream=None) -> None:
+    """Row absmax -> E4M3 quantisation -> FP8 GEMM -> dequantisation.
+    x: [M,K] bf16; wq: [N,K] uint8 E4M3 codes; sw: [N] fp32; y: [M,N] bf16
+    out; sx_out: [M] fp32 out or None; xq_out: [M,K] uint8 out or None;
+    workspace: uint8 CUDA tensor (needed when sx_out or xq_out is None)."""
+    M, K = x.shape
+    N = wq.shape[0]
+    _need(x, torch.bfloat16, (M, K), "x")
+    _need(wq, torch.uint8, (N, K), "wq")
+    _need(sw, torch.float32, (N,), "sw")
+    _need(y, torch.bfloat16, (M, N), "y")
+    if sx_out is not None:
+        _need(sx_out, torch.float32, (M,), "sx_out")
+    if xq_out is not None:
+        _need(xq_out, torch.uint8, (M, K), "xq_out")
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.rf_absmax_fp8_gemm(_ptr(x), _ptr(wq), _ptr(sw), _ptr(y), M, N, K, _ptr(sx_out),
+                                  _ptr(xq_out), _ptr(workspace), ws_bytes, _stream(stream)),
+           "rf_absmax_fp8_gemm")
+
+
+def rf_selftest_wait_timeout(timeout_us: int, stream=None) -> None:
+    _check(lib.rf_selftest_wait_timeout(int(timeout_us), _stream(stream)),
+           "rf_selftest_wait_timeout")

@@ -1,0 +1,257 @@
+// api.cu -- the C ABI: argument validation, dispatch to the kernels, the
+// device-side error word, tensor-map encoding and the wait-timeout self-test.
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <mutex>
+
+#include "rf_device.cuh"
+#include "rf_internal.h"
+
+#define RF_VERSION_NUM 10000
+
+namespace rf {
+
+// One error word per device: kernels OR kDevErr* bits into it when a bounded
+// wait runs out; rf_get_device_status reads and clears it.
+static __device__ unsigned g_error_word;
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned* g_err_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+}  // namespace
+
+unsigned* device_error_word() {
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+int sm_count() {
+  const int dev = current_device();
+  if (dev < 0) return 0;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_sm_count[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
+                    uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                    bool swizzle128) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return false;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  }
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------ self-test
+
+// One thread waits on a barrier that expects two arrivals but only ever
+// receives one, with a short limit; on timeout it records the error bit and
+// returns.  Exercises the bounded-wait path without hanging or faulting.
+__global__ void selftest_wait_kernel(uint64_t limit_ns, unsigned* err) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 2);
+    fence_mbar_init();
+    mbar_arrive(b);                 // one of two arrivals: the phase never completes
+    if (!mbar_wait(b, 0, limit_ns)) raise_error(err, kDevErrTimeout);
+  }
+}
+
+cudaError_t launch_selftest_wait_timeout(int timeout_us, unsigned* err, cudaStream_t s) {
+  selftest_wait_kernel<<<1, 32, 0, s>>>((uint64_t)timeout_us * 1000ull, err);
+  return cudaGetLastError();
+}
+
+}  // namespace rf
+
+// ================================================================ C ABI
+
+using namespace rf;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool ptr_ok(const void* p) { return p != nullptr && aligned16(p); }
+
+rf_status from_cuda(cudaError_t e) { return e == cudaSuccess ? RF_OK : RF_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* rf_status_string(int status) {
+  switch (status) {
+    case RF_OK: return "RF_OK";
+    case RF_ERR_INVALID_ARG: return "RF_ERR_INVALID_ARG: invalid argument";
+    case RF_ERR_UNSUPPORTED: return "RF_ERR_UNSUPPORTED: shape or option not supported";
+    case RF_ERR_WORKSPACE: return "RF_ERR_WORKSPACE: workspace missing or too small";
+    case RF_ERR_CUDA: return "RF_ERR_CUDA: CUDA runtime call or kernel launch failed";
+    case RF_ERR_DEVICE_TIMEOUT: return "RF_ERR_DEVICE_TIMEOUT: a kernel's bounded wait ran out";
+    default: return "unknown rf_status";
+  }
+}
+
+int rf_version(void) { return RF_VERSION_NUM; }
+
+rf_status rf_get_device_status(rf_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return RF_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_error_word, sizeof(v)) != cudaSuccess) return RF_ERR_CUDA;
+  if (v != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) return RF_ERR_CUDA;
+  }
+  return (v & kDevErrTimeout) ? RF_ERR_DEVICE_TIMEOUT : RF_OK;
+}
+
+rf_status rf_attn_fwd(int dtype, const void* Q, const void* K, const void* V, void* O, int B,
+                      int H, int Lq, int Lk, int d, float scale, int causal, rf_stream_t stream) {
+  if (dtype != RF_F32 && dtype != RF_BF16) return RF_ERR_INVALID_ARG;
+  if (!ptr_ok(Q) || !ptr_ok(K) || !ptr_ok(V) || !ptr_ok(O)) return RF_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Lq < 1 || Lk < 1 || d < 1 || causal != 0) return RF_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !(scale < INFINITY)) return RF_ERR_INVALID_ARG;
+  if ((int64_t)B * H * Lq >= (1ll << 31) || (int64_t)B * H * Lk >= (1ll << 31))
+    return RF_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == RF_F32) {
+    if (d != 64 && d != 128) return RF_ERR_UNSUPPORTED;
+    return from_cuda(launch_attn_fwd_f32(static_cast<const float*>(Q),
+                                         static_cast<const float*>(K),
+                                         static_cast<const float*>(V), static_cast<float*>(O), B,
+                                         H, Lq, Lk, d, scale, s));
+  }
+  if (d != 64) return RF_ERR_UNSUPPORTED;
+  unsigned* err = device_error_word();
+  if (!err) return RF_ERR_CUDA;
+  return from_cuda(launch_attn_fwd_bf16_tc(Q, K, V, O, B, H, Lq, Lk, d, scale, err, s));
+}
+
+static rf_status decode_shape_check(int B, int Hq, int Hkv, int Lk, int d, int num_splits) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lk < 1 || d < 1 || num_splits < 0) return RF_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return RF_ERR_INVALID_ARG;
+  if (num_splits > Lk) return RF_ERR_INVALID_ARG;
+  if ((int64_t)B * Hkv * Lk >= (1ll << 31)) return RF_ERR_INVALID_ARG;
+  const int G = Hq / Hkv;
+  if (d != 128 || (G != 1 && G != 2 && G != 4 && G != 8)) return RF_ERR_UNSUPPORTED;
+  return RF_OK;
+}
+
+int rf_attn_decode_splitkv_num_splits(int B, int Hq, int Hkv, int Lk, int d, int num_splits) {
+  if (decode_shape_check(B, Hq, Hkv, Lk, d, num_splits) != RF_OK) return 0;
+  return decode_num_splits(B, Hq, Hkv, Lk, d, num_splits);
+}
+
+size_t rf_attn_decode_splitkv_workspace_size(int B, int Hq, int Hkv, int Lk, int d,
+                                             int num_splits) {
+  const int S = rf_attn_decode_splitkv_num_splits(B, Hq, Hkv, Lk, d, num_splits);
+  if (S <= 0) return 0;
+  return decode_workspace_bytes(B, Hq, d, S);
+}
+
+rf_status rf_attn_decode_splitkv(const void* Q, const void* K, const void* V, void* O, int B,
+                                 int Hq, int Hkv, int Lk, int d, float scale, int num_splits,
+                                 void* workspace, size_t workspace_bytes, rf_stream_t stream) {
+  if (!ptr_ok(Q) || !ptr_ok(K) || !ptr_ok(V) || !ptr_ok(O)) return RF_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !(scale < INFINITY)) return RF_ERR_INVALID_ARG;
+  rf_status st = decode_shape_check(B, Hq, Hkv, Lk, d, num_splits);
+  if (st != RF_OK) return st;
+  const int S = decode_num_splits(B, Hq, Hkv, Lk, d, num_splits);
+  if (S <= 0) return RF_ERR_CUDA;   // auto choice needs the device's SM count
+  if (!workspace || !aligned16(workspace) ||
+      workspace_bytes < decode_workspace_bytes(B, Hq, d, S))
+    return RF_ERR_WORKSPACE;
+  unsigned* err = device_error_word();
+  if (!err) return RF_ERR_CUDA;
+  return from_cuda(launch_decode_splitkv(Q, K, V, O, B, Hq, Hkv, Lk, d, scale, S, workspace, err,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+rf_status rf_moe_gate_topk_softmax(const void* X, const void* Wg, int T, int D, int E, int k,
+                                   int32_t* idx, float* w, rf_stream_t stream) {
+  if (!ptr_ok(X) || !ptr_ok(Wg) || !ptr_ok(idx) || !ptr_ok(w)) return RF_ERR_INVALID_ARG;
+  if (T < 1 || D < 1 || E < 1 || k < 1 || k > E) return RF_ERR_INVALID_ARG;
+  if (D % 8 != 0) return RF_ERR_INVALID_ARG;   // 16-byte row pitch for TMA
+  if (E != 64 || k > 8) return RF_ERR_UNSUPPORTED;
+  unsigned* err = device_error_word();
+  if (!err) return RF_ERR_CUDA;
+  return from_cuda(launch_moe_gate(X, Wg, T, D, E, k, idx, w, err,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t rf_absmax_fp8_gemm_workspace_size(int M, int N, int K) {
+  if (M < 1 || N < 1 || K < 16 || K % 16 != 0) return 0;
+  return fp8_workspace_bytes(M, N, K);
+}
+
+rf_status rf_absmax_fp8_gemm(const void* X, const uint8_t* Wq, const float* sw, void* Y, int M,
+                             int N, int K, float* sx_out, uint8_t* xq_out, void* workspace,
+                             size_t workspace_bytes, rf_stream_t stream) {
+  if (!ptr_ok(X) || !ptr_ok(Wq) || !ptr_ok(sw) || !ptr_ok(Y)) return RF_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 16 || K % 16 != 0) return RF_ERR_INVALID_ARG;
+  if ((int64_t)M * K >= (1ll << 40) || (int64_t)N * K >= (1ll << 40)) return RF_ERR_INVALID_ARG;
+  if ((sx_out && !aligned16(sx_out)) || (xq_out && !aligned16(xq_out))) return RF_ERR_INVALID_ARG;
+  float* sx = sx_out;
+  uint8_t* xq = xq_out;
+  if (!sx || !xq) {
+    if (!workspace || !aligned16(workspace) || workspace_bytes < fp8_workspace_bytes(M, N, K))
+      return RF_ERR_WORKSPACE;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const size_t xq_bytes = ((size_t)M * K + 255) & ~(size_t)255;
+    if (!xq) xq = ws;
+    if (!sx) sx = reinterpret_cast<float*>(ws + xq_bytes);
+  }
+  unsigned* err = device_error_word();
+  if (!err) return RF_ERR_CUDA;
+  return from_cuda(launch_absmax_fp8_gemm(X, Wq, sw, Y, M, N, K, sx, xq, err,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+rf_status rf_selftest_wait_timeout(int timeout_us, rf_stream_t stream) {
+  if (timeout_us < 1 || timeout_us > 1000000) return RF_ERR_INVALID_ARG;
+  unsigned* err = device_error_word();
+  if (!err) return RF_ERR_CUDA;
+  return from_cuda(launch_selftest_wait_timeout(timeout_us, err,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,307 @@
+// attn_fwd_bf16_tc.cu -- single-segment fused attention on the tcgen05 tensor
+// cores (bf16 in, fp32 accumulation and softmax state, bf16 out), d = 64.
+//
+// Safe-softmax cascade ([E] §2.2) in the single-loop incremental form ([E]
+// §2.3, §4.1; [S] Methodologie 2, single-segment strategy of Methodologie 3):
+// one CTA owns 128 query rows of one (batch, head) and walks all key tiles of
+// 128 once.  Per tile j:
+//   1. MMA warp:      S = Q K_j^T            (tcgen05 kind::f16, M=128, N=128,
+//                                            fp32 in tensor memory)
+//   2. softmax warps: one thread per query row reads its S row from TMEM,
+//                     m' = max(m, rowmax), alpha = 2^(m - m'),
+//                     P = 2^(S*c - m') (c = scale*log2 e), l' = alpha*l + sum P,
+//                     and writes P as bf16 into a 128-byte-swizzled K-major
+//                     shared tile (the A operand of the next MMA)
+//   3. MMA warp:      O_j = P V_j            (M=128, N=64, K=128; V is the
+//                                            MN-major B operand)
+//   4. softmax warps: o = alpha*o + O_j in registers.
+// After the last tile each thread writes o / l as bf16.  S and P never
+// leave the SM.  A TMA warp streams Q once and K/V tiles through a 2-stage
+// ring; every wait is bounded.
+#include <math.h>
+
+#include "rf_device.cuh"
+#include "rf_internal.h"
+
+namespace rf {
+namespace {
+
+constexpr int kD = 64;
+constexpr int BQ = 128, BKV = 128;
+constexpr int kKV = 2;                                // K/V ring depth
+constexpr int kTileBytes = 128 * kD * 2;              // 16 KB: 128 rows x 128 B
+constexpr int kQOff = 0;
+constexpr int kKOff = kQOff + kTileBytes;
+constexpr int kVOff = kKOff + kKV * kTileBytes;
+constexpr int kPOff = kVOff + kKV * kTileBytes;       // two 16 KB blocks (keys 0-63, 64-127)
+constexpr int kBarOff = kPOff + 2 * kTileBytes;
+constexpr int kSmem = kBarOff + 256;
+constexpr int kThreads = 192;                         // warp 0 TMA, 1 MMA, 2-5 softmax
+constexpr int kTmemCols = 256;                        // S: cols 0-127, O_j: cols 128-191
+constexpr uint32_t kIdescS = make_idesc(BQ, BKV, /*bf16*/ 1, 0, 0);
+constexpr uint32_t kIdescO = make_idesc(BQ, kD, /*bf16*/ 1, 0, /*V MN-major*/ 1);
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t kv_full[kKV];
+  uint64_t kv_empty[kKV];
+  uint64_t s_full;
+  uint64_t p_full;
+  uint64_t o_full;
+  uint64_t drain;
+  uint32_t tmem;
+  int abort;
+};
+
+__global__ void __launch_bounds__(kThreads, 2)
+    attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
+                         const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
+                         int Lq, int Lk, float c_log2, unsigned* err) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  Bars* bars = reinterpret_cast<Bars*>(smem + kBarOff);
+  volatile int* abort_flag = &bars->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = blockIdx.x;
+  const int64_t bh = blockIdx.y;
+  const int nkv = (Lk + BKV - 1) / BKV;
+  const int32_t q_row0 = (int32_t)(bh * Lq + (int64_t)qt * BQ);
+  const int32_t kv_row0 = (int32_t)(bh * Lk);
+
+  if ((smem_u32(smem) & 1023u) != 0) {   // swizzled tiles need 1 KB alignment
+    if (threadIdx.x == 0) raise_error(err, kDevErrTimeout);
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+    mbar_init(smem_u32(&bars->q_full), 1);
+    for (int i = 0; i < kKV; ++i) {
+      mbar_init(smem_u32(&bars->kv_full[i]), 1);
+      mbar_init(smem_u32(&bars->kv_empty[i]), 1);
+    }
+    mbar_init(smem_u32(&bars->s_full), 1);
+    mbar_init(smem_u32(&bars->p_full), BQ);
+    mbar_init(smem_u32(&bars->o_full), 1);
+    mbar_init(smem_u32(&bars->drain), 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&bars->tmem), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem;
+  const uint32_t tmem_s = tmem, tmem_o = tmem + BKV;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      const uint64_t pol_kv = policy_evict_last();   // K/V tiles are read by Lq/128 CTAs
+      mbar_arrive_expect_tx(smem_u32(&bars->q_full), kTileBytes);
+      tma_load_2d(smem_u32(smem + kQOff), &tmQ, smem_u32(&bars->q_full), 0, q_row0);
+      int j = 0;
+      for (; j < nkv; ++j) {
+        const int slot = j % kKV;
+        if (j >= kKV &&
+            !mbar_wait(smem_u32(&bars->kv_empty[slot]), (uint32_t)(((j / kKV) + 1) & 1))) {
+          raise_error(err, kDevErrTimeout);
+          *abort_flag = 1;
+          break;
+        }
+        if (*abort_flag) break;
+        const uint32_t bar = smem_u32(&bars->kv_full[slot]);
+        mbar_arrive_expect_tx(bar, 2 * kTileBytes);
+        tma_load_2d_hint(smem_u32(smem + kKOff + slot * kTileBytes), &tmK, bar, 0,
+                         kv_row0 + j * BKV, pol_kv);
+        tma_load_2d_hint(smem_u32(smem + kVOff + slot * kTileBytes), &tmV, bar, 0,
+                         kv_row0 + j * BKV, pol_kv);
+      }
+      if (*abort_flag) {
+        (void)mbar_wait(smem_u32(&bars->q_full), 0, 1000000ull);
+        for (int i = j - kKV < 0 ? 0 : j - kKV; i < j; ++i)
+          (void)mbar_wait(smem_u32(&bars->kv_full[i % kKV]), (uint32_t)((i / kKV) & 1),
+                          1000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      const uint32_t q_addr = smem_u32(smem + kQOff);
+      const uint32_t p_addr = smem_u32(smem + kPOff);
+      auto issue_s = [&](int j) -> bool {
+        const int slot = j % kKV;
+        if (!mbar_wait(smem_u32(&bars->kv_full[slot]), (uint32_t)((j / kKV) & 1))) return false;
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(smem + kKOff + slot * kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_bf16_ss(tmem_s, sw128_desc(q_addr + kk * 32, 1024, 16),
+                      sw128_desc(k_addr + kk * 32, 1024, 16), kIdescS, kk != 0);
+        mma_commit(smem_u32(&bars->s_full));
+        return true;
+      };
+      bool ok = mbar_wait(smem_u32(&bars->q_full), 0);
+      ok = ok && issue_s(0);
+      for (int j = 0; ok && j < nkv; ++j) {
+        const int slot = j % kKV;
+        if (!mbar_wait(smem_u32(&bars->p_full), (uint32_t)(j & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(smem + kVOff + slot * kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < BKV / 16; ++kk)
+          mma_bf16_ss(tmem_o,
+                      sw128_desc(p_addr + (kk >> 2) * kTileBytes + (kk & 3) * 32, 1024, 16),
+                      sw128_desc(v_addr + kk * 16 * 128, 1024, kTileBytes), kIdescO, kk != 0);
+        mma_commit(smem_u32(&bars->o_full));
+        mma_commit(smem_u32(&bars->kv_empty[slot]));
+        if (j + 1 < nkv && !issue_s(j + 1)) ok = false;
+      }
+      if (!ok) {
+        raise_error(err, kDevErrTimeout);
+        *abort_flag = 1;
+      }
+      // drain: nothing may still be running on the tensor core when TMEM and
+      // shared memory are released
+      mma_commit(smem_u32(&bars->drain));
+      (void)mbar_wait(smem_u32(&bars->drain), 0, 1000000000ull);
+    }
+  } else {
+    // ------------------------------------------------ softmax / epilogue
+    const int sub = warp & 3;
+    const int r = sub * 32 + lane;                     // query row within the tile
+    const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
+    uint8_t* prow = smem + kPOff + r * 128;
+    float o[kD];
+#pragma unroll
+    for (int i = 0; i < kD; ++i) o[i] = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+
+    for (int j = 0; j < nkv; ++j) {
+      if (!mbar_wait(smem_u32(&bars->s_full), (uint32_t)(j & 1)) || *abort_flag) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int valid = min(BKV, Lk - j * BKV);        // keys of this tile that exist
+      // pass 1: row max
+      float mx = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t v[32];
+        tmem_ld32(tmem_s + lane_off + q * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (q * 32 + i < valid) mx = fmaxf(mx, __uint_as_float(v[i]));
+      }
+      const float m_new = fmaxf(m_run, mx * c_log2);
+      const float alpha = ex2(m_run - m_new);          // 0 on the first tile
+      // pass 2: P = 2^(S c - m'), row sum, P -> swizzled bf16 tile
+      float psum = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t v[32];
+        tmem_ld32(tmem_s + lane_off + q * 32, v);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int c0 = q * 32 + 2 * i;
+          const float p0 = c0 < valid ? ex2(fmaf(__uint_as_float(v[2 * i]), c_log2, -m_new)) : 0.f;
+          const float p1 =
+              c0 + 1 < valid ? ex2(fmaf(__uint_as_float(v[2 * i + 1]), c_log2, -m_new)) : 0.f;
+          psum += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        // keys 32q..32q+31 = block q/2, 16-byte chunks (q%2)*4 .. +3
+        uint8_t* blk = prow + (q >> 1) * kTileBytes;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int chunk = (q & 1) * 4 + c;
+          *reinterpret_cast<uint4*>(blk + ((chunk ^ (r & 7)) << 4)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        }
+      }
+      l_run = l_run * alpha + psum;
+      m_run = m_new;
+      fence_proxy_async_smem();                        // P visible to the tensor core
+      tc_fence_before();                               // S reads ordered before the arrive
+      mbar_arrive(smem_u32(&bars->p_full));
+
+      if (!mbar_wait(smem_u32(&bars->o_full), (uint32_t)(j & 1)) || *abort_flag) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t v[32];
+        tmem_ld32(tmem_o + lane_off + h * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[h * 32 + i] = fmaf(o[h * 32 + i], alpha, __uint_as_float(v[i]));
+      }
+    }
+    if (!ok) {
+      raise_error(err, kDevErrTimeout);
+      *abort_flag = 1;
+    } else if (qt * BQ + r < Lq) {
+      const float inv = 1.f / l_run;
+      uint4* dst = reinterpret_cast<uint4*>(O + ((int64_t)q_row0 + r) * kD);
+#pragma unroll
+      for (int c = 0; c < kD / 8; ++c)
+        dst[c] = make_uint4(pack_bf16x2(o[8 * c] * inv, o[8 * c + 1] * inv),
+                            pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
+                            pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
+                            pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd_bf16_tc(const void* Q, const void* K, const void* V, void* O, int B,
+                                    int H, int Lq, int Lk, int d, float scale, unsigned* err,
+                                    cudaStream_t s) {
+  (void)d;
+  CUtensorMap tmQ, tmK, tmV;
+  const uint64_t q_rows = (uint64_t)B * H * Lq, kv_rows = (uint64_t)B * H * Lk;
+  if (!encode_tmap_2d(&tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Q, kD, q_rows, kD * 2, kD, BQ, true) ||
+      !encode_tmap_2d(&tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, kD, kv_rows, kD * 2, kD, BKV, true) ||
+      !encode_tmap_2d(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, kD, kv_rows, kD * 2, kD, BKV, true))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_bf16_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((Lq + BQ - 1) / BQ, B * H);
+  if (grid.y > 65535u) return cudaErrorInvalidValue;
+  const float c_log2 = scale * 1.4426950408889634f;
+  attn_fwd_bf16_kernel<<<grid, kThreads, kSmem, s>>>(tmQ, tmK, tmV, static_cast<__nv_bfloat16*>(O),
+                                                     Lq, Lk, c_log2, err);
+  return cudaGetLastError();
+}
+
+}  // namespace rf

@@ -1,0 +1,355 @@
+// decode_splitkv.cu -- multi-segment (split-KV) fused decode attention.
+//
+// Multi-segment strategy ([S] Methodologie 3; [E] §3.3 inter-block merge and
+// multi-kernel cooperation): the keys of every (batch, kv head) are cut into
+// S segments.  Kernel 1 (decode_partial_kernel) gives each segment to one
+// CTA, which runs the incremental safe-softmax loop ([E] §2.3, §4.1) over its
+// keys and writes the partial state (m, l, o) -- o unnormalised, m in log2
+// units -- for each of the G query heads that share the kv head.  Kernel 2
+// (decode_merge_kernel) combines the S partial states of every (batch, query
+// head): M = max m_j, L = sum l_j 2^(m_j - M), O = sum o_j 2^(m_j - M) / L.
+//
+// Data movement: K and V stream from HBM exactly once, by TMA into 128-byte
+// swizzled shared-memory tiles (chunks of 32 keys x 128 dims, two 64-dim
+// boxes each), one private ring of stages per warp.  The G (<= 8) query rows
+// of a kv head form the M = 16 side of mma.sync m16n8k16 bf16 tiles with fp32
+// accumulation: S = Q K^T, then O += P V with P rounded to bf16; the row max,
+// exp2 and sums stay in registers (quad shuffles).
+#include <math.h>
+
+#include "rf_device.cuh"
+#include "rf_internal.h"
+
+namespace rf {
+namespace {
+
+constexpr int kD = 128;          // head dim
+constexpr int kCK = 32;          // keys per chunk
+constexpr int kStages = 2;       // ring depth per warp
+constexpr int kWarps = 4;        // consumer warps per CTA
+constexpr int kBoxBytes = kCK * 128;             // one 64-dim box of kCK rows
+constexpr int kStageBytes = 4 * kBoxBytes;       // K box0, K box1, V box0, V box1
+constexpr int kSmemBytes = kWarps * kStages * kStageBytes + 1024 + 256;
+
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// Byte offset of 16-byte chunk c (0..15, i.e. dims 8c..8c+7) of key row r in
+// a K or V stage (two 64-dim boxes, each 128-byte swizzled).
+__device__ __forceinline__ uint32_t sw_off(int r, int c) {
+  return (uint32_t)((c >> 3) * kBoxBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+template <int G>
+__global__ void __launch_bounds__(kWarps * 32)
+    decode_partial_kernel(const __grid_constant__ CUtensorMap tmK,
+                          const __grid_constant__ CUtensorMap tmV,
+                          const __nv_bfloat16* __restrict__ Q, float* __restrict__ part_o,
+                          float* __restrict__ part_ml, int Hq, int Hkv, int Lk, int S,
+                          float qk_scale_log2, unsigned* err) {
+  static_assert(G >= 1 && G <= 8, "query heads per kv head");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * kStages * kStageBytes);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int seg = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int64_t lo = (int64_t)seg * Lk / S, hi = (int64_t)(seg + 1) * Lk / S;
+  const int nchunks = (int)((hi - lo + kCK - 1) / kCK);
+  const int64_t row_base = ((int64_t)b * Hkv + kvh) * Lk;   // first K/V row of this sequence
+
+  uint8_t* my_stage = smem + warp * kStages * kStageBytes;
+  uint64_t* my_full = bars + warp * kStages;
+  const int my_n = nchunks > warp ? (nchunks - warp + kWarps - 1) / kWarps : 0;
+
+  if (lane == 0) {
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+#pragma unroll
+    for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&my_full[i]), 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  auto issue = [&](int i) {   // chunk (warp + i * kWarps) into slot i % kStages
+    const int slot = i % kStages;
+    const int ci = warp + i * kWarps;
+    const int32_t row = (int32_t)(row_base + lo + (int64_t)ci * kCK);
+    const uint32_t dst = smem_u32(my_stage + slot * kStageBytes);
+    const uint32_t bar = smem_u32(&my_full[slot]);
+    mbar_arrive_expect_tx(bar, kStageBytes);
+    tma_load_2d(dst, &tmK, bar, 0, row);
+    tma_load_2d(dst + kBoxBytes, &tmK, bar, 64, row);
+    tma_load_2d(dst + 2 * kBoxBytes, &tmV, bar, 0, row);
+    tma_load_2d(dst + 3 * kBoxBytes, &tmV, bar, 64, row);
+  };
+  if (lane == 0)
+    for (int i = 0; i < kStages && i < my_n; ++i) issue(i);
+
+  // Q as the A operand (rows = the G query heads, zero-padded to 16).
+  const int hrow = lane >> 2;           // head of this lane's accumulator rows
+  const int kq = (lane & 3) * 2;        // first of this lane's two columns
+  uint32_t qa[8][2];
+  {
+    const uint32_t* qp = reinterpret_cast<const uint32_t*>(
+        Q + ((int64_t)b * Hq + (int64_t)kvh * G + (hrow < G ? hrow : 0)) * kD);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      qa[ks][0] = hrow < G ? qp[(ks * 16 + kq) >> 1] : 0u;
+      qa[ks][1] = hrow < G ? qp[(ks * 16 + kq + 8) >> 1] : 0u;
+    }
+  }
+
+  float oacc[16][4];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.f;
+  float m_run = -INFINITY, l_run = 0.f;
+  bool failed = false;
+
+  // ldmatrix lane roles: matrix mi = lane / 8, row lane % 8 of that matrix.
+  const int mi = lane >> 3, mr = lane & 7;
+
+  int fail_at = -1;
+  for (int i = 0; i < my_n; ++i) {
+    const int slot = i % kStages;
+    bool ok = mbar_wait(smem_u32(&my_full[slot]), (uint32_t)((i / kStages) & 1));
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) {
+      failed = true;
+      fail_at = i;
+      break;
+    }
+    const uint32_t kbase = smem_u32(my_stage + slot * kStageBytes);
+    const uint32_t vbase = kbase + 2 * kBoxBytes;
+    const int64_t key0 = lo + (int64_t)(warp + i * kWarps) * kCK;   // first key of the chunk
+
+    // ---- S = Q K^T for 32 keys: two 16-key sub-blocks x two 8-key n-blocks
+    float s[2][2][4];
+#pragma unroll
+    for (int sb = 0; sb < 2; ++sb) {
+      s[sb][0][0] = s[sb][0][1] = s[sb][0][2] = s[sb][0][3] = 0.f;
+      s[sb][1][0] = s[sb][1][1] = s[sb][1][2] = s[sb][1][3] = 0.f;
+      const int krow = sb * 16 + (mi >> 1) * 8 + mr;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4(kbase + sw_off(krow, 2 * ks + (mi & 1)), r0, r1, r2, r3);
+        const uint32_t a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
+        mma16816(s[sb][0], a, r0, r1);
+        mma16816(s[sb][1], a, r2, r3);
+      }
+    }
+
+    // ---- online softmax for head hrow over this chunk (log2 domain)
+    float mx = -INFINITY;
+#pragma unroll
+    for (int sb = 0; sb < 2; ++sb)
+#pragma unroll
+      for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int64_t key = key0 + sb * 16 + nb * 8 + kq + e;
+          const float v = key < hi ? s[sb][nb][e] * qk_scale_log2 : -INFINITY;
+          s[sb][nb][e] = v;
+          mx = fmaxf(mx, v);
+        }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float m_new = fmaxf(m_run, mx);          // finite: every chunk has a valid key
+    const float alpha = exp2f(m_run - m_new);      // 0 on the first chunk
+    float psum = 0.f;
+    uint32_t pa[2][2];
+#pragma unroll
+    for (int sb = 0; sb < 2; ++sb)
+#pragma unroll
+      for (int nb = 0; nb < 2; ++nb) {
+        const float p0 = exp2f(s[sb][nb][0] - m_new);
+        const float p1 = exp2f(s[sb][nb][1] - m_new);
+        psum += p0 + p1;
+        pa[sb][nb] = pack_bf16x2(p0, p1);
+      }
+    l_run = l_run * alpha + psum;
+    m_run = m_new;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      oacc[j][0] *= alpha;
+      oacc[j][1] *= alpha;
+    }
+
+    // ---- O += P V: A = P (16 rows x 16 keys), B = V (16 keys x 8 dims)
+#pragma unroll
+    for (int sb = 0; sb < 2; ++sb) {
+      const uint32_t a[4] = {pa[sb][0], 0u, pa[sb][1], 0u};
+      const int vrow = sb * 16 + (mi & 1) * 8 + mr;
+#pragma unroll
+      for (int j = 0; j < 16; j += 2) {
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4_t(vbase + sw_off(vrow, j + (mi >> 1)), r0, r1, r2, r3);
+        mma16816(oacc[j], a, r0, r1);
+        mma16816(oacc[j + 1], a, r2, r3);
+      }
+    }
+
+    __syncwarp();
+    if (lane == 0 && i + kStages < my_n) issue(i + kStages);
+  }
+
+  if (failed) {
+    raise_error(err, kDevErrTimeout);
+    // Chunks fail_at .. min(fail_at + kStages, my_n) - 1 were issued but not
+    // consumed: give their copies a bounded chance to land before the CTA's
+    // shared memory is released.
+    if (lane == 0)
+      for (int c = fail_at; c < fail_at + kStages && c < my_n; ++c)
+        (void)mbar_wait(smem_u32(&my_full[c % kStages]), (uint32_t)((c / kStages) & 1), 1000000ull);
+  }
+
+  // ---- combine the warps' states, then write the segment's partial state
+  l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+  l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+  __syncthreads();                                  // all stages consumed
+  float* wo = reinterpret_cast<float*>(smem);       // [kWarps][G][kD]
+  float* wm = wo + kWarps * G * kD;                 // [kWarps][G]
+  float* wl = wm + kWarps * G;                      // [kWarps][G]
+  if (hrow < G) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      wo[(warp * G + hrow) * kD + j * 8 + kq] = oacc[j][0];
+      wo[(warp * G + hrow) * kD + j * 8 + kq + 1] = oacc[j][1];
+    }
+    if ((lane & 3) == 0) {
+      wm[warp * G + hrow] = m_run;
+      wl[warp * G + hrow] = l_run;
+    }
+  }
+  __syncthreads();
+  for (int t = threadIdx.x; t < G * kD; t += kWarps * 32) {
+    const int h = t / kD, dim = t % kD;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * G + h]);
+    float o = 0.f, L = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float sc = exp2f(wm[w * G + h] - M);   // 0 for warps without keys
+        o += wo[(w * G + h) * kD + dim] * sc;
+        L += wl[w * G + h] * sc;
+      }
+    }
+    const int64_t pidx = ((int64_t)b * Hq + (int64_t)kvh * G + h) * S + seg;
+    part_o[pidx * kD + dim] = o;
+    if (dim == 0) {
+      part_ml[pidx * 2] = M;
+      part_ml[pidx * 2 + 1] = L;
+    }
+  }
+}
+
+// One CTA per (batch, query head): merge the S partial states.
+__global__ void __launch_bounds__(kD)
+    decode_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
+                        __nv_bfloat16* __restrict__ O, int S) {
+  const int64_t bh = blockIdx.x;
+  const int dim = threadIdx.x;
+  const float* ml = part_ml + bh * S * 2;
+  float M = -INFINITY;
+  for (int j = 0; j < S; ++j) M = fmaxf(M, ml[2 * j]);
+  float L = 0.f, o = 0.f;
+  for (int j = 0; j < S; ++j) {
+    const float mj = ml[2 * j];
+    if (mj == -INFINITY) continue;                 // empty segment
+    const float w = exp2f(mj - M);
+    L += ml[2 * j + 1] * w;
+    o += part_o[(bh * S + j) * kD + dim] * w;
+  }
+  O[bh * kD + dim] = __float2bfloat16_rn(o / L);
+}
+
+template <int G>
+cudaError_t launch_g(const CUtensorMap& tmK, const CUtensorMap& tmV, const void* Q, void* O,
+                     int B, int Hq, int Hkv, int Lk, float scale, int S, float* part_o,
+                     float* part_ml, unsigned* err, cudaStream_t s) {
+  auto kern = decode_partial_kernel<G>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSmemBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid(S, Hkv, B);
+  const float qk_scale_log2 = scale * 1.4426950408889634f;
+  kern<<<grid, kWarps * 32, kSmemBytes, s>>>(tmK, tmV, static_cast<const __nv_bfloat16*>(Q),
+                                             part_o, part_ml, Hq, Hkv, Lk, S, qk_scale_log2, err);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  decode_merge_kernel<<<B * Hq, kD, 0, s>>>(part_o, part_ml, static_cast<__nv_bfloat16*>(O), S);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int decode_num_splits(int B, int Hq, int Hkv, int Lk, int d, int requested) {
+  (void)Hq;
+  (void)d;
+  if (requested > 0) return requested;
+  const int sms = sm_count();
+  if (sms <= 0) return 0;
+  // Aim for about four CTAs per SM in total while keeping segments at least
+  // 256 keys long (eight chunks, two per warp).
+  const int64_t pairs = (int64_t)B * Hkv;
+  int64_t S = (4 * (int64_t)sms + pairs - 1) / pairs;
+  const int64_t max_by_len = (Lk + 255) / 256;
+  if (S > max_by_len) S = max_by_len;
+  if (S < 1) S = 1;
+  if (S > 65535) S = 65535;
+  return (int)S;
+}
+
+size_t decode_workspace_bytes(int B, int Hq, int d, int S) {
+  const size_t n = (size_t)B * Hq * S;
+  const size_t o_bytes = (n * d * sizeof(float) + 255) & ~(size_t)255;
+  return o_bytes + n * 2 * sizeof(float);
+}
+
+cudaError_t launch_decode_splitkv(const void* Q, const void* K, const void* V, void* O, int B,
+                                  int Hq, int Hkv, int Lk, int d, float scale, int S,
+                                  void* workspace, unsigned* err, cudaStream_t s) {
+  if (S > 65535 || Hkv > 65535 || B > 65535) return cudaErrorInvalidValue;
+  const uint64_t rows = (uint64_t)B * Hkv * Lk;
+  CUtensorMap tmK, tmV;
+  if (!encode_tmap_2d(&tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, kD, rows, kD * 2, 64, kCK, true) ||
+      !encode_tmap_2d(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, kD, rows, kD * 2, 64, kCK, true))
+    return cudaErrorInvalidValue;
+  const size_t n = (size_t)B * Hq * S;
+  float* part_o = static_cast<float*>(workspace);
+  float* part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                            ((n * d * sizeof(float) + 255) & ~(size_t)255));
+  switch (Hq / Hkv) {
+    case 1: return launch_g<1>(tmK, tmV, Q, O, B, Hq, Hkv, Lk, scale, S, part_o, part_ml, err, s);
+    case 2: return launch_g<2>(tmK, tmV, Q, O, B, Hq, Hkv, Lk, scale, S, part_o, part_ml, err, s);
+    case 4: return launch_g<4>(tmK, tmV, Q, O, B, Hq, Hkv, Lk, scale, S, part_o, part_ml, err, s);
+    case 8: return launch_g<8>(tmK, tmV, Q, O, B, Hq, Hkv, Lk, scale, S, part_o, part_ml, err, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace rf

@@ -1,0 +1,320 @@
+// moe_gate.cu -- fused MoE gate: scores = x . W_gate^T -> top-k -> softmax of
+// the selected scores ([E] §4.2), one kernel, no score matrix in HBM.
+//
+// Each CTA owns 128 tokens and one slice of the reduction dimension D; the
+// CTAs covering the slices of the same 128 tokens form a thread-block
+// cluster (split-K).  Per CTA: a TMA producer warp streams 128x64 tiles of x
+// and 64x64 tiles of W_gate (both K-major, 128-byte swizzled) through a
+// 4-stage ring; one thread issues tcgen05.mma kind::f16 (bf16 x bf16 -> fp32,
+// M=128, N=64 experts) into tensor memory.  The epilogue warps copy the
+// partial 128x64 score tile from TMEM to shared memory; after a cluster
+// barrier each CTA sums one quarter of the rows over all cluster peers
+// through distributed shared memory, then one thread per token selects the
+// top k (descending score, ties to the lower expert index) and computes the
+// softmax over the k selected scores.
+#include <math.h>
+
+#include "rf_device.cuh"
+#include "rf_internal.h"
+
+namespace rf {
+namespace {
+
+constexpr int BM = 128;            // tokens per CTA
+constexpr int kE = 64;             // experts (MMA N)
+constexpr int BK = 64;             // bf16 elements per k-block (128 bytes)
+constexpr int kStages = 4;
+constexpr int kABytes = BM * BK * 2, kBBytes = kE * BK * 2, kStageBytes = kABytes + kBBytes;
+constexpr int kThreads = 192;      // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kTmemCols = 64;
+constexpr int kRedStride = kE + 4;  // padded fp32 row of the partial-score tile
+constexpr int kSmem = kStages * kStageBytes + 1024 + 256;
+constexpr uint32_t kIdesc = make_idesc(BM, kE, /*bf16*/ 1, 0, 0);
+
+static_assert(2 * BM * kRedStride * 4 <= kStages * kStageBytes, "both score tiles fit in the ring");
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+__device__ __forceinline__ uint32_t map_peer(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float4 ld_peer_v4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// Top-KT of a 64-score row: a sorted insertion scan in expert order.  A new
+// score displaces an entry only when strictly greater, so among equal scores
+// the lower expert index stays ahead.
+template <int KT>
+__device__ __forceinline__ void topk_softmax_row(const float* srow, int32_t* idx_out,
+                                                 float* w_out) {
+  float v[KT];
+  int ix[KT];
+#pragma unroll
+  for (int j = 0; j < KT; ++j) {
+    v[j] = -INFINITY;
+    ix[j] = 0;
+  }
+#pragma unroll 4
+  for (int e = 0; e < kE; ++e) {
+    float cv = srow[e];
+    int ce = e;
+#pragma unroll
+    for (int j = 0; j < KT; ++j) {
+      if (cv > v[j]) {
+        const float tv = v[j];
+        const int te = ix[j];
+        v[j] = cv;
+        ix[j] = ce;
+        cv = tv;
+        ce = te;
+      }
+    }
+  }
+  // softmax over the selected scores (v[0] is their max)
+  float ex[KT], sum = 0.f;
+#pragma unroll
+  for (int j = 0; j < KT; ++j) {
+    ex[j] = expf(v[j] - v[0]);
+    sum += ex[j];
+  }
+#pragma unroll
+  for (int j = 0; j < KT; ++j) {
+    idx_out[j] = ix[j];
+    w_out[j] = ex[j] / sum;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_gate_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                    int T, int D, int k, int kb_per_cta, int32_t* __restrict__ idx_out,
+                    float* __restrict__ w_out, unsigned* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* accum = empty + kStages;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(accum + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  float* red = reinterpret_cast<float*>(smem);     // [BM][kRedStride], reuses the ring
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_rank(), csize = cluster_size();
+  const int m0 = blockIdx.y * BM;
+  const int nkb_total = (D + BK - 1) / BK;
+  const int kb0 = (int)crank * kb_per_cta;
+  int nk = nkb_total - kb0;
+  nk = nk < 0 ? 0 : (nk > kb_per_cta ? kb_per_cta : nk);
+
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmX);
+    prefetch_tmap(&tmW);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(smem_u32(&full[i]), 1);
+      mbar_init(smem_u32(&empty[i]), 1);
+    }
+    mbar_init(smem_u32(accum), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol_x = policy_evict_first();   // x is streamed once
+      const uint64_t pol_w = policy_evict_last();    // W_gate is re-read by every token tile
+      int i = 0;
+      for (; i < nk; ++i) {
+        const int slot = i % kStages;
+        if (i >= kStages &&
+            !mbar_wait(smem_u32(&empty[slot]), (uint32_t)(((i / kStages) + 1) & 1))) {
+          raise_error(err, kDevErrTimeout);
+          *abort_flag = 1;
+          break;
+        }
+        if (*abort_flag) break;
+        uint8_t* a = smem + slot * kStageBytes;
+        const uint32_t bar = smem_u32(&full[slot]);
+        mbar_arrive_expect_tx(bar, kStageBytes);
+        tma_load_2d_hint(smem_u32(a), &tmX, bar, (kb0 + i) * BK, m0, pol_x);
+        tma_load_2d_hint(smem_u32(a + kABytes), &tmW, bar, (kb0 + i) * BK, 0, pol_w);
+      }
+      if (*abort_flag)
+        for (int j = i - kStages < 0 ? 0 : i - kStages; j < i; ++j)
+          (void)mbar_wait(smem_u32(&full[j % kStages]), (uint32_t)((j / kStages) & 1), 1000000ull);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      for (int i = 0; i < nk; ++i) {
+        const int slot = i % kStages;
+        if (!mbar_wait(smem_u32(&full[slot]), (uint32_t)((i / kStages) & 1))) {
+          raise_error(err, kDevErrTimeout);
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a = smem_u32(smem + slot * kStageBytes);
+        const uint32_t b = a + kABytes;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          mma_bf16_ss(tmem, sw128_desc(a + kk * 32, 1024, 16), sw128_desc(b + kk * 32, 1024, 16),
+                      kIdesc, (i | kk) != 0);
+        mma_commit(smem_u32(&empty[slot]));
+      }
+      mma_commit(smem_u32(accum));
+    }
+  } else {
+    // partial scores: TMEM -> padded shared tile (row = token)
+    const int sub = warp & 3;
+    const int r = sub * 32 + lane;
+    if (!mbar_wait(smem_u32(accum), 0)) {
+      raise_error(err, kDevErrTimeout);
+      *abort_flag = 1;
+    }
+    tc_fence_after();
+#pragma unroll
+    for (int c0 = 0; c0 < kE; c0 += 32) {
+      uint32_t v[32];
+      tmem_ld32(tmem + ((uint32_t)(sub * 32) << 16) + c0, v);
+      tmem_ld_wait();
+      float4* dst = reinterpret_cast<float4*>(red + r * kRedStride + c0);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float4 f;
+        f.x = nk > 0 ? __uint_as_float(v[4 * q]) : 0.f;
+        f.y = nk > 0 ? __uint_as_float(v[4 * q + 1]) : 0.f;
+        f.z = nk > 0 ? __uint_as_float(v[4 * q + 2]) : 0.f;
+        f.w = nk > 0 ? __uint_as_float(v[4 * q + 3]) : 0.f;
+        dst[q] = f;
+      }
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync_all();        // every peer's partial tile is complete and visible
+
+  // Split-K reduction: this CTA finalises rows [r_lo, r_hi) of the 128, summing
+  // them over every cluster peer's partial tile into a second local tile.
+  float* red2 = red + BM * kRedStride;
+  const int rows_per = (BM + (int)csize - 1) / (int)csize;
+  const int r_lo = (int)crank * rows_per;
+  const int r_hi = min(BM, r_lo + rows_per);
+  if (warp >= 2) {
+    const int t = threadIdx.x - 64;           // 4 threads per row, 16 experts each
+    const int q16 = (t & 3) * 16;
+    for (int row = r_lo + (t >> 2); row < r_hi; row += 32) {
+      float4 acc[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      const uint32_t local = smem_u32(red + row * kRedStride + q16);
+      for (uint32_t p = 0; p < csize; ++p) {
+        const uint32_t raddr = map_peer(local, p);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 f = ld_peer_v4(raddr + q * 16);
+          acc[q].x += f.x;
+          acc[q].y += f.y;
+          acc[q].z += f.z;
+          acc[q].w += f.w;
+        }
+      }
+      float4* dst = reinterpret_cast<float4*>(red2 + row * kRedStride + q16);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dst[q] = acc[q];
+    }
+  }
+  __syncthreads();
+  if (warp >= 2 && !*abort_flag) {
+    const int row = r_lo + (threadIdx.x - 64);
+    const int tok = m0 + row;
+    if (row < r_hi && tok < T) {
+      const float* srow = red2 + row * kRedStride;
+      int32_t* io = idx_out + (size_t)tok * k;
+      float* wo = w_out + (size_t)tok * k;
+      switch (k) {
+        case 1: topk_softmax_row<1>(srow, io, wo); break;
+        case 2: topk_softmax_row<2>(srow, io, wo); break;
+        case 3: topk_softmax_row<3>(srow, io, wo); break;
+        case 4: topk_softmax_row<4>(srow, io, wo); break;
+        case 5: topk_softmax_row<5>(srow, io, wo); break;
+        case 6: topk_softmax_row<6>(srow, io, wo); break;
+        case 7: topk_softmax_row<7>(srow, io, wo); break;
+        default: topk_softmax_row<8>(srow, io, wo); break;
+      }
+    }
+  }
+  cluster_sync_all();        // no peer reads this CTA's tile any more
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_moe_gate(const void* X, const void* Wg, int T, int D, int E, int k,
+                            int32_t* idx, float* w, unsigned* err, cudaStream_t s) {
+  (void)E;
+  CUtensorMap tmX, tmW;
+  if (!encode_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)D, (uint64_t)T,
+                      (uint64_t)D * 2, BK, BM, true) ||
+      !encode_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Wg, (uint64_t)D, (uint64_t)kE,
+                      (uint64_t)D * 2, BK, kE, true))
+    return cudaErrorInvalidValue;
+  // split the reduction over a cluster of up to 4 CTAs, keeping >= 8 k-blocks each
+  const int nkb = (D + BK - 1) / BK;
+  int cs = nkb / 8;
+  cs = cs < 1 ? 1 : (cs > 4 ? 4 : cs);
+  const int kb_per = (nkb + cs - 1) / cs;
+  const int tiles = (T + BM - 1) / BM;
+  if (tiles > 65535) return cudaErrorInvalidValue;
+
+  cudaError_t e = cudaFuncSetAttribute(moe_gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs, tiles, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, moe_gate_kernel, tmX, tmW, T, D, k, kb_per, idx, w, err);
+}
+
+}  // namespace rf

@@ -1,0 +1,54 @@
+// rf_internal.h -- host-side declarations shared by the library's translation
+// units (launchers called from api.cu after argument validation).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/rf.h"
+
+namespace rf {
+
+// Device address of the per-device error word (set up once per device).
+// Returns nullptr if the address could not be obtained.
+unsigned* device_error_word();
+
+// SM count of the current device (cached per device).
+int sm_count();
+
+// Encodes a 2-D tiled tensor map: inner dimension `inner` elements (contiguous),
+// `outer` rows with a row pitch of `row_bytes`; box = box_inner x box_outer;
+// 128-byte swizzle when swizzle128 is set.  Returns false on failure.
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                    uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
+                    uint32_t box_outer, bool swizzle128);
+
+// ---------------------------------------------------------------- launchers
+// Each returns cudaSuccess or the launch error.  Arguments are pre-validated.
+
+cudaError_t launch_attn_fwd_f32(const float* Q, const float* K, const float* V, float* O, int B,
+                                int H, int Lq, int Lk, int d, float scale, cudaStream_t s);
+
+cudaError_t launch_attn_fwd_bf16_tc(const void* Q, const void* K, const void* V, void* O, int B,
+                                    int H, int Lq, int Lk, int d, float scale, unsigned* err,
+                                    cudaStream_t s);
+
+int decode_num_splits(int B, int Hq, int Hkv, int Lk, int d, int requested);
+size_t decode_workspace_bytes(int B, int Hq, int d, int S);
+cudaError_t launch_decode_splitkv(const void* Q, const void* K, const void* V, void* O, int B,
+                                  int Hq, int Hkv, int Lk, int d, float scale, int S,
+                                  void* workspace, unsigned* err, cudaStream_t s);
+
+cudaError_t launch_moe_gate(const void* X, const void* Wg, int T, int D, int E, int k,
+                            int32_t* idx, float* w, unsigned* err, cudaStream_t s);
+
+size_t fp8_workspace_bytes(int M, int N, int K);
+cudaError_t launch_absmax_fp8_gemm(const void* X, const uint8_t* Wq, const float* sw, void* Y,
+                                   int M, int N, int K, float* sx, uint8_t* xq, unsigned* err,
+                                   cudaStream_t s);
+
+cudaError_t launch_selftest_wait_timeout(int timeout_us, unsigned* err, cudaStream_t s);
+
+}  // namespace rf

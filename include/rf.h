@@ -1,0 +1,190 @@
+/*
+ * rf.h -- C ABI of the fused cascaded-reduction kernels for GB300 (sm_103a).
+ *
+ * A cascaded reduction is a chain of reductions in which each step needs the
+ * result of the previous one (safe softmax: max, then sum of exp(x - max),
+ * then the weighted sum with V).  The kernels behind this header run each
+ * chain as one pass over its input, keeping a small running state on chip
+ * and rescaling it as each tile arrives ("incremental computation form").
+ *
+ * Sources of the operations (cited by title and section):
+ *  [A] "RedFuser: An Automatic Operator Fusion Framework for Cascaded
+ *      Reductions on AI Accelerators", ASPLOS 2026, abstract.
+ *  [E] "RedFuser框架：AI加速器中的算子融合技术解析" (explainer article),
+ *      §2.2 softmax cascade, §2.3 incremental form, §3.3 execution hierarchy,
+ *      §4.1 fused attention, §4.2 MoE routing, §4.3 FP8 quantised GEMM.
+ *  [S] gist.science technical summary of [A], "Methodologie" 1-3
+ *      (fusion conditions, incremental form, single-/multi-segment code).
+ *
+ * Conventions for every entry point:
+ *  - Tensor arguments are DEVICE pointers on the current CUDA device, owned
+ *    by the caller; the library never allocates, frees or synchronises
+ *    (except rf_get_device_status, which synchronises the given stream).
+ *  - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default).
+ *  - Layouts are dense row-major (C order) with the shapes given.
+ *  - Pointers must be 16-byte aligned.
+ *  - Arguments are validated on the host before anything is launched; a bad
+ *    argument returns an error code and enqueues nothing.  Launch failures
+ *    return RF_ERR_CUDA.  Asynchronous device-side problems (a bounded wait
+ *    that ran out) are reported by rf_get_device_status.
+ *  - The functions are reentrant; calls on one stream execute in order, and
+ *    concurrent calls on different streams must not share output buffers
+ *    or workspaces.
+ */
+#ifndef RF_H_
+#define RF_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* rf_stream_t;
+
+typedef enum {
+  RF_OK = 0,
+  RF_ERR_INVALID_ARG = 1,     /* null / misaligned pointer, bad size       */
+  RF_ERR_UNSUPPORTED = 2,     /* valid request this build does not cover    */
+  RF_ERR_WORKSPACE = 3,       /* workspace missing or too small             */
+  RF_ERR_CUDA = 4,            /* a CUDA runtime call or launch failed       */
+  RF_ERR_DEVICE_TIMEOUT = 5   /* a kernel's bounded wait ran out            */
+} rf_status;
+
+typedef enum { RF_F32 = 0, RF_BF16 = 1 } rf_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* rf_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int rf_version(void);
+
+/*
+ * Synchronises `stream`, then reads and clears the device-side error word of
+ * the current device.  Returns RF_OK, RF_ERR_DEVICE_TIMEOUT (some kernel gave
+ * up on a bounded wait and returned early; its outputs are incomplete) or
+ * RF_ERR_CUDA (the synchronisation itself failed).
+ */
+rf_status rf_get_device_status(rf_stream_t stream);
+
+/*
+ * Single-segment fused attention ([E] §2.2, §4.1; [S] Methodologie 2 and the
+ * single-segment strategy of Methodologie 3): for every (b, h, query row),
+ *     s_j = scale * q . k_j,  m = max_j s_j,  l = sum_j exp(s_j - m),
+ *     o   = sum_j exp(s_j - m) / l * v_j,
+ * computed by one CTA per block of query rows in a single loop over key
+ * tiles with the running (m, l, o) rescaled per tile; S and P never reach
+ * global memory.
+ *   dtype   RF_F32: Q/K/V/O fp32, exact-fp32 SIMT path (no tensor cores).
+ *           RF_BF16: Q/K/V/O bf16, tcgen05 tensor-core path, fp32
+ *           accumulation and softmax state, P rounded to bf16 for P.V.
+ *   Q, O    [B][H][Lq][d];  K, V  [B][H][Lk][d]  (multi-head: one K/V head
+ *           per query head).
+ *   Sizes   B, H, Lq, Lk >= 1 (B*H*Lq and B*H*Lk below 2^31);
+ *           d = 64 (both dtypes) or 128 (RF_F32 only).
+ *   scale   finite and > 0 (the usual 1/sqrt(d)).
+ *   causal  must be 0 (the cascade as defined has no mask).
+ * Errors: RF_ERR_INVALID_ARG (null/misaligned pointer, size < 1, causal != 0,
+ * bad dtype), RF_ERR_UNSUPPORTED (d not covered), RF_ERR_CUDA.
+ */
+rf_status rf_attn_fwd(int dtype, const void* Q, const void* K, const void* V, void* O,
+                      int B, int H, int Lq, int Lk, int d, float scale, int causal,
+                      rf_stream_t stream);
+
+/*
+ * Number of key segments rf_attn_decode_splitkv uses for this shape when its
+ * num_splits argument is `num_splits` (0 = automatic choice, which sizes the
+ * grid of the partial kernel to the device's SM count).  Returns 0 for an
+ * invalid shape.
+ */
+int rf_attn_decode_splitkv_num_splits(int B, int Hq, int Hkv, int Lk, int d, int num_splits);
+
+/* Workspace bytes rf_attn_decode_splitkv needs for the same arguments. */
+size_t rf_attn_decode_splitkv_workspace_size(int B, int Hq, int Hkv, int Lk, int d,
+                                             int num_splits);
+
+/*
+ * Multi-segment (split-KV) fused decode attention ([S] Methodologie 3,
+ * multi-segment strategy; [E] §3.3 inter-block merge and multi-kernel
+ * cooperation).  One query token per (b, query head):
+ *   Q   [B][Hq][d] bf16;  K, V  [B][Hkv][Lk][d] bf16;  O  [B][Hq][d] bf16.
+ * Grouped-query attention: query head hq reads K/V head hq / (Hq / Hkv).
+ * Kernel 1 splits each (b, kv head) sequence into S key segments and writes,
+ * per (b, hq, segment), the partial state (m, l, o) with o unnormalised
+ * (m in log2 units); kernel 2 merges them: M = max m_j,
+ * L = sum l_j 2^(m_j - M), O = sum o_j 2^(m_j - M) / L.
+ *   Sizes   B, Lk >= 1; d = 128; Hq / Hkv in {1, 2, 4, 8}; scale finite, > 0.
+ *   num_splits  0 = automatic, else 1..Lk segments.
+ *   workspace   device buffer of at least
+ *               rf_attn_decode_splitkv_workspace_size(...) bytes, 16-byte
+ *               aligned, owned by the caller; holds the partial states
+ *               between the two kernels (contents on return unspecified).
+ * Errors: RF_ERR_INVALID_ARG, RF_ERR_UNSUPPORTED, RF_ERR_WORKSPACE, RF_ERR_CUDA.
+ */
+rf_status rf_attn_decode_splitkv(const void* Q, const void* K, const void* V, void* O,
+                                 int B, int Hq, int Hkv, int Lk, int d, float scale,
+                                 int num_splits, void* workspace, size_t workspace_bytes,
+                                 rf_stream_t stream);
+
+/*
+ * Fused MoE gate ([E] §4.2): scores = x . W_gate^T, top-k experts per token,
+ * softmax over the k selected scores; the score matrix never reaches
+ * global memory.
+ *   X      [T][D] bf16 (token activations).
+ *   Wg     [E][D] bf16 (gate weight, expert-major: a linear layer's weight).
+ *   idx    [T][k] int32 out: selected experts by descending score, equal
+ *          scores by ascending expert index.
+ *   w      [T][k] fp32 out: softmax of the selected scores (same order).
+ *   Sizes  T >= 1; D >= 1 with D % 8 == 0; E = 64; 1 <= k <= 8.
+ * Scores are accumulated in fp32 on the tensor cores (exact when every
+ * partial sum is an integer below 2^24, e.g. small-integer inputs).
+ * Errors: RF_ERR_INVALID_ARG, RF_ERR_UNSUPPORTED, RF_ERR_CUDA.
+ */
+rf_status rf_moe_gate_topk_softmax(const void* X, const void* Wg, int T, int D, int E, int k,
+                                   int32_t* idx, float* w, rf_stream_t stream);
+
+/* Workspace bytes rf_absmax_fp8_gemm needs (0 for an invalid shape). */
+size_t rf_absmax_fp8_gemm_workspace_size(int M, int N, int K);
+
+/*
+ * Dynamic FP8 quantised GEMM ([E] §4.3), read per row of X:
+ *   sx[m]    = fp32(max_k |X[m,k]| / 448)                     (row absmax)
+ *   Xq[m,k]  = E4M3(fp32(X[m,k] / sx[m])), round-to-nearest-even,
+ *              saturating to +-448; rows with sx = 0 give code 0x00
+ *   Y[m,n]   = bf16( (sum_k Xq[m,k] * Wq[n,k]) * sx[m] * sw[n] )
+ * The division is an IEEE fp32 division; the sum is accumulated in fp32 on
+ * the tensor cores (tcgen05 kind::f8f6f4); Y is rounded to nearest even.
+ * Kernel 1 reads each row of X once (absmax and quantisation from
+ * registers); kernel 2 is the FP8 GEMM with the dequantising epilogue.
+ *   X       [M][K] bf16.
+ *   Wq      [N][K] uint8 E4M3 codes (pre-quantised weight; K contiguous).
+ *   sw      [N] fp32 per-output-column weight scales.
+ *   Y       [M][N] bf16 out.
+ *   sx_out  [M] fp32 out, or NULL (then kept in the workspace).
+ *   xq_out  [M][K] uint8 out, or NULL (then kept in the workspace).
+ *   workspace  device buffer of rf_absmax_fp8_gemm_workspace_size(M,N,K)
+ *              bytes, 16-byte aligned; may be NULL with 0 bytes when both
+ *              sx_out and xq_out are given.
+ *   Sizes   M, N >= 1; K >= 16 with K % 16 == 0.
+ * Errors: RF_ERR_INVALID_ARG, RF_ERR_WORKSPACE, RF_ERR_CUDA.
+ */
+rf_status rf_absmax_fp8_gemm(const void* X, const uint8_t* Wq, const float* sw, void* Y,
+                             int M, int N, int K, float* sx_out, uint8_t* xq_out,
+                             void* workspace, size_t workspace_bytes, rf_stream_t stream);
+
+/*
+ * Failure-detection self-test (no counterpart in the paper).  Launches one
+ * CTA that waits on an mbarrier nothing ever completes, with a wait limit of
+ * `timeout_us` microseconds (1..1000000).  The kernel gives up, records
+ * RF_ERR_DEVICE_TIMEOUT in the device error word and returns, leaving the
+ * context usable; rf_get_device_status then reports it.
+ */
+rf_status rf_selftest_wait_timeout(int timeout_us, rf_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RF_H_ */

@@ -1,0 +1,64 @@
+"""Shared comparison helpers and tolerances for the GPU parity tests.
+
+Tolerances (written here once, used by every parity test):
+* bf16 in / fp32 accumulation / bf16 out (prefill, decode): elementwise
+  max-abs error <= 2e-2 and relative L2 error <= 5e-3 against the fp64
+  oracle.  Sources of error: bf16 P (2^-9 relative per weight), fp32
+  accumulation, bf16 output rounding (2^-9 relative).
+* fp32 tiny attention: relative L2 <= 1e-5 and
+  |O - O_ref| <= 1e-5 * max(1, |O_ref|) elementwise.
+* FP8 GEMM output Y (magnitudes up to ~1e3, where one bf16 ulp is 4 or
+  more): |Y - Y_ref| <= 2e-2 * max(1, |Y_ref|) elementwise and relative
+  L2 <= 5e-3.
+* MoE weights: the scores are exact integers, so the weights differ only
+  by fp32 exp/divide rounding: |w - w_ref| <= 1e-6.
+* Integer and byte outputs (top-k indices, E4M3 codes) and the fp32 row
+  scale sx (one IEEE division of exact values): bit-exact.
+"""
+import numpy as np
+import torch
+
+BF16_MAX_ABS = 2e-2
+BF16_REL_L2 = 5e-3
+F32_REL = 1e-5
+FP8_Y_REL = 2e-2
+FP8_Y_REL_L2 = 5e-3
+MOE_W_ABS = 1e-6
+
+
+def to64(t) -> np.ndarray:
+    if isinstance(t, torch.Tensor):
+        return t.detach().to("cpu", torch.float64).numpy()
+    return np.asarray(t, dtype=np.float64)
+
+
+def rel_l2(got, ref) -> float:
+    got, ref = to64(got), to64(ref)
+    return float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
+
+
+def assert_bf16_close(got, ref, what=""):
+    got, ref = to64(got), to64(ref)
+    assert np.isfinite(got).all(), f"{what}: non-finite output (unwritten element?)"
+    err = np.abs(got - ref).max()
+    r = rel_l2(got, ref)
+    assert err <= BF16_MAX_ABS, f"{what}: max-abs {err:.3e} > {BF16_MAX_ABS}"
+    assert r <= BF16_REL_L2, f"{what}: rel-L2 {r:.3e} > {BF16_REL_L2}"
+
+
+def assert_f32_close(got, ref, what=""):
+    got, ref = to64(got), to64(ref)
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    bound = F32_REL * np.maximum(1.0, np.abs(ref))
+    bad = np.abs(got - ref) > bound
+    assert not bad.any(), f"{what}: {bad.sum()} elements outside 1e-5 (max {np.abs(got - ref).max():.3e})"
+    assert rel_l2(got, ref) <= F32_REL, f"{what}: rel-L2 {rel_l2(got, ref):.3e}"
+
+
+def assert_fp8_y_close(got, ref, what=""):
+    got, ref = to64(got), to64(ref)
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    bound = FP8_Y_REL * np.maximum(1.0, np.abs(ref))
+    bad = np.abs(got - ref) > bound
+    assert not bad.any(), f"{what}: {bad.sum()} elements outside tolerance"
+    assert rel_l2(got, ref) <= FP8_Y_REL_L2, f"{what}: rel-L2 {rel_l2(got, ref):.3e}"

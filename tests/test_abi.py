@@ -1,0 +1,85 @@
+"""The C-ABI library builds, loads and exports every function include/rf.h
+declares; host-side argument validation rejects bad calls before any CUDA
+work (these calls need no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from cascaded_reductions_loop_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def rf():
+    _build.build()
+    import cascaded_reductions_loop_gb300 as m
+    return m
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "rf.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rf_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("rf_attn_fwd", "rf_attn_decode_splitkv", "rf_moe_gate_topk_softmax",
+              "rf_absmax_fp8_gemm", "rf_status_string", "rf_get_device_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(rf):
+    lib = ctypes.CDLL(_build.LIB_PATH)
+    for n in _declared():
+        assert hasattr(lib, n), f"{n} declared in rf.h but not exported"
+        assert hasattr(rf, n), f"{n} has no Python binding"
+
+
+def test_status_strings(rf):
+    assert rf.rf_status_string(0) == "RF_OK"
+    for s in range(1, 6):
+        assert rf.rf_status_string(s).startswith("RF_ERR_")
+    assert "unknown" in rf.rf_status_string(99)
+    assert rf.rf_version() >= 10000
+
+
+def test_validation_rejects_bad_arguments_without_a_gpu(rf):
+    L = rf.lib
+    p = ctypes.c_void_p(1 << 20)        # 16-byte aligned, never dereferenced
+    mis = ctypes.c_void_p((1 << 20) + 4)
+    null = None
+    # attention: null / misaligned pointers, bad sizes, causal, dtype, scale
+    assert L.rf_attn_fwd(1, null, p, p, p, 1, 1, 64, 64, 64, 0.125, 0, None) == rf.RF_ERR_INVALID_ARG
+    assert L.rf_attn_fwd(1, mis, p, p, p, 1, 1, 64, 64, 64, 0.125, 0, None) == rf.RF_ERR_INVALID_ARG
+    assert L.rf_attn_fwd(1, p, p, p, p, 0, 1, 64, 64, 64, 0.125, 0, None) == rf.RF_ERR_INVALID_ARG
+    assert L.rf_attn_fwd(1, p, p, p, p, 1, 1, 64, 64, 64, 0.125, 1, None) == rf.RF_ERR_INVALID_ARG
+    assert L.rf_attn_fwd(7, p, p, p, p, 1, 1, 64, 64, 64, 0.125, 0, None) == rf.RF_ERR_INVALID_ARG
+    assert L.rf_attn_fwd(1, p, p, p, p, 1, 1, 64, 64, 64, -1.0, 0, None) == rf.RF_ERR_INVALID_ARG
+    assert L.rf_attn_fwd(1, p, p, p, p, 1, 1, 64, 64, 96, 0.125, 0, None) == rf.RF_ERR_UNSUPPORTED
+    assert L.rf_attn_fwd(0, p, p, p, p, 1, 1, 64, 64, 48, 0.125, 0, None) == rf.RF_ERR_UNSUPPORTED
+    # decode: Hq not a multiple of Hkv, unsupported group / head dim, too many splits
+    assert L.rf_attn_decode_splitkv(p, p, p, p, 1, 6, 4, 64, 128, 0.1, 0, p, 1 << 20, None) == rf.RF_ERR_INVALID_ARG
+    assert L.rf_attn_decode_splitkv(p, p, p, p, 1, 12, 4, 64, 128, 0.1, 0, p, 1 << 20, None) == rf.RF_ERR_UNSUPPORTED
+    assert L.rf_attn_decode_splitkv(p, p, p, p, 1, 8, 2, 64, 64, 0.1, 0, p, 1 << 20, None) == rf.RF_ERR_UNSUPPORTED
+    assert L.rf_attn_decode_splitkv(p, p, p, p, 1, 8, 2, 64, 128, 0.1, 65, p, 1 << 20, None) == rf.RF_ERR_INVALID_ARG
+    # an explicit split count needs no device: a too-small workspace is caught on the host
+    assert L.rf_attn_decode_splitkv(p, p, p, p, 1, 8, 2, 64, 128, 0.1, 4, p, 16, None) == rf.RF_ERR_WORKSPACE
+    assert L.rf_attn_decode_splitkv(p, p, p, p, 1, 8, 2, 64, 128, 0.1, 4, null, 1 << 20, None) == rf.RF_ERR_WORKSPACE
+    assert rf.rf_attn_decode_splitkv_workspace_size(2, 8, 2, 64, 128, 4) == 2 * 8 * 4 * (128 + 2) * 4
+    assert rf.rf_attn_decode_splitkv_num_splits(1, 6, 4, 64, 128, 0) == 0
+    # MoE: D not a multiple of 8, k out of range, E not covered
+    assert L.rf_moe_gate_topk_softmax(p, p, 16, 100, 64, 2, p, p, None) == rf.RF_ERR_INVALID_ARG
+    assert L.rf_moe_gate_topk_softmax(p, p, 16, 128, 64, 0, p, p, None) == rf.RF_ERR_INVALID_ARG
+    assert L.rf_moe_gate_topk_softmax(p, p, 16, 128, 32, 2, p, p, None) == rf.RF_ERR_UNSUPPORTED
+    assert L.rf_moe_gate_topk_softmax(p, p, 16, 128, 64, 9, p, p, None) == rf.RF_ERR_UNSUPPORTED
+    # FP8: K not a multiple of 16, missing workspace
+    assert L.rf_absmax_fp8_gemm(p, p, p, p, 16, 16, 40, p, p, null, 0, None) == rf.RF_ERR_INVALID_ARG
+    assert L.rf_absmax_fp8_gemm(p, p, p, p, 16, 16, 64, null, null, null, 0, None) == rf.RF_ERR_WORKSPACE
+    assert rf.rf_absmax_fp8_gemm_workspace_size(16, 16, 64) == 16 * 64 + 16 * 4
+    assert rf.rf_absmax_fp8_gemm_workspace_size(16, 16, 40) == 0
+    # self-test: out-of-range limit
+    assert L.rf_selftest_wait_timeout(0, None) == rf.RF_ERR_INVALID_ARG

@@ -1,0 +1,81 @@
+"""GPU parity: single-segment fused attention (fp32 SIMT and bf16 tcgen05)
+against the fp64 three-pass oracle, through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from cascaded_reductions_loop_gb300 import inputs as I
+from oracle import attention as A
+from tests.helpers import assert_bf16_close, assert_f32_close, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def rf():
+    import cascaded_reductions_loop_gb300 as m
+    assert torch.cuda.is_available()
+    return m
+
+
+def _run(rf, q, k, v, scale):
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o = torch.full_like(qd, float("nan"))
+    rf.rf_attn_fwd(qd, kd, vd, o, scale)
+    assert rf.rf_get_device_status() == rf.RF_OK
+    return o.cpu()
+
+
+def test_tiny_fp32_workload(rf):
+    s = I.TINY_ATTN
+    q, k, v = I.attention_inputs(s)
+    o = _run(rf, q, k, v, s.scale)
+    assert_f32_close(o, A.attention(q, k, v, s.scale), "tiny fp32")
+
+
+@pytest.mark.parametrize("shape", [(2, 3, 37, 101, 64), (1, 2, 5, 300, 128), (1, 1, 1, 1, 64),
+                                   (1, 1, 33, 32, 64), (1, 1, 4, 1000, 64)])
+def test_fp32_ragged(rf, shape):
+    B, H, Lq, Lk, d = shape
+    sh = I.AttnShape(B, H, H, Lq, Lk, d, "f32", seed=11 + Lk)
+    q, k, v = I.attention_inputs(sh)
+    o = _run(rf, q, k, v, sh.scale)
+    assert_f32_close(o, A.attention(q, k, v, sh.scale), f"fp32 {shape}")
+
+
+def test_bert_prefill_bf16_full(rf):
+    s = I.BERT_PREFILL
+    q, k, v = I.attention_inputs(s)
+    o = _run(rf, q, k, v, s.scale)
+    assert_bf16_close(o, A.attention(q, k, v, s.scale), "BERT prefill")
+
+
+@pytest.mark.parametrize("shape", [(2, 3, 200, 333, 64), (1, 1, 1, 1, 64), (1, 2, 128, 128, 64),
+                                   (1, 1, 129, 257, 64), (3, 1, 64, 1000, 64),
+                                   (1, 1, 300, 5, 64)])
+def test_bf16_ragged(rf, shape):
+    B, H, Lq, Lk, d = shape
+    sh = I.AttnShape(B, H, H, Lq, Lk, d, "bf16", seed=100 + Lq + Lk)
+    q, k, v = I.attention_inputs(sh)
+    o = _run(rf, q, k, v, sh.scale)
+    assert_bf16_close(o, A.attention(q, k, v, sh.scale), f"bf16 {shape}")
+
+
+def test_bf16_single_key_returns_v0(rf):
+    sh = I.AttnShape(2, 2, 2, 130, 1, 64, "bf16", seed=7)
+    q, k, v = I.attention_inputs(sh)
+    o = _run(rf, q, k, v, sh.scale)
+    ref = v.float().expand(-1, -1, 130, -1)
+    np.testing.assert_array_equal(to64(o), to64(ref.to(torch.bfloat16)))
+
+
+def test_bf16_large_scores_stay_finite(rf):
+    """Scores of magnitude ~200 exercise the running-max rescale (a missing
+    rescale overflows exp)."""
+    sh = I.AttnShape(1, 2, 2, 128, 512, 64, "bf16", seed=9)
+    q, k, v = I.attention_inputs(sh)
+    q = (q.float() * 8).to(torch.bfloat16)
+    o = _run(rf, q, k, v, 1.0 / math.sqrt(64))
+    assert_bf16_close(o, A.attention(q, k, v, 1.0 / math.sqrt(64)), "large scores")

@@ -1,0 +1,62 @@
+"""GPU parity: fused MoE gate (tcgen05 scores, top-k, softmax) against the
+fp64 oracle, through the C ABI.  Indices must match bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+from cascaded_reductions_loop_gb300 import inputs as I
+from oracle import moe_gate as G
+from tests.helpers import MOE_W_ABS
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def rf():
+    import cascaded_reductions_loop_gb300 as m
+    assert torch.cuda.is_available()
+    return m
+
+
+def _run(rf, x, w, k):
+    T = x.shape[0]
+    idx = torch.full((T, k), -1, dtype=torch.int32, device="cuda")
+    wts = torch.full((T, k), float("nan"), dtype=torch.float32, device="cuda")
+    rf.rf_moe_gate_topk_softmax(x.cuda(), w.cuda(), k, idx, wts)
+    assert rf.rf_get_device_status() == rf.RF_OK
+    return idx.cpu().numpy(), wts.cpu().numpy()
+
+
+def _check(x, w, k, idx, wts, what):
+    ref_idx, ref_w, scores = G.moe_gate(x, w, k)
+    mism = np.nonzero((idx != ref_idx).any(axis=1))[0]
+    assert mism.size == 0, f"{what}: {mism.size} tokens with different experts, e.g. {mism[:5]}"
+    assert np.abs(wts - ref_w).max() <= MOE_W_ABS, f"{what}: weights"
+    return scores
+
+
+def test_moe_gate_full(rf):
+    s = I.MOE_GATE
+    x, w = I.moe_inputs(s)
+    idx, wts = _run(rf, x, w, s.k)
+    scores = _check(x, w, s.k, idx, wts, "MoE 8192x4096x64")
+    # the tie-break is exercised at this size
+    sel2 = np.take_along_axis(scores, idx[:, 1:2].astype(np.int64), axis=1)
+    assert ((scores == sel2).sum(axis=1) > 1).sum() > 10
+
+
+@pytest.mark.parametrize("T,D,k", [(300, 256, 2), (1, 64, 1), (129, 1024, 4), (64, 4096, 8),
+                                   (513, 200, 2), (256, 2048, 3), (100, 8, 2)])
+def test_moe_gate_small(rf, T, D, k):
+    x, w = I.moe_inputs(I.MoEShape(T=T, D=D, E=64, k=k, seed=T + D + k))
+    idx, wts = _run(rf, x, w, k)
+    _check(x, w, k, idx, wts, f"MoE {T}x{D} k={k}")
+
+
+def test_moe_gate_all_equal_scores(rf):
+    """All scores equal: the first k experts, uniform weights."""
+    x = torch.ones(130, 128, dtype=torch.bfloat16)
+    w = torch.ones(64, 128, dtype=torch.bfloat16)
+    idx, wts = _run(rf, x, w, 4)
+    assert (idx == np.arange(4)[None, :]).all()
+    assert np.abs(wts - 0.25).max() <= MOE_W_ABS
