@@ -46,7 +46,6 @@ UNIT = "% of roofline (step roofline time / measured step time)"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFS = 1900.0
 FALLBACK_BF16_TFS_SUSTAINED = 1700.0
-DOMINANT = "decode_32k"
 
 
 # ------------------------------------------------------------------ peaks
@@ -113,15 +112,26 @@ def make_ops():
     ]
 
 
-def host_inputs():
-    """All step inputs as CPU tensors (seeded), keyed by op name."""
-    q32, k32, v32 = I.decode_inputs(I.DECODE_32K)
-    q2, k2, v2 = I.decode_inputs(I.DECODE_2K)
-    qb, kb, vb = I.attention_inputs(I.BERT_PREFILL)
-    xm, wm = I.moe_inputs(I.MOE_GATE)
-    xf, wqf, swf = I.fp8_inputs(I.FP8_GEMM)
-    return {"decode_32k": [q32, k32, v32], "decode_2k": [q2, k2, v2],
-            "bert_prefill": [qb, kb, vb], "moe_gate": [xm, wm], "fp8_gemm": [xf, wqf, swf]}
+GENERATORS = {
+    "decode_32k": lambda: list(I.decode_inputs(I.DECODE_32K)),
+    "decode_2k": lambda: list(I.decode_inputs(I.DECODE_2K)),
+    "bert_prefill": lambda: list(I.attention_inputs(I.BERT_PREFILL)),
+    "moe_gate": lambda: list(I.moe_inputs(I.MOE_GATE)),
+    "fp8_gemm": lambda: list(I.fp8_inputs(I.FP8_GEMM)),
+}
+
+
+def host_inputs(names):
+    """Step inputs as CPU tensors (seeded), keyed by op name."""
+    return {n: GENERATORS[n]() for n in names}
+
+
+SPLITS = {}
+
+
+def args_splits(lk):
+    """Explicit split count for a decode length (0 = the library's automatic choice)."""
+    return SPLITS.get(lk, 0)
 
 
 class Step:
@@ -136,9 +146,10 @@ class Step:
         self.o32 = torch.empty(s32.B, s32.Hq, s32.d, dtype=torch.bfloat16, device=cuda)
         self.o2 = torch.empty(s2.B, s2.Hq, s2.d, dtype=torch.bfloat16, device=cuda)
         self.ws32 = torch.empty(rf.rf_attn_decode_splitkv_workspace_size(
-            s32.B, s32.Hq, s32.Hkv, s32.Lk, s32.d, 0), dtype=torch.uint8, device=cuda)
+            s32.B, s32.Hq, s32.Hkv, s32.Lk, s32.d, args_splits(32768)), dtype=torch.uint8,
+            device=cuda)
         self.ws2 = torch.empty(rf.rf_attn_decode_splitkv_workspace_size(
-            s2.B, s2.Hq, s2.Hkv, s2.Lk, s2.d, 0), dtype=torch.uint8, device=cuda)
+            s2.B, s2.Hq, s2.Hkv, s2.Lk, s2.d, args_splits(2048)), dtype=torch.uint8, device=cuda)
         self.ob = torch.empty(sb.B, sb.Hq, sb.Lq, sb.d, dtype=torch.bfloat16, device=cuda)
         self.idx = torch.empty(sm.T, sm.k, dtype=torch.int32, device=cuda)
         self.wts = torch.empty(sm.T, sm.k, dtype=torch.float32, device=cuda)
@@ -147,13 +158,13 @@ class Step:
                                dtype=torch.uint8, device=cuda)
         self.calls = {
             "decode_32k": lambda: rf.rf_attn_decode_splitkv(*d["decode_32k"], self.o32, s32.scale,
-                                                            self.ws32),
+                                                            self.ws32, args_splits(32768)),
             "bert_prefill": lambda: rf.rf_attn_fwd(*d["bert_prefill"], self.ob, sb.scale),
             "moe_gate": lambda: rf.rf_moe_gate_topk_softmax(*d["moe_gate"], sm.k, self.idx,
                                                             self.wts),
             "fp8_gemm": lambda: rf.rf_absmax_fp8_gemm(*d["fp8_gemm"], self.y, workspace=self.wsf),
             "decode_2k": lambda: rf.rf_attn_decode_splitkv(*d["decode_2k"], self.o2, s2.scale,
-                                                           self.ws2),
+                                                           self.ws2, args_splits(2048)),
         }
         self.outputs = {"decode_32k": [self.o32], "decode_2k": [self.o2],
                         "bert_prefill": [self.ob], "moe_gate": [self.idx, self.wts],
@@ -264,8 +275,8 @@ def run_ours(args, world, rank, local):
 
     torch.cuda.set_device(local)
     peaks = load_peaks()
-    ops = make_ops()
-    host = host_inputs()
+    ops = select_ops(args)
+    host = host_inputs([op.name for op in ops])
     dev = {k: [t.cuda() for t in v] for k, v in host.items()}
     step = Step(rf, dev)
     stream = torch.cuda.current_stream()
@@ -322,14 +333,20 @@ def run_ours(args, world, rank, local):
             r["TFLOPs"] = round(op.flops / t / 1e12, 1)
         rows[op.name] = r
 
-    dom = next(op for op in ops if op.name == DOMINANT)
-    dom_t = per_op_ms[DOMINANT] * 1e-3
-    achieved = dom.bytes / dom_t / 1e9
-    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": traffic_for("decode_32k"),
-                "kernel": "rf_attn_decode_splitkv at Lk=32768 (partial + merge kernels)",
-                "peak_source": peaks["source"]}
+    dom = max(ops, key=lambda op: per_op_ms[op.name])
+    dom_t = per_op_ms[dom.name] * 1e-3
+    if dom.bound(peaks) == "hbm":
+        achieved = dom.bytes / dom_t / 1e9
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
+    else:
+        achieved = dom.flops / dom_t / 1e12
+        pk = peaks["bf16_tfs_sustained"] * (2.0 if dom.tc_dtype == "fp8" else 1.0)
+        roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk,
+                    "unit": "TFLOP/s", "frac": round(achieved / pk, 4)}
+    roofline.update({"traffic": traffic_for(dom.name), "kernel": dom.name,
+                     "launches_per_call": dom.n_kernels,
+                     "peak_source": peaks["source"]})
 
     result = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
@@ -356,12 +373,23 @@ def run_ours(args, world, rank, local):
     return result
 
 
+def select_ops(args):
+    ops = make_ops()
+    if args.only:
+        names = args.only.split(",")
+        unknown = set(names) - {op.name for op in ops}
+        if unknown:
+            raise SystemExit(f"unknown op(s) {sorted(unknown)}")
+        ops = [op for op in ops if op.name in names]
+    return ops
+
+
 def run_e2e(rf, ops, peaks, host, step, world, args):
     """Same metric through the public binding with host buffers: every step
     copies its inputs from pinned host memory and its results back."""
     pinned = {k: [t.pin_memory() for t in v] for k, v in host.items()}
-    out_host = {k: [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
-                for k, outs in step.outputs.items()}
+    out_host = {op.name: [torch.empty(o.shape, dtype=o.dtype).pin_memory()
+                          for o in step.outputs[op.name]] for op in ops}
     h2d = sum(t.numel() * t.element_size() for v in pinned.values() for t in v)
     d2h = sum(t.numel() * t.element_size() for v in out_host.values() for t in v)
     stream = torch.cuda.current_stream()
@@ -397,8 +425,8 @@ def run_e2e(rf, ops, peaks, host, step, world, args):
 
 
 def oracle_sample_seconds(host, frac):
-    """Times the fp64 oracle on a bounded sample of every op; returns
-    {op: (seconds, fraction of the op's full work covered)}."""
+    """Times the fp64 oracle on a bounded sample of every op present in
+    ``host``; returns {op: (seconds, fraction of the op's full work covered)}."""
     from oracle import attention as A
     from oracle import fp8_quant_gemm as F
     from oracle import moe_gate as G
@@ -406,44 +434,43 @@ def oracle_sample_seconds(host, frac):
     out = {}
     rng = np.random.default_rng(0)
 
-    s = I.DECODE_32K
-    q, k, v = host["decode_32k"]
-    nrows = max(1, int(round(frac * s.B * s.Hq)))
-    rows = [(int(b), int(h)) for b, h in zip(rng.integers(0, s.B, nrows), rng.integers(0, s.Hq, nrows))]
-    t = time.perf_counter()
-    A.decode_attention(q, k, v, s.scale, rows=rows)
-    out["decode_32k"] = (time.perf_counter() - t, nrows / (s.B * s.Hq))
+    for name, s in (("decode_32k", I.DECODE_32K), ("decode_2k", I.DECODE_2K)):
+        if name not in host:
+            continue
+        q, k, v = host[name]
+        scale_rows = 1 if name == "decode_32k" else 4
+        nrows = max(1, int(round(frac * scale_rows * s.B * s.Hq)))
+        rows = [(int(b), int(h)) for b, h in
+                zip(rng.integers(0, s.B, nrows), rng.integers(0, s.Hq, nrows))]
+        t = time.perf_counter()
+        A.decode_attention(q, k, v, s.scale, rows=rows)
+        out[name] = (time.perf_counter() - t, nrows / (s.B * s.Hq))
 
-    s = I.DECODE_2K
-    q, k, v = host["decode_2k"]
-    nrows = max(1, int(round(frac * 4 * s.B * s.Hq)))
-    rows = [(int(b), int(h)) for b, h in zip(rng.integers(0, s.B, nrows), rng.integers(0, s.Hq, nrows))]
-    t = time.perf_counter()
-    A.decode_attention(q, k, v, s.scale, rows=rows)
-    out["decode_2k"] = (time.perf_counter() - t, nrows / (s.B * s.Hq))
+    if "bert_prefill" in host:
+        s = I.BERT_PREFILL
+        q, k, v = host["bert_prefill"]
+        nh = max(1, int(round(frac * 4 * s.B * s.Hq)))
+        t = time.perf_counter()
+        for i in range(nh):
+            b, h = divmod(i % (s.B * s.Hq), s.Hq)
+            A.attention(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1], s.scale)
+        out["bert_prefill"] = (time.perf_counter() - t, nh / (s.B * s.Hq))
 
-    s = I.BERT_PREFILL
-    q, k, v = host["bert_prefill"]
-    nh = max(1, int(round(frac * 4 * s.B * s.Hq)))
-    t = time.perf_counter()
-    for i in range(nh):
-        b, h = divmod(i % (s.B * s.Hq), s.Hq)
-        A.attention(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1], s.scale)
-    out["bert_prefill"] = (time.perf_counter() - t, nh / (s.B * s.Hq))
+    if "moe_gate" in host:
+        s = I.MOE_GATE
+        x, w = host["moe_gate"]
+        nt = max(1, int(round(frac * 4 * s.T)))
+        t = time.perf_counter()
+        G.moe_gate(x, w, s.k, rows=range(nt))
+        out["moe_gate"] = (time.perf_counter() - t, nt / s.T)
 
-    s = I.MOE_GATE
-    x, w = host["moe_gate"]
-    nt = max(1, int(round(frac * 4 * s.T)))
-    t = time.perf_counter()
-    G.moe_gate(x, w, s.k, rows=range(nt))
-    out["moe_gate"] = (time.perf_counter() - t, nt / s.T)
-
-    s = I.FP8_GEMM
-    x, wq, sw = host["fp8_gemm"]
-    nr = max(1, int(round(frac * s.M)))
-    t = time.perf_counter()
-    F.absmax_fp8_gemm(x, wq, sw, rows=range(nr))
-    out["fp8_gemm"] = (time.perf_counter() - t, nr / s.M)
+    if "fp8_gemm" in host:
+        s = I.FP8_GEMM
+        x, wq, sw = host["fp8_gemm"]
+        nr = max(1, int(round(frac * s.M)))
+        t = time.perf_counter()
+        F.absmax_fp8_gemm(x, wq, sw, rows=range(nr))
+        out["fp8_gemm"] = (time.perf_counter() - t, nr / s.M)
     return out
 
 
@@ -477,8 +504,8 @@ def run_reference(args, world, rank):
     if rank != 0:
         return None
     peaks = load_peaks()
-    ops = make_ops()
-    host = host_inputs()
+    ops = select_ops(args)
+    host = host_inputs([op.name for op in ops])
     frac = 1.0 / 1024
     for _ in range(max(1, min(args.warmup, 1))):
         oracle_sample_seconds(host, frac)
@@ -506,8 +533,13 @@ def run_reference(args, world, rank):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--only", default="",
+                    help="comma-separated subset of ops (decode_32k, bert_prefill, moe_gate, "
+                         "fp8_gemm, decode_2k); default: the whole step")
+    ap.add_argument("--splits", default="",
+                    help="explicit decode split counts, e.g. 32768:64,2048:8 (default: automatic)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -517,6 +549,10 @@ def main():
     if args.warmup < 3 and args.impl == "ours":
         print("note: raising --warmup to 3 (minimum)", file=sys.stderr)
         args.warmup = 3
+
+    for item in filter(None, args.splits.split(",")):
+        lk, n = item.split(":")
+        SPLITS[int(lk)] = int(n)
 
     world, rank, local = dist_info()
     if world > 1:

@@ -6,8 +6,8 @@ dtypes, then calls the C entry point of the same name (declared in
 ``include/rf.h``) with raw device pointers and the current torch CUDA
 stream.  Every step of the computation runs in the library's CUDA kernels;
 there is no other implementation behind these names.  If the library is
-missing, importing this package raises: build it with
-``cascaded_reductions_loop_gb300._build.build()``.
+missing, importing this package raises: build it first with
+``python __graft_entry__.py`` (or ``python cascaded_reductions_loop_gb300/_build.py``).
 """
 from __future__ import annotations
 
@@ -36,7 +36,7 @@ LIB_PATH = _build.LIB_PATH
 if not os.path.exists(LIB_PATH):
     raise ImportError(
         f"{LIB_PATH} is missing: the CUDA library must be built first "
-        "(cascaded_reductions_loop_gb300._build.build()); there is no fallback path")
+        "(python __graft_entry__.py); there is no fallback path")
 
 _c = ctypes
 _P = _c.c_void_p

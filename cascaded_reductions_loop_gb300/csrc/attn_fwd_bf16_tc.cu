@@ -193,7 +193,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     bool ok = true;
 
     for (int j = 0; j < nkv; ++j) {
-      if (!mbar_wait(smem_u32(&bars->s_full), (uint32_t)(j & 1)) || *abort_flag) {
+      // warp-uniform decision: the TMEM loads below are warp-collective
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full), (uint32_t)(j & 1)) &&
+                                       !*abort_flag)) {
         ok = false;
         break;
       }
@@ -244,7 +246,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       tc_fence_before();                               // S reads ordered before the arrive
       mbar_arrive(smem_u32(&bars->p_full));
 
-      if (!mbar_wait(smem_u32(&bars->o_full), (uint32_t)(j & 1)) || *abort_flag) {
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->o_full), (uint32_t)(j & 1)) &&
+                                       !*abort_flag)) {
         ok = false;
         break;
       }

@@ -46,10 +46,11 @@ __device__ __forceinline__ uint2 quant8(const uint4 v, float s) {
 }
 
 __device__ __forceinline__ uint32_t absmax_bits(const uint4 v) {
-  // |bf16| ordering equals the ordering of its bits with the sign cleared
-  const uint32_t a = max(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu);
-  const uint32_t b = max(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu);
-  const uint32_t c = max(a, b);
+  // |bf16| ordering equals the ordering of its bits with the sign cleared;
+  // __vmaxu2 takes the max of each 16-bit half separately
+  const uint32_t a = __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu);
+  const uint32_t b = __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu);
+  const uint32_t c = __vmaxu2(a, b);
   return max(c & 0xFFFFu, c >> 16);
 }
 

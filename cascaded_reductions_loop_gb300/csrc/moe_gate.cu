@@ -61,9 +61,10 @@ __device__ __forceinline__ float4 ld_peer_v4(uint32_t addr) {
   return v;
 }
 
-// Top-KT of a 64-score row: a sorted insertion scan in expert order.  A new
-// score displaces an entry only when strictly greater, so among equal scores
-// the lower expert index stays ahead.
+// Top-KT of a 64-score row: a sorted insertion scan in expert order under the
+// total order (score descending, expert index ascending).  An entry pushed
+// down by a larger score carries its (lower) index, so it must also displace
+// an equal score with a higher index further down.
 template <int KT>
 __device__ __forceinline__ void topk_softmax_row(const float* srow, int32_t* idx_out,
                                                  float* w_out) {
@@ -72,7 +73,7 @@ __device__ __forceinline__ void topk_softmax_row(const float* srow, int32_t* idx
 #pragma unroll
   for (int j = 0; j < KT; ++j) {
     v[j] = -INFINITY;
-    ix[j] = 0;
+    ix[j] = kE;
   }
 #pragma unroll 4
   for (int e = 0; e < kE; ++e) {
@@ -80,7 +81,7 @@ __device__ __forceinline__ void topk_softmax_row(const float* srow, int32_t* idx
     int ce = e;
 #pragma unroll
     for (int j = 0; j < KT; ++j) {
-      if (cv > v[j]) {
+      if (cv > v[j] || (cv == v[j] && ce < ix[j])) {
         const float tv = v[j];
         const int te = ix[j];
         v[j] = cv;

@@ -17,3 +17,14 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return GOLDEN
+
+
+def _ensure_library_built():
+    """Builds librf_gb300.so if it is missing or older than its sources (a no-op
+    otherwise), so that every test sees the library of the current sources."""
+    import __graft_entry__
+
+    __graft_entry__._load_build_module().build()
+
+
+_ensure_library_built()

@@ -7,9 +7,10 @@ import re
 
 import pytest
 
-from cascaded_reductions_loop_gb300 import _build
+import __graft_entry__
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+_build = __graft_entry__._load_build_module()
 
 
 @pytest.fixture(scope="module")

@@ -60,3 +60,17 @@ def test_moe_gate_all_equal_scores(rf):
     idx, wts = _run(rf, x, w, 4)
     assert (idx == np.arange(4)[None, :]).all()
     assert np.abs(wts - 0.25).max() <= MOE_W_ABS
+
+
+@pytest.mark.parametrize("k", [1, 2, 4, 8])
+def test_moe_gate_dense_ties(rf, k):
+    """Scores drawn from {-2..2}: nearly every token has ties across the top-k
+    boundary and inside it, including an equal score pushed down past a
+    higher-index twin by a larger one."""
+    T, D = 512, 8
+    g = torch.Generator().manual_seed(77 + k)
+    x = torch.zeros(T, D, dtype=torch.bfloat16)
+    x[torch.arange(T), torch.arange(T) % D] = 1
+    w = torch.randint(-2, 3, (64, D), generator=g).to(torch.bfloat16)
+    idx, wts = _run(rf, x, w, k)
+    _check(x, w, k, idx, wts, f"dense ties k={k}")
