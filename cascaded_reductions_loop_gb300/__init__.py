@@ -21,7 +21,8 @@ from . import _build
 __all__ = [
     "RFError", "lib", "rf_status_string", "rf_version", "rf_get_device_status",
     "rf_attn_fwd", "rf_attn_decode_splitkv", "rf_attn_decode_splitkv_num_splits",
-    "rf_attn_decode_splitkv_workspace_size", "rf_moe_gate_topk_softmax",
+    "rf_attn_decode_splitkv_workspace_size", "rf_attn_decode_splitkv_noalloc",
+    "RF_DECODE_NOALLOC_SCRATCH_BYTES", "rf_moe_gate_topk_softmax",
     "rf_absmax_fp8_gemm", "rf_absmax_fp8_gemm_workspace_size", "rf_selftest_wait_timeout",
     "RF_OK", "RF_ERR_INVALID_ARG", "RF_ERR_UNSUPPORTED", "RF_ERR_WORKSPACE", "RF_ERR_CUDA",
     "RF_ERR_DEVICE_TIMEOUT", "RF_F32", "RF_BF16",
@@ -30,6 +31,7 @@ __all__ = [
 RF_OK, RF_ERR_INVALID_ARG, RF_ERR_UNSUPPORTED, RF_ERR_WORKSPACE, RF_ERR_CUDA, \
     RF_ERR_DEVICE_TIMEOUT = range(6)
 RF_F32, RF_BF16 = 0, 1
+RF_DECODE_NOALLOC_SCRATCH_BYTES = 16 << 20   # as in rf.h
 
 LIB_PATH = _build.LIB_PATH
 
@@ -54,6 +56,7 @@ _SIGS = {
     "rf_attn_decode_splitkv_num_splits": (_I, [_I, _I, _I, _I, _I, _I]),
     "rf_attn_decode_splitkv_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I]),
     "rf_attn_decode_splitkv": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
+    "rf_attn_decode_splitkv_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
     "rf_moe_gate_topk_softmax": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "rf_absmax_fp8_gemm_workspace_size": (_Z, [_I, _I, _I]),
     "rf_absmax_fp8_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _Z, _P]),
@@ -153,6 +156,23 @@ def rf_attn_decode_splitkv(q, k, v, o, scale: float, workspace, num_splits: int 
     _check(lib.rf_attn_decode_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, Hq, Hkv, Lk, d,
                                       float(scale), int(num_splits), _ptr(workspace), ws_bytes,
                                       _stream(stream)), "rf_attn_decode_splitkv")
+
+
+def rf_attn_decode_splitkv_noalloc(q, k, v, o, scale: float, num_splits: int = 0,
+                                   stream=None) -> None:
+    """rf_attn_decode_splitkv with the library's built-in scratch instead of a
+    caller workspace, for callers that cannot provide device memory.  The
+    first call on a device must come before any stream capture; calls that
+    overlap on the GPU race on the shared scratch."""
+    B, Hq, d = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    _need(q, torch.bfloat16, (B, Hq, d), "q")
+    _need(k, torch.bfloat16, (B, Hkv, Lk, d), "k")
+    _need(v, torch.bfloat16, (B, Hkv, Lk, d), "v")
+    _need(o, torch.bfloat16, (B, Hq, d), "o")
+    _check(lib.rf_attn_decode_splitkv_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, Hq, Hkv, Lk,
+                                              d, float(scale), int(num_splits), _stream(stream)),
+           "rf_attn_decode_splitkv_noalloc")
 
 
 def rf_moe_gate_topk_softmax(x, w_gate, k: int, idx, weights, stream=None) -> None:

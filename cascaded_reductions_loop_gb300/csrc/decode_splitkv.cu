@@ -17,6 +17,8 @@
 // exp2 and sums stay in registers (quad shuffles).
 #include <math.h>
 
+#include <mutex>
+
 #include "rf_device.cuh"
 #include "rf_internal.h"
 
@@ -353,3 +355,59 @@ cudaError_t launch_decode_splitkv(const void* Q, const void* K, const void* V, v
 }
 
 }  // namespace rf
+
+// ====================================================================
+// Allocation-free variant of rf_attn_decode_splitkv.
+//
+// Some callers cannot hand this library a device buffer: a plugin reached
+// through a fixed C interface that carries no workspace argument, a serving
+// loop that forbids device allocation after start-up (cudaMalloc can
+// synchronise the device and stall the loop), or a host framework whose pool
+// allocator already holds nearly all device memory, so that a direct
+// cudaMalloc would fail or fragment it.  For them the partial states live in
+// the file-scope array below, which every GPU that loads the library keeps
+// for the life of the process.
+// ====================================================================
+
+namespace rf {
+namespace {
+
+// Scratch for the partial (m, l, o) states of the split-KV decode.  Its size
+// is part of the ABI (RF_DECODE_NOALLOC_SCRATCH_BYTES in rf.h).
+constexpr size_t kNoAllocScratchBytes = RF_DECODE_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) uint8_t g_decode_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxScratchDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxScratchDevices] = {};
+
+// Device address of g_decode_scratch on the current device.  In host code the
+// array's name is only a host-side handle, so the address is looked up once
+// per device (with that device current) and cached.  Returns nullptr on error.
+void* decode_scratch_address() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxScratchDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return nullptr;
+    g_scratch_ptr[dev] = p;
+  }
+  return g_scratch_ptr[dev];
+}
+
+}  // namespace
+}  // namespace rf
+
+extern "C" rf_status rf_attn_decode_splitkv_noalloc(const void* Q, const void* K, const void* V,
+                                                    void* O, int B, int Hq, int Hkv, int Lk,
+                                                    int d, float scale, int num_splits,
+                                                    rf_stream_t stream) {
+  // Nothing in the scratch has to start at zero: the partial kernel writes
+  // every (batch, head, segment) state that the merge kernel reads.
+  void* scratch = rf::decode_scratch_address();
+  if (!scratch) return RF_ERR_CUDA;
+  return rf_attn_decode_splitkv(Q, K, V, O, B, Hq, Hkv, Lk, d, scale, num_splits, scratch,
+                                rf::kNoAllocScratchBytes, stream);
+}
+

@@ -128,6 +128,35 @@ rf_status rf_attn_decode_splitkv(const void* Q, const void* K, const void* V, vo
                                  int num_splits, void* workspace, size_t workspace_bytes,
                                  rf_stream_t stream);
 
+/* Size in bytes of the built-in scratch of rf_attn_decode_splitkv_noalloc. */
+#define RF_DECODE_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * Allocation-free form of rf_attn_decode_splitkv (the paper has no
+ * counterpart: this is an interface convenience).  For callers that cannot
+ * provide device memory -- a plugin behind a fixed C interface with no
+ * workspace argument, a serving loop that must not allocate after start-up,
+ * or a host framework whose own pool allocator owns the device memory.
+ * Same arguments, computation and results as rf_attn_decode_splitkv, but the
+ * partial states go to a 16 MiB scratch array built into the library (a
+ * file-scope __device__ array that every GPU loading the library keeps
+ * until the process exits); the function never allocates or frees memory.
+ *   - Returns RF_ERR_WORKSPACE when the partial states of the request,
+ *     rf_attn_decode_splitkv_workspace_size(...), exceed
+ *     RF_DECODE_NOALLOC_SCRATCH_BYTES (lower num_splits, or use
+ *     rf_attn_decode_splitkv with a caller workspace).
+ *   - The first call on a device looks up the scratch's device address (one
+ *     cudaGetSymbolAddress with that device current) and caches it; make
+ *     that first call before any stream capture on the device.
+ *   - All calls on a device share the one scratch, which keeps the last
+ *     call's contents (nothing in it needs to start at zero).  Calls that
+ *     may overlap on the GPU -- on different streams without ordering, or
+ *     from several host threads -- race on it; serialise them on one stream.
+ */
+rf_status rf_attn_decode_splitkv_noalloc(const void* Q, const void* K, const void* V, void* O,
+                                         int B, int Hq, int Hkv, int Lk, int d, float scale,
+                                         int num_splits, rf_stream_t stream);
+
 /*
  * Fused MoE gate ([E] §4.2): scores = x . W_gate^T, top-k experts per token,
  * softmax over the k selected scores; the score matrix never reaches
