@@ -1,0 +1,33 @@
+"""The seeded input generators: shapes, dtypes, determinism and the value
+sets the workloads promise (integers in {-2..2}, ~1% outliers, E4M3 codes
+without NaN)."""
+import torch
+
+from cascaded_reductions_loop_gb300 import inputs as I
+
+
+def test_attention_shapes_and_determinism():
+    s = I.AttnShape(2, 4, 2, 3, 70, 64, "bf16", seed=9)
+    q, k, v = I.attention_inputs(s)
+    assert q.shape == (2, 4, 3, 64) and k.shape == (2, 2, 70, 64) and v.dtype == torch.bfloat16
+    q2, k2, v2 = I.attention_inputs(s)
+    assert torch.equal(q, q2) and torch.equal(k, k2) and torch.equal(v, v2)
+    qd, kd, vd = I.decode_inputs(I.AttnShape(2, 4, 2, 1, 70, 128, "bf16", seed=9))
+    assert qd.shape == (2, 4, 128)
+    assert I.TINY_ATTN.scale == 0.125 and I.DECODE_2K.scale == 128 ** -0.5
+
+
+def test_moe_values_are_small_integers():
+    x, w = I.moe_inputs(I.MoEShape(T=64, D=128, E=64, k=2, seed=1))
+    assert x.shape == (64, 128) and w.shape == (64, 128)
+    for t in (x, w):
+        assert set(t.float().unique().tolist()) <= {-2.0, -1.0, 0.0, 1.0, 2.0}
+
+
+def test_fp8_inputs():
+    x, wq, sw = I.fp8_inputs(I.FP8Shape(M=256, N=64, K=512, seed=2))
+    assert x.dtype == torch.bfloat16 and wq.dtype == torch.uint8 and sw.dtype == torch.float32
+    frac = (x.float().abs() > 6).float().mean().item()      # outliers (|N(0,1)| > 6 is ~2e-9)
+    assert 0.004 < frac < 0.012
+    assert not ((wq & 0x7F) == 0x7F).any()                  # no NaN codes
+    assert (((wq & 0x7F) == 0x7E).sum(dim=1) >= 1).all()    # every column reaches +-448
