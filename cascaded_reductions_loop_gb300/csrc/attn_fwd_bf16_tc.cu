@@ -186,11 +186,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int r = sub * 32 + lane;                     // query row within the tile
     const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
     uint8_t* prow = smem + kPOff + r * 128;
-    float o[kD];
+    uint64_t o2[kD / 2];                               // o as fp32 pairs
 #pragma unroll
-    for (int i = 0; i < kD; ++i) o[i] = 0.f;
+    for (int i = 0; i < kD / 2; ++i) o2[i] = 0ull;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
+    const uint64_t c2 = f2(c_log2, c_log2);
 
     for (int j = 0; j < nkv; ++j) {
       // warp-uniform decision: the TMEM loads below are warp-collective
@@ -201,21 +202,29 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       tc_fence_after();
       const int valid = min(BKV, Lk - j * BKV);        // keys of this tile that exist
-      // pass 1: row max
+      const bool full = valid == BKV;                  // uniform over the CTA
+      // pass 1: row max of the raw scores
       float mx = -INFINITY;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint32_t v[32];
         tmem_ld32(tmem_s + lane_off + q * 32, v);
         tmem_ld_wait();
+        if (full) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (q * 32 + i < valid) mx = fmaxf(mx, __uint_as_float(v[i]));
+          for (int i = 0; i < 32; i += 2)
+            mx = fmax3(mx, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (q * 32 + i < valid) mx = fmaxf(mx, __uint_as_float(v[i]));
+        }
       }
       const float m_new = fmaxf(m_run, mx * c_log2);
       const float alpha = ex2(m_run - m_new);          // 0 on the first tile
+      const uint64_t negm2 = f2(-m_new, -m_new);
       // pass 2: P = 2^(S c - m'), row sum, P -> swizzled bf16 tile
-      float psum = 0.f;
+      uint64_t sum2 = 0ull;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint32_t v[32];
@@ -224,11 +233,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int c0 = q * 32 + 2 * i;
-          const float p0 = c0 < valid ? ex2(fmaf(__uint_as_float(v[2 * i]), c_log2, -m_new)) : 0.f;
-          const float p1 =
-              c0 + 1 < valid ? ex2(fmaf(__uint_as_float(v[2 * i + 1]), c_log2, -m_new)) : 0.f;
-          psum += p0 + p1;
+          float t0, t1;
+          f2_split(ffma2(f2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), c2, negm2),
+                   t0, t1);
+          float p0 = ex2(t0), p1 = ex2(t1);
+          if (!full) {
+            const int c0 = q * 32 + 2 * i;
+            p0 = c0 < valid ? p0 : 0.f;
+            p1 = c0 + 1 < valid ? p1 : 0.f;
+          }
+          sum2 = fadd2(sum2, f2(p0, p1));
           pk[i] = pack_bf16x2(p0, p1);
         }
         // keys 32q..32q+31 = block q/2, 16-byte chunks (q%2)*4 .. +3
@@ -240,7 +254,9 @@ __global__ void __launch_bounds__(kThreads, 2)
               make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
         }
       }
-      l_run = l_run * alpha + psum;
+      float s_lo, s_hi;
+      f2_split(sum2, s_lo, s_hi);
+      l_run = l_run * alpha + (s_lo + s_hi);
       m_run = m_new;
       fence_proxy_async_smem();                        // P visible to the tensor core
       tc_fence_before();                               // S reads ordered before the arrive
@@ -252,13 +268,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         break;
       }
       tc_fence_after();
+      const uint64_t a2 = f2(alpha, alpha);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t v[32];
         tmem_ld32(tmem_o + lane_off + h * 32, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[h * 32 + i] = fmaf(o[h * 32 + i], alpha, __uint_as_float(v[i]));
+        for (int i = 0; i < 16; ++i)
+          o2[h * 16 + i] =
+              ffma2(o2[h * 16 + i], a2, f2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])));
       }
     }
     if (!ok) {
@@ -268,11 +287,13 @@ __global__ void __launch_bounds__(kThreads, 2)
       const float inv = 1.f / l_run;
       uint4* dst = reinterpret_cast<uint4*>(O + ((int64_t)q_row0 + r) * kD);
 #pragma unroll
-      for (int c = 0; c < kD / 8; ++c)
-        dst[c] = make_uint4(pack_bf16x2(o[8 * c] * inv, o[8 * c + 1] * inv),
-                            pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
-                            pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
-                            pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
+      for (int c = 0; c < kD / 8; ++c) {
+        float o[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) f2_split(o2[4 * c + e], o[2 * e], o[2 * e + 1]);
+        dst[c] = make_uint4(pack_bf16x2(o[0] * inv, o[1] * inv), pack_bf16x2(o[2] * inv, o[3] * inv),
+                            pack_bf16x2(o[4] * inv, o[5] * inv), pack_bf16x2(o[6] * inv, o[7] * inv));
+      }
     }
   }
 

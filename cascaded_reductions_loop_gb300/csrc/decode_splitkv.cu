@@ -3,11 +3,12 @@
 // Multi-segment strategy ([S] Methodologie 3; [E] §3.3 inter-block merge and
 // multi-kernel cooperation): the keys of every (batch, kv head) are cut into
 // S segments.  Kernel 1 (decode_partial_kernel) gives each segment to one
-// CTA, which runs the incremental safe-softmax loop ([E] §2.3, §4.1) over its
-// keys and writes the partial state (m, l, o) -- o unnormalised, m in log2
-// units -- for each of the G query heads that share the kv head.  Kernel 2
-// (decode_merge_kernel) combines the S partial states of every (batch, query
-// head): M = max m_j, L = sum l_j 2^(m_j - M), O = sum o_j 2^(m_j - M) / L.
+// CTA, whose four warps each run the incremental safe-softmax loop ([E] §2.3,
+// §4.1) over every fourth chunk of the segment and write their partial state
+// (m, l, o) -- o unnormalised, m in log2 units -- for each of the G query heads
+// that share the kv head.  Kernel 2 (decode_merge_kernel) combines the 4 S
+// partial states of every (batch, query head): M = max m_j,
+// L = sum l_j 2^(m_j - M), O = sum o_j 2^(m_j - M) / L.
 //
 // Data movement: K and V stream from HBM exactly once, by TMA into 128-byte
 // swizzled shared-memory tiles (chunks of 32 keys x 128 dims, two 64-dim
@@ -62,12 +63,37 @@ __device__ __forceinline__ uint32_t sw_off(int r, int c) {
   return (uint32_t)((c >> 3) * kBoxBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
+// A work item is one key segment of one (batch, kv head): item = (b * Hkv +
+// kvh) * S + seg.  The grid is persistent: CTA c takes items c, c + gridDim.x,
+// ...  Within a CTA, warp w takes chunks w, w + kWarps, ... of each item in
+// turn; its private ring is refilled across item boundaries, so the next
+// item's keys are already in flight while the current item's partial state
+// is merged and written.
+struct DecodeItem {
+  int b, kvh, seg;
+  int64_t lo, hi, row_base;
+  int nchunks;
+};
+
+__device__ __forceinline__ DecodeItem decode_item(int item, int Hkv, int Lk, int S) {
+  DecodeItem it;
+  it.seg = item % S;
+  const int pair = item / S;
+  it.kvh = pair % Hkv;
+  it.b = pair / Hkv;
+  it.lo = (int64_t)it.seg * Lk / S;
+  it.hi = (int64_t)(it.seg + 1) * Lk / S;
+  it.row_base = (int64_t)pair * Lk;
+  it.nchunks = (int)((it.hi - it.lo + kCK - 1) / kCK);
+  return it;
+}
+
 template <int G>
 __global__ void __launch_bounds__(kWarps * 32)
     decode_partial_kernel(const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV,
                           const __nv_bfloat16* __restrict__ Q, float* __restrict__ part_o,
-                          float* __restrict__ part_ml, int Hq, int Hkv, int Lk, int S,
+                          float* __restrict__ part_ml, int Hq, int Hkv, int Lk, int S, int items,
                           float qk_scale_log2, unsigned* err) {
   static_assert(G >= 1 && G <= 8, "query heads per kv head");
   extern __shared__ uint8_t smem_raw[];
@@ -76,14 +102,10 @@ __global__ void __launch_bounds__(kWarps * 32)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * kStages * kStageBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int seg = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-  const int64_t lo = (int64_t)seg * Lk / S, hi = (int64_t)(seg + 1) * Lk / S;
-  const int nchunks = (int)((hi - lo + kCK - 1) / kCK);
-  const int64_t row_base = ((int64_t)b * Hkv + kvh) * Lk;   // first K/V row of this sequence
-
+  const int my_items =
+      items > (int)blockIdx.x ? (items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
   uint8_t* my_stage = smem + warp * kStages * kStageBytes;
   uint64_t* my_full = bars + warp * kStages;
-  const int my_n = nchunks > warp ? (nchunks - warp + kWarps - 1) / kWarps : 0;
 
   if (lane == 0) {
     prefetch_tmap(&tmK);
@@ -94,10 +116,21 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
   __syncwarp();
 
-  auto issue = [&](int i) {   // chunk (warp + i * kWarps) into slot i % kStages
-    const int slot = i % kStages;
-    const int ci = warp + i * kWarps;
-    const int32_t row = (int32_t)(row_base + lo + (int64_t)ci * kCK);
+  // producer cursor over this warp's chunk stream (lane 0 only)
+  int pk = 0, pci = warp, issued = 0;
+  DecodeItem pit = decode_item(my_items > 0 ? (int)blockIdx.x : 0, Hkv, Lk, S);
+  auto skip_empty = [&]() {
+    while (pk < my_items && pci >= pit.nchunks) {
+      ++pk;
+      pci = warp;
+      if (pk < my_items) pit = decode_item((int)blockIdx.x + pk * (int)gridDim.x, Hkv, Lk, S);
+    }
+  };
+  auto issue_next = [&]() {
+    skip_empty();
+    if (pk >= my_items) return;
+    const int slot = issued % kStages;
+    const int32_t row = (int32_t)(pit.row_base + pit.lo + (int64_t)pci * kCK);
     const uint32_t dst = smem_u32(my_stage + slot * kStageBytes);
     const uint32_t bar = smem_u32(&my_full[slot]);
     mbar_arrive_expect_tx(bar, kStageBytes);
@@ -105,167 +138,152 @@ __global__ void __launch_bounds__(kWarps * 32)
     tma_load_2d(dst + kBoxBytes, &tmK, bar, 64, row);
     tma_load_2d(dst + 2 * kBoxBytes, &tmV, bar, 0, row);
     tma_load_2d(dst + 3 * kBoxBytes, &tmV, bar, 64, row);
+    ++issued;
+    pci += kWarps;
   };
   if (lane == 0)
-    for (int i = 0; i < kStages && i < my_n; ++i) issue(i);
+    for (int i = 0; i < kStages; ++i) issue_next();
 
-  // Q as the A operand (rows = the G query heads, zero-padded to 16).
   const int hrow = lane >> 2;           // head of this lane's accumulator rows
   const int kq = (lane & 3) * 2;        // first of this lane's two columns
-  uint32_t qa[8][2];
-  {
-    const uint32_t* qp = reinterpret_cast<const uint32_t*>(
-        Q + ((int64_t)b * Hq + (int64_t)kvh * G + (hrow < G ? hrow : 0)) * kD);
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      qa[ks][0] = hrow < G ? qp[(ks * 16 + kq) >> 1] : 0u;
-      qa[ks][1] = hrow < G ? qp[(ks * 16 + kq + 8) >> 1] : 0u;
-    }
-  }
-
-  float oacc[16][4];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.f;
-  float m_run = -INFINITY, l_run = 0.f;
+  const int mi = lane >> 3, mr = lane & 7;   // ldmatrix: matrix, row within it
+  int consumed = 0;
   bool failed = false;
 
-  // ldmatrix lane roles: matrix mi = lane / 8, row lane % 8 of that matrix.
-  const int mi = lane >> 3, mr = lane & 7;
-
-  int fail_at = -1;
-  for (int i = 0; i < my_n; ++i) {
-    const int slot = i % kStages;
-    bool ok = mbar_wait(smem_u32(&my_full[slot]), (uint32_t)((i / kStages) & 1));
-    ok = __all_sync(0xffffffffu, ok);
-    if (!ok) {
-      failed = true;
-      fail_at = i;
-      break;
+  // Q of the G query heads as the A operand (rows zero-padded to 16); the
+  // next item's Q is loaded while the current item runs.
+  auto load_q = [&](int k, uint32_t (&q)[8][2]) {
+    if (k >= my_items) return;
+    const DecodeItem it = decode_item((int)blockIdx.x + k * (int)gridDim.x, Hkv, Lk, S);
+    const uint32_t* qp = reinterpret_cast<const uint32_t*>(
+        Q + ((int64_t)it.b * Hq + (int64_t)it.kvh * G + (hrow < G ? hrow : 0)) * kD);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      q[ks][0] = hrow < G ? __ldg(qp + ((ks * 16 + kq) >> 1)) : 0u;
+      q[ks][1] = hrow < G ? __ldg(qp + ((ks * 16 + kq + 8) >> 1)) : 0u;
     }
-    const uint32_t kbase = smem_u32(my_stage + slot * kStageBytes);
-    const uint32_t vbase = kbase + 2 * kBoxBytes;
-    const int64_t key0 = lo + (int64_t)(warp + i * kWarps) * kCK;   // first key of the chunk
+  };
+  uint32_t qa[8][2], qn[8][2];
+  load_q(0, qn);
 
-    // ---- S = Q K^T for 32 keys: two 16-key sub-blocks x two 8-key n-blocks
-    float s[2][2][4];
+  for (int k = 0; k < my_items && !failed; ++k) {
+    const DecodeItem it = decode_item((int)blockIdx.x + k * (int)gridDim.x, Hkv, Lk, S);
 #pragma unroll
-    for (int sb = 0; sb < 2; ++sb) {
-      s[sb][0][0] = s[sb][0][1] = s[sb][0][2] = s[sb][0][3] = 0.f;
-      s[sb][1][0] = s[sb][1][1] = s[sb][1][2] = s[sb][1][3] = 0.f;
-      const int krow = sb * 16 + (mi >> 1) * 8 + mr;
+    for (int ks = 0; ks < 8; ++ks) {
+      qa[ks][0] = qn[ks][0];
+      qa[ks][1] = qn[ks][1];
+    }
+    load_q(k + 1, qn);
+    float oacc[16][4];
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        uint32_t r0, r1, r2, r3;
-        ldsm_x4(kbase + sw_off(krow, 2 * ks + (mi & 1)), r0, r1, r2, r3);
-        const uint32_t a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
-        mma16816(s[sb][0], a, r0, r1);
-        mma16816(s[sb][1], a, r2, r3);
+    for (int j = 0; j < 16; ++j) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;
+
+    for (int ci = warp; ci < it.nchunks; ci += kWarps) {
+      const int slot = consumed % kStages;
+      bool ok = mbar_wait(smem_u32(&my_full[slot]), (uint32_t)((consumed / kStages) & 1));
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        failed = true;
+        break;
       }
-    }
+      const uint32_t kbase = smem_u32(my_stage + slot * kStageBytes);
+      const uint32_t vbase = kbase + 2 * kBoxBytes;
+      const int64_t key0 = it.lo + (int64_t)ci * kCK;   // first key of the chunk
 
-    // ---- online softmax for head hrow over this chunk (log2 domain)
-    float mx = -INFINITY;
+      // ---- S = Q K^T for 32 keys: two 16-key sub-blocks x two 8-key n-blocks
+      float sc[2][2][4];
 #pragma unroll
-    for (int sb = 0; sb < 2; ++sb)
+      for (int sb = 0; sb < 2; ++sb) {
+        sc[sb][0][0] = sc[sb][0][1] = sc[sb][0][2] = sc[sb][0][3] = 0.f;
+        sc[sb][1][0] = sc[sb][1][1] = sc[sb][1][2] = sc[sb][1][3] = 0.f;
+        const int krow = sb * 16 + (mi >> 1) * 8 + mr;
 #pragma unroll
-      for (int nb = 0; nb < 2; ++nb)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int64_t key = key0 + sb * 16 + nb * 8 + kq + e;
-          const float v = key < hi ? s[sb][nb][e] * qk_scale_log2 : -INFINITY;
-          s[sb][nb][e] = v;
-          mx = fmaxf(mx, v);
+        for (int ks = 0; ks < 8; ++ks) {
+          uint32_t r0, r1, r2, r3;
+          ldsm_x4(kbase + sw_off(krow, 2 * ks + (mi & 1)), r0, r1, r2, r3);
+          const uint32_t a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
+          mma16816(sc[sb][0], a, r0, r1);
+          mma16816(sc[sb][1], a, r2, r3);
         }
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const float m_new = fmaxf(m_run, mx);          // finite: every chunk has a valid key
-    const float alpha = exp2f(m_run - m_new);      // 0 on the first chunk
-    float psum = 0.f;
-    uint32_t pa[2][2];
-#pragma unroll
-    for (int sb = 0; sb < 2; ++sb)
-#pragma unroll
-      for (int nb = 0; nb < 2; ++nb) {
-        const float p0 = exp2f(s[sb][nb][0] - m_new);
-        const float p1 = exp2f(s[sb][nb][1] - m_new);
-        psum += p0 + p1;
-        pa[sb][nb] = pack_bf16x2(p0, p1);
       }
-    l_run = l_run * alpha + psum;
-    m_run = m_new;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      oacc[j][0] *= alpha;
-      oacc[j][1] *= alpha;
-    }
 
-    // ---- O += P V: A = P (16 rows x 16 keys), B = V (16 keys x 8 dims)
+      // ---- online softmax for head hrow over this chunk (log2 domain)
+      float mx = -INFINITY;
 #pragma unroll
-    for (int sb = 0; sb < 2; ++sb) {
-      const uint32_t a[4] = {pa[sb][0], 0u, pa[sb][1], 0u};
-      const int vrow = sb * 16 + (mi & 1) * 8 + mr;
+      for (int sb = 0; sb < 2; ++sb)
 #pragma unroll
-      for (int j = 0; j < 16; j += 2) {
-        uint32_t r0, r1, r2, r3;
-        ldsm_x4_t(vbase + sw_off(vrow, j + (mi >> 1)), r0, r1, r2, r3);
-        mma16816(oacc[j], a, r0, r1);
-        mma16816(oacc[j + 1], a, r2, r3);
+        for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int64_t key = key0 + sb * 16 + nb * 8 + kq + e;
+            const float v = key < it.hi ? sc[sb][nb][e] * qk_scale_log2 : -INFINITY;
+            sc[sb][nb][e] = v;
+            mx = fmaxf(mx, v);
+          }
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m_run, mx);          // finite: every chunk has a valid key
+      const float alpha = exp2f(m_run - m_new);      // 0 on the first chunk
+      float psum = 0.f;
+      uint32_t pa[2][2];
+#pragma unroll
+      for (int sb = 0; sb < 2; ++sb)
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb) {
+          const float p0 = exp2f(sc[sb][nb][0] - m_new);
+          const float p1 = exp2f(sc[sb][nb][1] - m_new);
+          psum += p0 + p1;
+          pa[sb][nb] = pack_bf16x2(p0, p1);
+        }
+      l_run = l_run * alpha + psum;
+      m_run = m_new;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        oacc[j][0] *= alpha;
+        oacc[j][1] *= alpha;
       }
-    }
 
-    __syncwarp();
-    if (lane == 0 && i + kStages < my_n) issue(i + kStages);
+      // ---- O += P V: A = P (16 rows x 16 keys), B = V (16 keys x 8 dims)
+#pragma unroll
+      for (int sb = 0; sb < 2; ++sb) {
+        const uint32_t a[4] = {pa[sb][0], 0u, pa[sb][1], 0u};
+        const int vrow = sb * 16 + (mi & 1) * 8 + mr;
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
+          uint32_t r0, r1, r2, r3;
+          ldsm_x4_t(vbase + sw_off(vrow, j + (mi >> 1)), r0, r1, r2, r3);
+          mma16816(oacc[j], a, r0, r1);
+          mma16816(oacc[j + 1], a, r2, r3);
+        }
+      }
+
+      __syncwarp();
+      ++consumed;
+      if (lane == 0) issue_next();               // refill the slot just freed
+    }
+    if (failed) break;
+
+    // ---- this warp's partial state of the item (o unnormalised, m in log2
+    // units); a warp without keys in the item writes (-inf, 0, 0)
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+    if (hrow < G) {
+      const int64_t pidx =
+          (((int64_t)it.b * Hq + (int64_t)it.kvh * G + hrow) * S + it.seg) * kWarps + warp;
+      float2* po = reinterpret_cast<float2*>(part_o + pidx * kD);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) po[(j * 8 + kq) >> 1] = make_float2(oacc[j][0], oacc[j][1]);
+      if ((lane & 3) == 0) reinterpret_cast<float2*>(part_ml)[pidx] = make_float2(m_run, l_run);
+    }
   }
 
   if (failed) {
     raise_error(err, kDevErrTimeout);
-    // Chunks fail_at .. min(fail_at + kStages, my_n) - 1 were issued but not
-    // consumed: give their copies a bounded chance to land before the CTA's
-    // shared memory is released.
+    // let this warp's copies still in flight land before shared memory is released
     if (lane == 0)
-      for (int c = fail_at; c < fail_at + kStages && c < my_n; ++c)
+      for (int c = consumed; c < issued; ++c)
         (void)mbar_wait(smem_u32(&my_full[c % kStages]), (uint32_t)((c / kStages) & 1), 1000000ull);
-  }
-
-  // ---- combine the warps' states, then write the segment's partial state
-  l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-  l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-  __syncthreads();                                  // all stages consumed
-  float* wo = reinterpret_cast<float*>(smem);       // [kWarps][G][kD]
-  float* wm = wo + kWarps * G * kD;                 // [kWarps][G]
-  float* wl = wm + kWarps * G;                      // [kWarps][G]
-  if (hrow < G) {
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      wo[(warp * G + hrow) * kD + j * 8 + kq] = oacc[j][0];
-      wo[(warp * G + hrow) * kD + j * 8 + kq + 1] = oacc[j][1];
-    }
-    if ((lane & 3) == 0) {
-      wm[warp * G + hrow] = m_run;
-      wl[warp * G + hrow] = l_run;
-    }
-  }
-  __syncthreads();
-  for (int t = threadIdx.x; t < G * kD; t += kWarps * 32) {
-    const int h = t / kD, dim = t % kD;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * G + h]);
-    float o = 0.f, L = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float sc = exp2f(wm[w * G + h] - M);   // 0 for warps without keys
-        o += wo[(w * G + h) * kD + dim] * sc;
-        L += wl[w * G + h] * sc;
-      }
-    }
-    const int64_t pidx = ((int64_t)b * Hq + (int64_t)kvh * G + h) * S + seg;
-    part_o[pidx * kD + dim] = o;
-    if (dim == 0) {
-      part_ml[pidx * 2] = M;
-      part_ml[pidx * 2 + 1] = L;
-    }
   }
 }
 
@@ -297,13 +315,19 @@ cudaError_t launch_g(const CUtensorMap& tmK, const CUtensorMap& tmV, const void*
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(S, Hkv, B);
+  const int64_t items = (int64_t)B * Hkv * S;
+  if (items >= (1ll << 31)) return cudaErrorInvalidValue;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidValue;
+  const int grid = (int)(items < sms ? items : sms);        // one CTA per SM, persistent
   const float qk_scale_log2 = scale * 1.4426950408889634f;
   kern<<<grid, kWarps * 32, kSmemBytes, s>>>(tmK, tmV, static_cast<const __nv_bfloat16*>(Q),
-                                             part_o, part_ml, Hq, Hkv, Lk, S, qk_scale_log2, err);
+                                             part_o, part_ml, Hq, Hkv, Lk, S, (int)items,
+                                             qk_scale_log2, err);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decode_merge_kernel<<<B * Hq, kD, 0, s>>>(part_o, part_ml, static_cast<__nv_bfloat16*>(O), S);
+  decode_merge_kernel<<<B * Hq, kD, 0, s>>>(part_o, part_ml, static_cast<__nv_bfloat16*>(O),
+                                            S * kWarps);
   return cudaGetLastError();
 }
 
@@ -315,19 +339,28 @@ int decode_num_splits(int B, int Hq, int Hkv, int Lk, int d, int requested) {
   if (requested > 0) return requested;
   const int sms = sm_count();
   if (sms <= 0) return 0;
-  // Aim for about four CTAs per SM in total while keeping segments at least
-  // 256 keys long (eight chunks, two per warp).
+  // The persistent grid has one CTA per SM.  Take the smallest S whose items
+  // (B * Hkv * S) keep the SMs at least 95 % busy (items / (rounds * SMs)),
+  // with segments of at least 128 keys (one chunk per warp); else the best S.
   const int64_t pairs = (int64_t)B * Hkv;
-  int64_t S = (4 * (int64_t)sms + pairs - 1) / pairs;
-  const int64_t max_by_len = (Lk + 255) / 256;
-  if (S > max_by_len) S = max_by_len;
-  if (S < 1) S = 1;
-  if (S > 65535) S = 65535;
-  return (int)S;
+  const int64_t max_s = (Lk + 127) / 128 < 1 ? 1 : (Lk + 127) / 128;
+  int best_s = 1;
+  double best_eff = -1.0;
+  for (int64_t S = 1; S <= max_s && S <= 4096; ++S) {
+    const int64_t items = pairs * S;
+    const int64_t rounds = (items + sms - 1) / sms;
+    const double eff = (double)items / (double)(rounds * sms);
+    if (eff >= 0.95) return (int)S;
+    if (eff > best_eff) {
+      best_eff = eff;
+      best_s = (int)S;
+    }
+  }
+  return best_s;
 }
 
 size_t decode_workspace_bytes(int B, int Hq, int d, int S) {
-  const size_t n = (size_t)B * Hq * S;
+  const size_t n = (size_t)B * Hq * S * kWarps;       // one partial state per warp
   const size_t o_bytes = (n * d * sizeof(float) + 255) & ~(size_t)255;
   return o_bytes + n * 2 * sizeof(float);
 }
@@ -335,13 +368,12 @@ size_t decode_workspace_bytes(int B, int Hq, int d, int S) {
 cudaError_t launch_decode_splitkv(const void* Q, const void* K, const void* V, void* O, int B,
                                   int Hq, int Hkv, int Lk, int d, float scale, int S,
                                   void* workspace, unsigned* err, cudaStream_t s) {
-  if (S > 65535 || Hkv > 65535 || B > 65535) return cudaErrorInvalidValue;
   const uint64_t rows = (uint64_t)B * Hkv * Lk;
   CUtensorMap tmK, tmV;
   if (!encode_tmap_2d(&tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, kD, rows, kD * 2, 64, kCK, true) ||
       !encode_tmap_2d(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, kD, rows, kD * 2, 64, kCK, true))
     return cudaErrorInvalidValue;
-  const size_t n = (size_t)B * Hq * S;
+  const size_t n = (size_t)B * Hq * S * kWarps;
   float* part_o = static_cast<float*>(workspace);
   float* part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
                                             ((n * d * sizeof(float) + 255) & ~(size_t)255));

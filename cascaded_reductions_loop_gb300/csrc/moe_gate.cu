@@ -4,8 +4,9 @@
 // Each CTA owns 128 tokens and one slice of the reduction dimension D; the
 // CTAs covering the slices of the same 128 tokens form a thread-block
 // cluster (split-K).  Per CTA: a TMA producer warp streams 128x64 tiles of x
-// and 64x64 tiles of W_gate (both K-major, 128-byte swizzled) through a
-// 4-stage ring; one thread issues tcgen05.mma kind::f16 (bf16 x bf16 -> fp32,
+// and 64x64 tiles of W_gate (both K-major, 128-byte swizzled), two adjacent
+// tiles of each per stage so that every row's 256 bytes are fetched together,
+// through a 4-stage ring; one thread issues tcgen05.mma kind::f16 (bf16 x bf16 -> fp32,
 // M=128, N=64 experts) into tensor memory.  The epilogue warps copy the
 // partial 128x64 score tile from TMEM to shared memory; after a cluster
 // barrier each CTA sums one quarter of the rows over all cluster peers
@@ -22,9 +23,12 @@ namespace {
 
 constexpr int BM = 128;            // tokens per CTA
 constexpr int kE = 64;             // experts (MMA N)
-constexpr int BK = 64;             // bf16 elements per k-block (128 bytes)
-constexpr int kStages = 4;
-constexpr int kABytes = BM * BK * 2, kBBytes = kE * BK * 2, kStageBytes = kABytes + kBBytes;
+constexpr int BK = 64;             // bf16 elements per TMA box (one 128-byte swizzle row)
+constexpr int kBoxes = 2;          // boxes per stage: each row contributes 256 contiguous bytes
+constexpr int KB = BK * kBoxes;    // bf16 elements per stage (k-block)
+constexpr int kStages = 4;         // 192 KB ring: one CTA per SM
+constexpr int kXBox = BM * BK * 2, kWBox = kE * BK * 2;
+constexpr int kABytes = kBoxes * kXBox, kBBytes = kBoxes * kWBox, kStageBytes = kABytes + kBBytes;
 constexpr int kThreads = 192;      // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kTmemCols = 64;
 constexpr int kRedStride = kE + 4;  // padded fp32 row of the partial-score tile
@@ -122,7 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t crank = cluster_rank(), csize = cluster_size();
   const int m0 = blockIdx.y * BM;
-  const int nkb_total = (D + BK - 1) / BK;
+  const int nkb_total = (D + KB - 1) / KB;
   const int kb0 = (int)crank * kb_per_cta;
   int nk = nkb_total - kb0;
   nk = nk < 0 ? 0 : (nk > kb_per_cta ? kb_per_cta : nk);
@@ -164,8 +168,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* a = smem + slot * kStageBytes;
         const uint32_t bar = smem_u32(&full[slot]);
         mbar_arrive_expect_tx(bar, kStageBytes);
-        tma_load_2d_hint(smem_u32(a), &tmX, bar, (kb0 + i) * BK, m0, pol_x);
-        tma_load_2d_hint(smem_u32(a + kABytes), &tmW, bar, (kb0 + i) * BK, 0, pol_w);
+#pragma unroll
+        for (int bx = 0; bx < kBoxes; ++bx) {
+          const int x = (kb0 + i) * KB + bx * BK;
+          tma_load_2d_hint(smem_u32(a + bx * kXBox), &tmX, bar, x, m0, pol_x);
+          tma_load_2d_hint(smem_u32(a + kABytes + bx * kWBox), &tmW, bar, x, 0, pol_w);
+        }
       }
       if (*abort_flag)
         for (int j = i - kStages < 0 ? 0 : i - kStages; j < i; ++j)
@@ -184,9 +192,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a = smem_u32(smem + slot * kStageBytes);
         const uint32_t b = a + kABytes;
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          mma_bf16_ss(tmem, sw128_desc(a + kk * 32, 1024, 16), sw128_desc(b + kk * 32, 1024, 16),
-                      kIdesc, (i | kk) != 0);
+        for (int kk = 0; kk < KB / 16; ++kk) {
+          const uint32_t ao = (kk / (BK / 16)) * kXBox + (kk % (BK / 16)) * 32;
+          const uint32_t bo = (kk / (BK / 16)) * kWBox + (kk % (BK / 16)) * 32;
+          mma_bf16_ss(tmem, sw128_desc(a + ao, 1024, 16), sw128_desc(b + bo, 1024, 16), kIdesc,
+                      (i | kk) != 0);
+        }
         mma_commit(smem_u32(&empty[slot]));
       }
       mma_commit(smem_u32(accum));
@@ -292,13 +303,26 @@ cudaError_t launch_moe_gate(const void* X, const void* Wg, int T, int D, int E, 
       !encode_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Wg, (uint64_t)D, (uint64_t)kE,
                       (uint64_t)D * 2, BK, kE, true))
     return cudaErrorInvalidValue;
-  // split the reduction over a cluster of up to 4 CTAs, keeping >= 8 k-blocks each
-  const int nkb = (D + BK - 1) / BK;
-  int cs = nkb / 8;
-  cs = cs < 1 ? 1 : (cs > 4 ? 4 : cs);
-  const int kb_per = (nkb + cs - 1) / cs;
+  // Split the reduction over a cluster of cs CTAs (one CTA per SM): pick the
+  // cs in {1, 2, 4, 8} that minimises waves x (k-blocks per CTA + a fixed
+  // per-CTA cost of about three k-blocks for start-up and epilogue).
+  const int nkb = (D + KB - 1) / KB;
   const int tiles = (T + BM - 1) / BM;
   if (tiles > 65535) return cudaErrorInvalidValue;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidValue;
+  int cs = 1;
+  int64_t best = -1;
+  for (int c = 1; c <= 8; c *= 2) {
+    if (c > nkb) break;
+    const int64_t waves = ((int64_t)tiles * c + sms - 1) / sms;
+    const int64_t cost = waves * ((nkb + c - 1) / c + 3);
+    if (best < 0 || cost < best) {
+      best = cost;
+      cs = c;
+    }
+  }
+  const int kb_per = (nkb + cs - 1) / cs;
 
   cudaError_t e = cudaFuncSetAttribute(moe_gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmem);

@@ -70,7 +70,8 @@ def test_validation_rejects_bad_arguments_without_a_gpu(rf):
     # an explicit split count needs no device: a too-small workspace is caught on the host
     assert L.rf_attn_decode_splitkv(p, p, p, p, 1, 8, 2, 64, 128, 0.1, 4, p, 16, None) == rf.RF_ERR_WORKSPACE
     assert L.rf_attn_decode_splitkv(p, p, p, p, 1, 8, 2, 64, 128, 0.1, 4, null, 1 << 20, None) == rf.RF_ERR_WORKSPACE
-    assert rf.rf_attn_decode_splitkv_workspace_size(2, 8, 2, 64, 128, 4) == 2 * 8 * 4 * (128 + 2) * 4
+    # one (m, l, o) partial state per (batch, query head, segment, warp of 4)
+    assert rf.rf_attn_decode_splitkv_workspace_size(2, 8, 2, 64, 128, 4) == 2 * 8 * 4 * 4 * (128 + 2) * 4
     assert rf.rf_attn_decode_splitkv_num_splits(1, 6, 4, 64, 128, 0) == 0
     # MoE: D not a multiple of 8, k out of range, E not covered
     assert L.rf_moe_gate_topk_softmax(p, p, 16, 100, 64, 2, p, p, None) == rf.RF_ERR_INVALID_ARG

@@ -85,3 +85,51 @@ def test_fp8_zero_row_and_signed_zero(rf):
     ref_sx, ref_xq, ref_y = F.absmax_fp8_gemm(x, wq, sw)
     np.testing.assert_array_equal(xq, ref_xq)
     assert_fp8_y_close(y, ref_y, "zero rows")
+
+
+def _domain_rows(a_lo, a_hi):
+    """Rows of 4096 bf16 covering every pair (row max a, x) with |x| <= a for
+    a's bit pattern in [a_lo, a_hi): element 0 is a, then 2047 magnitudes m
+    (both signs) of block b of a's range, zeros where m > a."""
+    a_list, b_list = [], []
+    for a in range(a_lo, a_hi):
+        nb = a // 2047 + 1
+        a_list += [a] * nb
+        b_list += range(nb)
+    a_t = torch.tensor(a_list, dtype=torch.int32, device="cuda")[:, None]
+    b_t = torch.tensor(b_list, dtype=torch.int32, device="cuda")[:, None]
+    mag = b_t * 2047 + torch.arange(2047, dtype=torch.int32, device="cuda")[None, :]
+    valid = mag <= a_t
+    pos = torch.where(valid, mag, torch.zeros_like(mag))
+    neg = torch.where(valid, mag | 0x8000, torch.zeros_like(mag))
+    body = torch.stack([pos, neg], dim=2).reshape(len(a_list), 4094)
+    bits = torch.cat([a_t, body, torch.zeros_like(a_t)], dim=1)          # 4096 columns
+    return bits.to(torch.int16).view(torch.bfloat16).contiguous()
+
+
+def test_quantisation_exhaustive_against_ieee_division(rf):
+    """Every bf16 x against every positive finite bf16 row max a >= |x|: the
+    kernel's codes equal E4M3(fp32(x / sx)) with an IEEE fp32 division (torch's
+    CUDA division) and torch's float8_e4m3fn cast; sx = a / 448 likewise."""
+    wq = torch.zeros(16, 4096, dtype=torch.uint8, device="cuda")
+    sw = torch.ones(16, dtype=torch.float32, device="cuda")
+    total = 0
+    step = 2048
+    for a_lo in range(1, 0x7F80, step):
+        x = _domain_rows(a_lo, min(a_lo + step, 0x7F80))
+        M = x.shape[0]
+        y = torch.empty(M, 16, dtype=torch.bfloat16, device="cuda")
+        sx = torch.empty(M, dtype=torch.float32, device="cuda")
+        xq = torch.empty(M, 4096, dtype=torch.uint8, device="cuda")
+        rf.rf_absmax_fp8_gemm(x, wq, sw, y, sx_out=sx, xq_out=xq)
+        assert rf.rf_get_device_status() == rf.RF_OK
+        # tensor / tensor: an IEEE division (dividing by a Python scalar would
+        # multiply by its reciprocal instead)
+        ref_sx = x[:, 0].float() / torch.full((M,), 448.0, device="cuda")
+        assert torch.equal(sx.view(torch.int32), ref_sx.view(torch.int32))
+        t = x.float() / ref_sx[:, None]
+        ref = t.to(torch.float8_e4m3fn).view(torch.uint8)
+        bad = (xq != ref).nonzero()
+        assert bad.numel() == 0, f"{bad.shape[0]} codes differ, first (row, col) {bad[:3].tolist()}"
+        total += M * 4095
+    assert total > 1_000_000_000
