@@ -14,6 +14,12 @@ k_i with values v_i,
 ``attention_incremental`` and ``attention_segments`` are the method's own
 single-loop and multi-segment forms, kept here only so that the tests can
 show they equal the three-pass definition on small inputs.
+
+Causal masking (an option of the fused loop the explainer presents for
+prefill, [E] §4.1): the pages do not define it, so the usual autoregressive
+reading is taken, aligned so that the last query row sees every key: with
+off = Lk - Lq, query row i reads keys j <= i + off only.  A row that reads no
+key at all (i + off < 0, possible only when Lq > Lk) is defined as zero.
 """
 from __future__ import annotations
 
@@ -36,8 +42,17 @@ def kv_head_of(hq: int, Hq: int, Hkv: int) -> int:
     return hq // (Hq // Hkv)
 
 
+def causal_limit(iq: int, Lq: int, Lk: int) -> int:
+    """Number of leading keys query row iq may read under the causal mask
+    (clamped to 0..Lk)."""
+    return max(0, min(Lk, iq + (Lk - Lq) + 1))
+
+
 def three_pass_row(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float) -> np.ndarray:
-    """One query row q [d] against K [Lk,d], V [Lk,d]; returns o [d] (fp64)."""
+    """One query row q [d] against K [Lk,d], V [Lk,d]; returns o [d] (fp64).
+    With no keys (Lk = 0, a fully masked causal row) the result is zero."""
+    if K.shape[0] == 0:
+        return np.zeros(V.shape[1])
     s = scale * (K @ q)            # scores
     m = s.max()                    # pass 1: max
     l = np.exp(s - m).sum()        # pass 2: sum of exp(s - m)
@@ -56,14 +71,16 @@ def probabilities(q, k, v, scale: float, b: int, hq: int) -> np.ndarray:
     return np.exp(s - m) / l
 
 
-def attention(q, k, v, scale: float, rows=None) -> np.ndarray:
+def attention(q, k, v, scale: float, rows=None, causal: bool = False) -> np.ndarray:
     """Three-pass attention.
 
     q: [B, Hq, Lq, d]; k, v: [B, Hkv, Lk, d] (any float dtype; converted to
     fp64 exactly).  Returns fp64 O [B, Hq, Lq, d], or, when ``rows`` is a
     list of (b, hq, iq) triples, O for those rows only as [len(rows), d].
+    ``causal``: row iq reads only the first causal_limit(iq, Lq, Lk) keys.
     """
     Hq, Hkv = q.shape[1], k.shape[1]
+    Lq, Lk = q.shape[2], k.shape[2]
     if rows is None:
         B, _, Lq, d = q.shape
         out = np.empty((B, Hq, Lq, d), dtype=np.float64)
@@ -73,6 +90,11 @@ def attention(q, k, v, scale: float, rows=None) -> np.ndarray:
                 Q = _f64(q[b, hq])
                 K = _f64(k[b, kvh])
                 V = _f64(v[b, kvh])
+                if causal:
+                    for iq in range(Lq):
+                        n = causal_limit(iq, Lq, Lk)
+                        out[b, hq, iq] = three_pass_row(Q[iq], K[:n], V[:n], scale)
+                    continue
                 s = scale * (Q @ K.T)                        # [Lq, Lk]
                 m = s.max(axis=1, keepdims=True)             # pass 1
                 l = np.exp(s - m).sum(axis=1, keepdims=True)  # pass 2
@@ -86,7 +108,8 @@ def attention(q, k, v, scale: float, rows=None) -> np.ndarray:
             cache.clear()
             cache[(b, kvh)] = (_f64(k[b, kvh]), _f64(v[b, kvh]))
         K, V = cache[(b, kvh)]
-        res[i] = three_pass_row(_f64(q[b, hq, iq]), K, V, scale)
+        n = causal_limit(iq, Lq, Lk) if causal else Lk
+        res[i] = three_pass_row(_f64(q[b, hq, iq]), K[:n], V[:n], scale)
     return res
 
 

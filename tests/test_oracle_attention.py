@@ -142,3 +142,61 @@ def test_planted_mistakes_are_caught():
     bad = sum(p[2] for p in parts) / sum(p[1] for p in parts)
     assert np.abs(bad - ref).max() > 1e-3
     np.testing.assert_allclose(A.merge_partials(parts), ref, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------- causal mask
+
+
+@pytest.mark.parametrize("L", [1, 6, 33])
+def test_causal_square_matches_library_sdpa(L):
+    """Lq = Lk: torch's fp64 SDPA with is_causal=True (lower-triangular
+    mask) is the same mask under either alignment convention."""
+    q = torch.from_numpy(_rand(40, 2, 3, L, 16))
+    k = torch.from_numpy(_rand(41, 2, 3, L, 16))
+    v = torch.from_numpy(_rand(42, 2, 3, L, 16))
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True, scale=0.4)
+    np.testing.assert_allclose(A.attention(q, k, v, 0.4, causal=True), ref.numpy(),
+                               rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(A.attention(q, k, v, 0.4, causal=True)[:, :, 0],
+                                  v[:, :, 0].numpy())      # row 0 reads key 0 only
+
+
+@pytest.mark.parametrize("Lq,Lk", [(5, 40), (17, 18), (1, 9)])
+def test_causal_bottom_right_matches_library_sdpa_with_mask(Lq, Lk):
+    """Lq <= Lk: row i reads keys 0 .. i + Lk - Lq, i.e. the boolean mask
+    tril(ones(Lq, Lk), diagonal = Lk - Lq) given to torch's SDPA."""
+    q = torch.from_numpy(_rand(43, 1, 2, Lq, 8))
+    k = torch.from_numpy(_rand(44, 1, 2, Lk, 8))
+    v = torch.from_numpy(_rand(45, 1, 2, Lk, 8))
+    mask = torch.ones(Lq, Lk, dtype=torch.bool).tril(diagonal=Lk - Lq)
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=0.6)
+    np.testing.assert_allclose(A.attention(q, k, v, 0.6, causal=True), ref.numpy(),
+                               rtol=1e-12, atol=1e-12)
+    if Lq == 1:      # one query row sees every key: the causal result is the unmasked one
+        np.testing.assert_array_equal(A.attention(q, k, v, 0.6, causal=True),
+                                      A.attention(q, k, v, 0.6))
+
+
+def test_causal_uniform_scores_give_running_mean_of_v():
+    """Q = 0: every visible key has the same weight, so row i is the mean of
+    the first i + Lk - Lq + 1 rows of V (closed form via a cumulative sum)."""
+    Lq, Lk, d = 12, 20, 4
+    q = np.zeros((1, 1, Lq, d))
+    k, v = _rand(46, 1, 1, Lk, d), _rand(47, 1, 1, Lk, d)
+    o = A.attention(q, k, v, 1.0, causal=True)[0, 0]
+    csum = np.cumsum(v[0, 0], axis=0)
+    n = np.arange(Lq) + (Lk - Lq) + 1
+    np.testing.assert_allclose(o, csum[n - 1] / n[:, None], rtol=0, atol=1e-14)
+
+
+def test_causal_rows_without_keys_are_zero():
+    """Lq > Lk: rows i < Lq - Lk read no key and are zero by definition; the
+    remaining rows match the square case on the last Lk query rows."""
+    Lq, Lk = 10, 4
+    q, k, v = _rand(48, 1, 1, Lq, 8), _rand(49, 1, 1, Lk, 8), _rand(50, 1, 1, Lk, 8)
+    o = A.attention(q, k, v, 0.5, causal=True)[0, 0]
+    np.testing.assert_array_equal(o[:Lq - Lk], 0.0)
+    sq = A.attention(q[:, :, Lq - Lk:], k, v, 0.5, causal=True)[0, 0]
+    np.testing.assert_array_equal(o[Lq - Lk:], sq)
+    rows = [(0, 0, i) for i in range(Lq)]
+    np.testing.assert_array_equal(A.attention(q, k, v, 0.5, causal=True, rows=rows), o)
