@@ -46,7 +46,8 @@ def test_moe_gate_full(rf):
 
 
 @pytest.mark.parametrize("T,D,k", [(300, 256, 2), (1, 64, 1), (129, 1024, 4), (64, 4096, 8),
-                                   (513, 200, 2), (256, 2048, 3), (100, 8, 2)])
+                                   (513, 200, 2), (256, 2048, 3), (100, 8, 2), (4000, 4096, 2),
+                                   (777, 65536, 2)])
 def test_moe_gate_small(rf, T, D, k):
     x, w = I.moe_inputs(I.MoEShape(T=T, D=D, E=64, k=k, seed=T + D + k))
     idx, wts = _run(rf, x, w, k)
