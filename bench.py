@@ -112,10 +112,45 @@ def make_ops():
     ]
 
 
+def make_extra_ops():
+    """Calls measured on request (--only) but not part of the step: the
+    causal-mask variant of the prefill workload (FLOPs count only the
+    (query, key) pairs the mask lets through)."""
+    b = I.BERT_PREFILL
+    pairs = sum(min(b.Lk, i + (b.Lk - b.Lq) + 1) for i in range(b.Lq))
+    ops = [Op("bert_prefill_causal", 4 * b.B * b.Hq * b.Lq * b.d * 2,
+              4 * b.B * b.Hq * pairs * b.d, "bf16", 1)]
+    for name, m in MOE_EXTRA.items():
+        ops.append(Op(name, m.T * m.D * 2 + m.E * m.D * 2 + m.T * m.k * 8, 2 * m.T * m.D * m.E,
+                      "bf16", 1))
+    v = I.PREFILL_VARLEN
+    lens = varlen_lengths()
+    ops.append(Op("prefill_varlen", 4 * sum(lens) * v.H * v.d * 2,
+                  4 * v.H * v.d * sum(n * n for n in lens), "bf16", 1))
+    return ops
+
+
+def varlen_lengths():
+    cu = I.varlen_inputs(I.PREFILL_VARLEN)[3]
+    return (cu[1:] - cu[:-1]).tolist()
+
+
+# Gate shapes outside the step: the step's token count and width with 8
+# experts / top-2 and 256 experts / top-8.
+MOE_EXTRA = {
+    "moe_gate_e8_k2": I.MoEShape(T=8192, D=4096, E=8, k=2, seed=41),
+    "moe_gate_e256_k8": I.MoEShape(T=8192, D=4096, E=256, k=8, seed=42),
+}
+
+
 GENERATORS = {
     "decode_32k": lambda: list(I.decode_inputs(I.DECODE_32K)),
     "decode_2k": lambda: list(I.decode_inputs(I.DECODE_2K)),
     "bert_prefill": lambda: list(I.attention_inputs(I.BERT_PREFILL)),
+    "bert_prefill_causal": lambda: list(I.attention_inputs(I.BERT_PREFILL)),
+    "prefill_varlen": lambda: list(I.varlen_inputs(I.PREFILL_VARLEN)),
+    "moe_gate_e8_k2": lambda: list(I.moe_inputs(MOE_EXTRA["moe_gate_e8_k2"])),
+    "moe_gate_e256_k8": lambda: list(I.moe_inputs(MOE_EXTRA["moe_gate_e256_k8"])),
     "moe_gate": lambda: list(I.moe_inputs(I.MOE_GATE)),
     "fp8_gemm": lambda: list(I.fp8_inputs(I.FP8_GEMM)),
 }
@@ -160,15 +195,34 @@ class Step:
             "decode_32k": lambda: rf.rf_attn_decode_splitkv(*d["decode_32k"], self.o32, s32.scale,
                                                             self.ws32, args_splits(32768)),
             "bert_prefill": lambda: rf.rf_attn_fwd(*d["bert_prefill"], self.ob, sb.scale),
+            "bert_prefill_causal": lambda: rf.rf_attn_fwd(*d["bert_prefill_causal"], self.ob,
+                                                          sb.scale, 1),
             "moe_gate": lambda: rf.rf_moe_gate_topk_softmax(*d["moe_gate"], sm.k, self.idx,
                                                             self.wts),
             "fp8_gemm": lambda: rf.rf_absmax_fp8_gemm(*d["fp8_gemm"], self.y, workspace=self.wsf),
             "decode_2k": lambda: rf.rf_attn_decode_splitkv(*d["decode_2k"], self.o2, s2.scale,
                                                            self.ws2, args_splits(2048)),
         }
+        if "prefill_varlen" in d:
+            qv, kv_, vv, cuv = d["prefill_varlen"]
+            self.ov = torch.empty_like(qv)
+            maxlen = int((cuv[1:] - cuv[:-1]).max().item())
+            self.calls["prefill_varlen"] = lambda: rf.rf_attn_fwd_varlen(
+                qv, kv_, vv, self.ov, cuv, cuv, maxlen, I.PREFILL_VARLEN.scale)
+        for name, m in MOE_EXTRA.items():
+            ix = torch.empty(m.T, m.k, dtype=torch.int32, device=cuda)
+            wt = torch.empty(m.T, m.k, dtype=torch.float32, device=cuda)
+            self.calls[name] = (lambda name=name, m=m, ix=ix, wt=wt:
+                                rf.rf_moe_gate_topk_softmax(*d[name], m.k, ix, wt))
+            setattr(self, "out_" + name, [ix, wt])
         self.outputs = {"decode_32k": [self.o32], "decode_2k": [self.o2],
-                        "bert_prefill": [self.ob], "moe_gate": [self.idx, self.wts],
+                        "bert_prefill": [self.ob], "bert_prefill_causal": [self.ob],
+                        "moe_gate": [self.idx, self.wts],
                         "fp8_gemm": [self.y]}
+        for name in MOE_EXTRA:
+            self.outputs[name] = getattr(self, "out_" + name)
+        if "prefill_varlen" in d:
+            self.outputs["prefill_varlen"] = [self.ov]
 
 
 # ------------------------------------------------------------------ clocks
@@ -353,7 +407,7 @@ def run_ours(args, world, rank, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; shapes of the five named workloads)",
-        "config": {"workload": "decode32k+bert_prefill+moe_gate+fp8_gemm+decode2k",
+        "config": {"workload": workload_name(ops),
                    "decode": "B32 Hq32 Hkv8 d128 Lk {32768, 2048} bf16",
                    "prefill": "B8 H16 L512 d64 bf16", "moe": "T8192 D4096 E64 top2 bf16",
                    "fp8": "M=N=K=4096 e4m3 (bf16 X in, bf16 Y out)",
@@ -377,11 +431,18 @@ def select_ops(args):
     ops = make_ops()
     if args.only:
         names = args.only.split(",")
-        unknown = set(names) - {op.name for op in ops}
+        known = ops + make_extra_ops()
+        unknown = set(names) - {op.name for op in known}
         if unknown:
             raise SystemExit(f"unknown op(s) {sorted(unknown)}")
-        ops = [op for op in ops if op.name in names]
+        ops = [op for op in known if op.name in names]
     return ops
+
+
+def workload_name(ops):
+    if [op.name for op in ops] == [op.name for op in make_ops()]:
+        return "decode32k+bert_prefill+moe_gate+fp8_gemm+decode2k"
+    return "+".join(op.name for op in ops)
 
 
 def run_e2e(rf, ops, peaks, host, step, world, args):
@@ -456,6 +517,17 @@ def oracle_sample_seconds(host, frac):
             A.attention(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1], s.scale)
         out["bert_prefill"] = (time.perf_counter() - t, nh / (s.B * s.Hq))
 
+    if "bert_prefill_causal" in host:
+        s = I.BERT_PREFILL
+        q, k, v = host["bert_prefill_causal"]
+        nh = max(1, int(round(frac * 4 * s.B * s.Hq)))
+        t = time.perf_counter()
+        for i in range(nh):
+            b, h = divmod(i % (s.B * s.Hq), s.Hq)
+            A.attention(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1], s.scale,
+                        causal=True)
+        out["bert_prefill_causal"] = (time.perf_counter() - t, nh / (s.B * s.Hq))
+
     if "moe_gate" in host:
         s = I.MOE_GATE
         x, w = host["moe_gate"]
@@ -463,6 +535,29 @@ def oracle_sample_seconds(host, frac):
         t = time.perf_counter()
         G.moe_gate(x, w, s.k, rows=range(nt))
         out["moe_gate"] = (time.perf_counter() - t, nt / s.T)
+
+    if "prefill_varlen" in host:
+        q, k, v, cu = host["prefill_varlen"]
+        nseq = len(cu) - 1
+        tot = sum(int(cu[b + 1] - cu[b]) ** 2 for b in range(nseq))
+        done, b = 0, 0
+        t = time.perf_counter()
+        while done < frac * 4 * tot and b < nseq:   # whole sequences until the sample is covered
+            sl = slice(int(cu[b]), int(cu[b + 1]))
+            one = cu[b:b + 2] - cu[b]                   # [0, length]
+            A.attention_varlen(q[sl], k[sl], v[sl], one, one, I.PREFILL_VARLEN.scale)
+            done += int(cu[b + 1] - cu[b]) ** 2
+            b += 1
+        out["prefill_varlen"] = (time.perf_counter() - t, done / tot)
+
+    for name, m in MOE_EXTRA.items():
+        if name not in host:
+            continue
+        x, w = host[name]
+        nt = max(1, int(round(frac * 4 * m.T)))
+        t = time.perf_counter()
+        G.moe_gate(x, w, m.k, rows=range(nt))
+        out[name] = (time.perf_counter() - t, nt / m.T)
 
     if "fp8_gemm" in host:
         s = I.FP8_GEMM
@@ -521,7 +616,7 @@ def run_reference(args, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(full_s * 1e3, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded; shapes of the five named workloads)",
-        "config": {"workload": "decode32k+bert_prefill+moe_gate+fp8_gemm+decode2k",
+        "config": {"workload": workload_name(ops),
                    "parallelism": "CPU oracle, rank 0 only"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                          "sample": f"{frac:.5f} of each op's rows/heads/tokens per step, "
@@ -537,7 +632,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--only", default="",
                     help="comma-separated subset of ops (decode_32k, bert_prefill, moe_gate, "
-                         "fp8_gemm, decode_2k); default: the whole step")
+                         "fp8_gemm, decode_2k) or calls outside the step (bert_prefill_causal, prefill_varlen, "
+                         "moe_gate_e8_k2, moe_gate_e256_k8); "
+                         "default: the whole step")
     ap.add_argument("--splits", default="",
                     help="explicit decode split counts, e.g. 32768:64,2048:8 (default: automatic)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")

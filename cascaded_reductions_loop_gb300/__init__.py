@@ -20,16 +20,17 @@ from . import _build
 
 __all__ = [
     "RFError", "lib", "rf_status_string", "rf_version", "rf_get_device_status",
-    "rf_attn_fwd", "rf_attn_decode_splitkv", "rf_attn_decode_splitkv_num_splits",
+    "rf_attn_fwd", "rf_attn_fwd_varlen", "rf_attn_decode_splitkv",
+    "rf_attn_decode_splitkv_num_splits",
     "rf_attn_decode_splitkv_workspace_size", "rf_attn_decode_splitkv_noalloc",
     "RF_DECODE_NOALLOC_SCRATCH_BYTES", "rf_moe_gate_topk_softmax",
     "rf_absmax_fp8_gemm", "rf_absmax_fp8_gemm_workspace_size", "rf_selftest_wait_timeout",
     "RF_OK", "RF_ERR_INVALID_ARG", "RF_ERR_UNSUPPORTED", "RF_ERR_WORKSPACE", "RF_ERR_CUDA",
-    "RF_ERR_DEVICE_TIMEOUT", "RF_F32", "RF_BF16",
+    "RF_ERR_DEVICE_TIMEOUT", "RF_ERR_DEVICE_INPUT", "RF_F32", "RF_BF16",
 ]
 
 RF_OK, RF_ERR_INVALID_ARG, RF_ERR_UNSUPPORTED, RF_ERR_WORKSPACE, RF_ERR_CUDA, \
-    RF_ERR_DEVICE_TIMEOUT = range(6)
+    RF_ERR_DEVICE_TIMEOUT, RF_ERR_DEVICE_INPUT = range(7)
 RF_F32, RF_BF16 = 0, 1
 RF_DECODE_NOALLOC_SCRATCH_BYTES = 16 << 20   # as in rf.h
 
@@ -53,6 +54,7 @@ _SIGS = {
     "rf_version": (_I, []),
     "rf_get_device_status": (_I, [_P]),
     "rf_attn_fwd": (_I, [_I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "rf_attn_fwd_varlen": (_I, [_I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "rf_attn_decode_splitkv_num_splits": (_I, [_I, _I, _I, _I, _I, _I]),
     "rf_attn_decode_splitkv_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I]),
     "rf_attn_decode_splitkv": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
@@ -131,6 +133,30 @@ def rf_attn_fwd(q, k, v, o, scale: float, causal: int = 0, stream=None) -> None:
     code = RF_F32 if dt == torch.float32 else RF_BF16
     _check(lib.rf_attn_fwd(code, _ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, Lq, Lk, d,
                            float(scale), int(causal), _stream(stream)), "rf_attn_fwd")
+
+
+def rf_attn_fwd_varlen(q, k, v, o, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, scale: float,
+                       causal: int = 0, stream=None) -> None:
+    """Fused attention over packed variable-length sequences.  q, o:
+    [total_q,H,d]; k, v: [total_k,H,d]; cu_seqlens_q/k: int32 CUDA tensors
+    of B+1 cumulative lengths (not read on the host)."""
+    total_q, H, d = q.shape
+    total_k = k.shape[0]
+    B = cu_seqlens_q.shape[0] - 1
+    dt = q.dtype
+    if dt not in (torch.float32, torch.bfloat16):
+        raise ValueError("q must be float32 or bfloat16")
+    _need(q, dt, (total_q, H, d), "q")
+    _need(k, dt, (total_k, H, d), "k")
+    _need(v, dt, (total_k, H, d), "v")
+    _need(o, dt, (total_q, H, d), "o")
+    _need(cu_seqlens_q, torch.int32, (B + 1,), "cu_seqlens_q")
+    _need(cu_seqlens_k, torch.int32, (B + 1,), "cu_seqlens_k")
+    code = RF_F32 if dt == torch.float32 else RF_BF16
+    _check(lib.rf_attn_fwd_varlen(code, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(cu_seqlens_q),
+                                  _ptr(cu_seqlens_k), B, H, int(max_seqlen_q), total_q, total_k,
+                                  d, float(scale), int(causal), _stream(stream)),
+           "rf_attn_fwd_varlen")
 
 
 def rf_attn_decode_splitkv_num_splits(B, Hq, Hkv, Lk, d, num_splits=0) -> int:

@@ -54,29 +54,50 @@ int sm_count() {
   return g_sm_count[dev];
 }
 
+// cuTensorMapEncodeTiled, looked up once through the runtime (no libcuda link).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return nullptr;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return g_encode;
+}
+
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
                     uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
                     bool swizzle128) {
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_encode) {
-      void* fn = nullptr;
-      cudaDriverEntryPointQueryResult q;
-      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                           &q) != cudaSuccess ||
-          q != cudaDriverEntryPointSuccess || !fn)
-        return false;
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
-  }
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return false;
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {row_bytes};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t d0,
+                    uint64_t d1, uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes,
+                    uint32_t b0, uint32_t b1, uint32_t b2, bool swizzle128) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = encode(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -126,6 +147,8 @@ const char* rf_status_string(int status) {
     case RF_ERR_WORKSPACE: return "RF_ERR_WORKSPACE: workspace missing or too small";
     case RF_ERR_CUDA: return "RF_ERR_CUDA: CUDA runtime call or kernel launch failed";
     case RF_ERR_DEVICE_TIMEOUT: return "RF_ERR_DEVICE_TIMEOUT: a kernel's bounded wait ran out";
+    case RF_ERR_DEVICE_INPUT:
+      return "RF_ERR_DEVICE_INPUT: device-side sizes (cu_seqlens) were inconsistent";
     default: return "unknown rf_status";
   }
 }
@@ -141,14 +164,16 @@ rf_status rf_get_device_status(rf_stream_t stream) {
     const unsigned zero = 0;
     if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) return RF_ERR_CUDA;
   }
-  return (v & kDevErrTimeout) ? RF_ERR_DEVICE_TIMEOUT : RF_OK;
+  if (v & kDevErrTimeout) return RF_ERR_DEVICE_TIMEOUT;
+  return (v & kDevErrInput) ? RF_ERR_DEVICE_INPUT : RF_OK;
 }
 
 rf_status rf_attn_fwd(int dtype, const void* Q, const void* K, const void* V, void* O, int B,
                       int H, int Lq, int Lk, int d, float scale, int causal, rf_stream_t stream) {
   if (dtype != RF_F32 && dtype != RF_BF16) return RF_ERR_INVALID_ARG;
   if (!ptr_ok(Q) || !ptr_ok(K) || !ptr_ok(V) || !ptr_ok(O)) return RF_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || Lq < 1 || Lk < 1 || d < 1 || causal != 0) return RF_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Lq < 1 || Lk < 1 || d < 1 || (causal != 0 && causal != 1))
+    return RF_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !(scale < INFINITY)) return RF_ERR_INVALID_ARG;
   if ((int64_t)B * H * Lq >= (1ll << 31) || (int64_t)B * H * Lk >= (1ll << 31))
     return RF_ERR_INVALID_ARG;
@@ -158,12 +183,43 @@ rf_status rf_attn_fwd(int dtype, const void* Q, const void* K, const void* V, vo
     return from_cuda(launch_attn_fwd_f32(static_cast<const float*>(Q),
                                          static_cast<const float*>(K),
                                          static_cast<const float*>(V), static_cast<float*>(O), B,
-                                         H, Lq, Lk, d, scale, s));
+                                         H, Lq, Lk, d, scale, causal, s));
   }
   if (d != 64) return RF_ERR_UNSUPPORTED;
   unsigned* err = device_error_word();
   if (!err) return RF_ERR_CUDA;
-  return from_cuda(launch_attn_fwd_bf16_tc(Q, K, V, O, B, H, Lq, Lk, d, scale, err, s));
+  return from_cuda(launch_attn_fwd_bf16_tc(Q, K, V, O, B, H, Lq, Lk, d, scale, causal, err, s));
+}
+
+rf_status rf_attn_fwd_varlen(int dtype, const void* Q, const void* K, const void* V, void* O,
+                             const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int B,
+                             int H, int max_seqlen_q, int total_q, int total_k, int d,
+                             float scale, int causal, rf_stream_t stream) {
+  if (dtype != RF_F32 && dtype != RF_BF16) return RF_ERR_INVALID_ARG;
+  if (!ptr_ok(Q) || !ptr_ok(K) || !ptr_ok(V) || !ptr_ok(O)) return RF_ERR_INVALID_ARG;
+  if (!cu_seqlens_q || !cu_seqlens_k || (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3) ||
+      (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3))
+    return RF_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || max_seqlen_q < 1 || total_q < 1 || total_k < 1 || d < 1 ||
+      (causal != 0 && causal != 1))
+    return RF_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !(scale < INFINITY)) return RF_ERR_INVALID_ARG;
+  if ((int64_t)total_q * H >= (1ll << 31) || (int64_t)total_k * H >= (1ll << 31) ||
+      (int64_t)B * H > 65535)
+    return RF_ERR_INVALID_ARG;
+  if (dtype == RF_F32 ? (d != 64 && d != 128) : d != 64) return RF_ERR_UNSUPPORTED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned* err = device_error_word();
+  if (!err) return RF_ERR_CUDA;
+  if (dtype == RF_F32) {
+    return from_cuda(launch_attn_fwd_f32_varlen(
+        static_cast<const float*>(Q), static_cast<const float*>(K), static_cast<const float*>(V),
+        static_cast<float*>(O), cu_seqlens_q, cu_seqlens_k, B, H, max_seqlen_q, total_q, total_k,
+        d, scale, causal, err, s));
+  }
+  return from_cuda(launch_attn_fwd_bf16_tc_varlen(Q, K, V, O, cu_seqlens_q, cu_seqlens_k, B, H,
+                                                  max_seqlen_q, total_q, total_k, scale, causal,
+                                                  err, s));
 }
 
 static rf_status decode_shape_check(int B, int Hq, int Hkv, int Lk, int d, int num_splits) {
@@ -211,7 +267,7 @@ rf_status rf_moe_gate_topk_softmax(const void* X, const void* Wg, int T, int D, 
   if (!ptr_ok(X) || !ptr_ok(Wg) || !ptr_ok(idx) || !ptr_ok(w)) return RF_ERR_INVALID_ARG;
   if (T < 1 || D < 1 || E < 1 || k < 1 || k > E) return RF_ERR_INVALID_ARG;
   if (D % 8 != 0) return RF_ERR_INVALID_ARG;   // 16-byte row pitch for TMA
-  if (E != 64 || k > 8) return RF_ERR_UNSUPPORTED;
+  if (E > 256 || k > 8) return RF_ERR_UNSUPPORTED;
   unsigned* err = device_error_word();
   if (!err) return RF_ERR_CUDA;
   return from_cuda(launch_moe_gate(X, Wg, T, D, E, k, idx, w, err,

@@ -18,6 +18,19 @@
 // After the last tile each thread writes o / l as bf16.  S and P never
 // leave the SM.  A TMA warp streams Q once and K/V tiles through a 2-stage
 // ring; every wait is bounded.
+//
+// Causal mask: row i reads keys j <= i + (Lk - Lq).  A CTA walks only the
+// key tiles its rows can read; tiles below the diagonal take the unmasked
+// path, the diagonal tiles mask per element, and within each (batch, head)
+// the query tiles with the most key tiles are launched first.  A row that
+// reads no key is written as zero.
+//
+// Two layouts: fixed-length [B][H][L][64] (2-D tensor maps over rows of 128
+// bytes), and packed variable-length sequences [total][H][64] delimited by
+// cumulative lengths cu_seqlens[B + 1] (3-D tensor maps over (dim, head,
+// token) with a box of 64 x 1 x 128, which lands in shared memory exactly
+// like the 2-D box).  Tiles that run past a sequence read the next
+// sequence's tokens (or zeros past the end of the tensor) and are masked.
 #include <math.h>
 
 #include "rf_device.cuh"
@@ -59,20 +72,70 @@ struct Bars {
   int abort;
 };
 
+// Sizes and addressing of the (sequence, head) a CTA works on.  Fixed
+// layout: tile rows are 2-D coordinates (row = bh * L + i).  Varlen: 3-D
+// coordinates (dim, head, token); sizes that contradict the host-side totals
+// are reported and the sequence is skipped.
+struct Seq {
+  int Lq, Lk, h;
+  int32_t q0, k0;       // first row (fixed) or first token (varlen)
+  int64_t o0;           // element offset of row 0 of O
+  int64_t o_stride;     // elements between consecutive rows of O
+  bool ok;
+};
+
+__device__ __forceinline__ Seq seq_of_cta(int Lq_, int Lk_, const int* cu_q, const int* cu_k,
+                                          int H, int total_q, int total_k, unsigned* err) {
+  Seq q;
+  if (!cu_q) {
+    const int64_t bh = blockIdx.y;
+    q = {Lq_, Lk_, 0, (int32_t)(bh * Lq_), (int32_t)(bh * Lk_), bh * Lq_ * kD, kD, true};
+    return q;
+  }
+  const int b = blockIdx.y / H, h = blockIdx.y % H;
+  const int q0 = cu_q[b], q1 = cu_q[b + 1], k0 = cu_k[b], k1 = cu_k[b + 1];
+  q.ok = 0 <= q0 && q0 <= q1 && q1 <= total_q && q1 - q0 <= Lq_ && 0 <= k0 && k0 <= k1 &&
+         k1 <= total_k;
+  if (!q.ok) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) raise_error(err, kDevErrInput);
+    return q;
+  }
+  q.Lq = q1 - q0;
+  q.Lk = k1 - k0;
+  q.h = h;
+  q.q0 = q0;
+  q.k0 = k0;
+  q.o0 = ((int64_t)q0 * H + h) * kD;
+  q.o_stride = (int64_t)H * kD;
+  return q;
+}
+
+template <bool kVarlen>
 __global__ void __launch_bounds__(kThreads, 2)
     attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
-                         int Lq, int Lk, float c_log2, unsigned* err) {
+                         int Lq_, int Lk_, float c_log2, int causal, const int* __restrict__ cu_q,
+                         const int* __restrict__ cu_k, int H, int total_q, int total_k,
+                         unsigned* err) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Bars* bars = reinterpret_cast<Bars*>(smem + kBarOff);
   volatile int* abort_flag = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = blockIdx.x;
-  const int64_t bh = blockIdx.y;
-  const int nkv = (Lk + BKV - 1) / BKV;
-  const int32_t q_row0 = (int32_t)(bh * Lq + (int64_t)qt * BQ);
-  const int32_t kv_row0 = (int32_t)(bh * Lk);
+  // causal: heavier query tiles (more key tiles) first
+  const int qt = causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+  const Seq sq = seq_of_cta(Lq_, Lk_, kVarlen ? cu_q : nullptr, cu_k, H, total_q, total_k, err);
+  if (!sq.ok || qt * BQ >= sq.Lq) return;           // uniform over the CTA, before any barrier
+  const int Lq = sq.Lq, Lk = sq.Lk;
+  const int off = Lk - Lq;                          // causal: row i reads keys <= i + off
+  int nkv = (Lk + BKV - 1) / BKV;
+  if (causal) {
+    const int last_row = min(qt * BQ + BQ - 1, Lq - 1);
+    const int keys = max(0, min(Lk, last_row + off + 1));
+    nkv = (keys + BKV - 1) / BKV;
+  }
+  const int32_t q_row0 = sq.q0 + qt * BQ;           // row (fixed) or token (varlen)
+  const int32_t kv_row0 = sq.k0;
 
   if ((smem_u32(smem) & 1023u) != 0) {   // swizzled tiles need 1 KB alignment
     if (threadIdx.x == 0) raise_error(err, kDevErrTimeout);
@@ -110,7 +173,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       // ------------------------------------------------ TMA producer
       const uint64_t pol_kv = policy_evict_last();   // K/V tiles are read by Lq/128 CTAs
       mbar_arrive_expect_tx(smem_u32(&bars->q_full), kTileBytes);
-      tma_load_2d(smem_u32(smem + kQOff), &tmQ, smem_u32(&bars->q_full), 0, q_row0);
+      if (kVarlen)
+        tma_load_3d(smem_u32(smem + kQOff), &tmQ, smem_u32(&bars->q_full), 0, sq.h, q_row0);
+      else
+        tma_load_2d(smem_u32(smem + kQOff), &tmQ, smem_u32(&bars->q_full), 0, q_row0);
       int j = 0;
       for (; j < nkv; ++j) {
         const int slot = j % kKV;
@@ -123,10 +189,17 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (*abort_flag) break;
         const uint32_t bar = smem_u32(&bars->kv_full[slot]);
         mbar_arrive_expect_tx(bar, 2 * kTileBytes);
-        tma_load_2d_hint(smem_u32(smem + kKOff + slot * kTileBytes), &tmK, bar, 0,
-                         kv_row0 + j * BKV, pol_kv);
-        tma_load_2d_hint(smem_u32(smem + kVOff + slot * kTileBytes), &tmV, bar, 0,
-                         kv_row0 + j * BKV, pol_kv);
+        if (kVarlen) {
+          tma_load_3d_hint(smem_u32(smem + kKOff + slot * kTileBytes), &tmK, bar, 0, sq.h,
+                           kv_row0 + j * BKV, pol_kv);
+          tma_load_3d_hint(smem_u32(smem + kVOff + slot * kTileBytes), &tmV, bar, 0, sq.h,
+                           kv_row0 + j * BKV, pol_kv);
+        } else {
+          tma_load_2d_hint(smem_u32(smem + kKOff + slot * kTileBytes), &tmK, bar, 0,
+                           kv_row0 + j * BKV, pol_kv);
+          tma_load_2d_hint(smem_u32(smem + kVOff + slot * kTileBytes), &tmV, bar, 0,
+                           kv_row0 + j * BKV, pol_kv);
+        }
       }
       if (*abort_flag) {
         (void)mbar_wait(smem_u32(&bars->q_full), 0, 1000000ull);
@@ -153,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         return true;
       };
       bool ok = mbar_wait(smem_u32(&bars->q_full), 0);
-      ok = ok && issue_s(0);
+      ok = ok && (nkv == 0 || issue_s(0));
       for (int j = 0; ok && j < nkv; ++j) {
         const int slot = j % kKV;
         if (!mbar_wait(smem_u32(&bars->p_full), (uint32_t)(j & 1))) {
@@ -201,8 +274,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         break;
       }
       tc_fence_after();
-      const int valid = min(BKV, Lk - j * BKV);        // keys of this tile that exist
-      const bool full = valid == BKV;                  // uniform over the CTA
+      int valid = min(BKV, Lk - j * BKV);              // keys of this tile that exist
+      bool full = valid == BKV;                        // uniform over the CTA
+      if (causal) {
+        // every row of the CTA reads the whole tile iff its first row does
+        full = full && qt * BQ + off + 1 - j * BKV >= BKV;
+        valid = max(0, min(valid, qt * BQ + r + off + 1 - j * BKV));   // per row
+      }
       // pass 1: row max of the raw scores
       float mx = -INFINITY;
 #pragma unroll
@@ -221,8 +299,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
       const float m_new = fmaxf(m_run, mx * c_log2);
-      const float alpha = ex2(m_run - m_new);          // 0 on the first tile
-      const uint64_t negm2 = f2(-m_new, -m_new);
+      // -inf only while the row has read no key (a causal row above the
+      // first visible key): then every P is masked to 0 and alpha is 0
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
+      const float alpha = ex2(m_run - m_use);          // 0 on the first tile
+      const uint64_t negm2 = f2(-m_use, -m_use);
       // pass 2: P = 2^(S c - m'), row sum, P -> swizzled bf16 tile
       uint64_t sum2 = 0ull;
 #pragma unroll
@@ -284,8 +365,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       raise_error(err, kDevErrTimeout);
       *abort_flag = 1;
     } else if (qt * BQ + r < Lq) {
-      const float inv = 1.f / l_run;
-      uint4* dst = reinterpret_cast<uint4*>(O + ((int64_t)q_row0 + r) * kD);
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;   // no key read: O = 0
+      uint4* dst = reinterpret_cast<uint4*>(O + sq.o0 + (int64_t)(qt * BQ + r) * sq.o_stride);
 #pragma unroll
       for (int c = 0; c < kD / 8; ++c) {
         float o[8];
@@ -308,8 +389,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 }  // namespace
 
 cudaError_t launch_attn_fwd_bf16_tc(const void* Q, const void* K, const void* V, void* O, int B,
-                                    int H, int Lq, int Lk, int d, float scale, unsigned* err,
-                                    cudaStream_t s) {
+                                    int H, int Lq, int Lk, int d, float scale, int causal,
+                                    unsigned* err, cudaStream_t s) {
   (void)d;
   CUtensorMap tmQ, tmK, tmV;
   const uint64_t q_rows = (uint64_t)B * H * Lq, kv_rows = (uint64_t)B * H * Lk;
@@ -317,14 +398,40 @@ cudaError_t launch_attn_fwd_bf16_tc(const void* Q, const void* K, const void* V,
       !encode_tmap_2d(&tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, kD, kv_rows, kD * 2, kD, BKV, true) ||
       !encode_tmap_2d(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, kD, kv_rows, kD * 2, kD, BKV, true))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_bf16_kernel,
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_bf16_kernel<false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   dim3 grid((Lq + BQ - 1) / BQ, B * H);
   if (grid.y > 65535u) return cudaErrorInvalidValue;
   const float c_log2 = scale * 1.4426950408889634f;
-  attn_fwd_bf16_kernel<<<grid, kThreads, kSmem, s>>>(tmQ, tmK, tmV, static_cast<__nv_bfloat16*>(O),
-                                                     Lq, Lk, c_log2, err);
+  attn_fwd_bf16_kernel<false><<<grid, kThreads, kSmem, s>>>(
+      tmQ, tmK, tmV, static_cast<__nv_bfloat16*>(O), Lq, Lk, c_log2, causal, nullptr, nullptr, H,
+      0, 0, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_fwd_bf16_tc_varlen(const void* Q, const void* K, const void* V, void* O,
+                                           const int* cu_q, const int* cu_k, int B, int H,
+                                           int max_q, int total_q, int total_k, float scale,
+                                           int causal, unsigned* err, cudaStream_t s) {
+  CUtensorMap tmQ, tmK, tmV;
+  const uint64_t pitch = (uint64_t)H * kD * 2;     // bytes between tokens
+  if (!encode_tmap_3d(&tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Q, kD, H, total_q, kD * 2, pitch,
+                      kD, 1, BQ, true) ||
+      !encode_tmap_3d(&tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, kD, H, total_k, kD * 2, pitch,
+                      kD, 1, BKV, true) ||
+      !encode_tmap_3d(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, kD, H, total_k, kD * 2, pitch,
+                      kD, 1, BKV, true))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_bf16_kernel<true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((max_q + BQ - 1) / BQ, B * H);
+  if (grid.y > 65535u) return cudaErrorInvalidValue;
+  const float c_log2 = scale * 1.4426950408889634f;
+  attn_fwd_bf16_kernel<true><<<grid, kThreads, kSmem, s>>>(
+      tmQ, tmK, tmV, static_cast<__nv_bfloat16*>(O), max_q, 0, c_log2, causal, cu_q, cu_k, H,
+      total_q, total_k, err);
   return cudaGetLastError();
 }
 

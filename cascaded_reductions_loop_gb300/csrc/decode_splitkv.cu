@@ -8,7 +8,10 @@
 // (m, l, o) -- o unnormalised, m in log2 units -- for each of the G query heads
 // that share the kv head.  Kernel 2 (decode_merge_kernel) combines the 4 S
 // partial states of every (batch, query head): M = max m_j,
-// L = sum l_j 2^(m_j - M), O = sum o_j 2^(m_j - M) / L.
+// L = sum l_j 2^(m_j - M), O = sum o_j 2^(m_j - M) / L.  (Merging inside
+// kernel 1, by the last warp to finish a group, was measured slower: each
+// warp must make its states visible with a fence before taking a ticket, and
+// the merging warp falls behind the others.)
 //
 // Data movement: K and V stream from HBM exactly once, by TMA into 128-byte
 // swizzled shared-memory tiles (chunks of 32 keys x 128 dims, two 64-dim
@@ -143,6 +146,8 @@ __global__ void __launch_bounds__(kWarps * 32)
   };
   if (lane == 0)
     for (int i = 0; i < kStages; ++i) issue_next();
+  // the merge kernel may be scheduled now; it waits for this grid to finish
+  asm volatile("griddepcontrol.launch_dependents;");
 
   const int hrow = lane >> 2;           // head of this lane's accumulator rows
   const int kq = (lane & 3) * 2;        // first of this lane's two columns
@@ -287,24 +292,63 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
 }
 
-// One CTA per (batch, query head): merge the S partial states.
-__global__ void __launch_bounds__(kD)
-    decode_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
-                        __nv_bfloat16* __restrict__ O, int S) {
-  const int64_t bh = blockIdx.x;
-  const int dim = threadIdx.x;
-  const float* ml = part_ml + bh * S * 2;
-  float M = -INFINITY;
-  for (int j = 0; j < S; ++j) M = fmaxf(M, ml[2 * j]);
-  float L = 0.f, o = 0.f;
-  for (int j = 0; j < S; ++j) {
-    const float mj = ml[2 * j];
-    if (mj == -INFINITY) continue;                 // empty segment
-    const float w = exp2f(mj - M);
-    L += ml[2 * j + 1] * w;
-    o += part_o[(bh * S + j) * kD + dim] * w;
+// Merge kernel: one warp per (batch, query head), lane = 4 consecutive dims.
+// Lane j holds the (m, l) of state j of each block of 32 states and hands its
+// weight 2^(m_j - M) to the other lanes by shuffle; o is read 16 states at a
+// time so that those loads are in flight together.  It is launched as a
+// programmatic dependent of the partial kernel: its CTAs may start while the
+// partial kernel drains and wait (griddepcontrol.wait) until that grid has
+// finished and its writes are visible.
+constexpr int kMergeWarps = 4;
+
+__device__ __forceinline__ float4 o_block16(const float4* po, int j0, int n, float w,
+                                            float4 acc) {
+  float4 o[16];
+  if (n >= 16) {                     // common case: no per-load condition
+#pragma unroll
+    for (int u = 0; u < 16; ++u) o[u] = po[(int64_t)(j0 + u) * (kD / 4)];
+  } else {
+#pragma unroll
+    for (int u = 0; u < 16; ++u)
+      o[u] = u < n ? po[(int64_t)(j0 + u) * (kD / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  O[bh * kD + dim] = __float2bfloat16_rn(o / L);
+#pragma unroll
+  for (int u = 0; u < 16; ++u) {
+    const float wu = __shfl_sync(0xffffffffu, w, (j0 + u) & 31);
+    acc.x = fmaf(o[u].x, wu, acc.x);
+    acc.y = fmaf(o[u].y, wu, acc.y);
+    acc.z = fmaf(o[u].z, wu, acc.z);
+    acc.w = fmaf(o[u].w, wu, acc.w);
+  }
+  return acc;
+}
+
+__global__ void __launch_bounds__(kMergeWarps * 32)
+    decode_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
+                        __nv_bfloat16* __restrict__ O, int n_heads, int P) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const int64_t bh = (int64_t)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
+  if (bh >= n_heads) return;
+  const float2* ml = reinterpret_cast<const float2*>(part_ml) + bh * P;
+  const float4* po = reinterpret_cast<const float4*>(part_o + bh * P * kD) + lane;
+  float M = -INFINITY;
+  for (int j = lane; j < P; j += 32) M = fmaxf(M, ml[j].x);
+  M = warp_max(M);                                 // finite: some segment has keys
+  float L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j0 = 0; j0 < P; j0 += 32) {
+    const float2 v = j0 + lane < P ? ml[j0 + lane] : make_float2(-INFINITY, 0.f);
+    const float w = exp2f(v.x - M);                // 0 for empty states
+    L += v.y * w;
+    acc = o_block16(po, j0, P - j0, w, acc);
+    if (P - j0 > 16) acc = o_block16(po, j0 + 16, P - j0 - 16, w, acc);
+  }
+  const float inv = 1.f / warp_sum(L);
+  uint2 out;
+  out.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+  out.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  reinterpret_cast<uint2*>(O + bh * kD)[lane] = out;
 }
 
 template <int G>
@@ -326,9 +370,19 @@ cudaError_t launch_g(const CUtensorMap& tmK, const CUtensorMap& tmV, const void*
                                              qk_scale_log2, err);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decode_merge_kernel<<<B * Hq, kD, 0, s>>>(part_o, part_ml, static_cast<__nv_bfloat16*>(O),
-                                            S * kWarps);
-  return cudaGetLastError();
+  const int n_heads = B * Hq;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((n_heads + kMergeWarps - 1) / kMergeWarps, 1, 1);
+  cfg.blockDim = dim3(kMergeWarps * 32, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_merge_kernel, (const float*)part_o,
+                            (const float*)part_ml, static_cast<__nv_bfloat16*>(O), n_heads,
+                            S * kWarps);
 }
 
 }  // namespace

@@ -25,15 +25,34 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
                     uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
                     uint32_t box_outer, bool swizzle128);
 
+// 3-D tiled tensor map: extents d0 (contiguous), d1, d2 with byte strides of
+// dims 1 and 2; box b0 x b1 x b2.  Returns false on failure.
+bool encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t d0,
+                    uint64_t d1, uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes,
+                    uint32_t b0, uint32_t b1, uint32_t b2, bool swizzle128);
+
 // ---------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error.  Arguments are pre-validated.
 
+// causal = 1: query row i reads keys j <= i + (Lk - Lq) only.
 cudaError_t launch_attn_fwd_f32(const float* Q, const float* K, const float* V, float* O, int B,
-                                int H, int Lq, int Lk, int d, float scale, cudaStream_t s);
+                                int H, int Lq, int Lk, int d, float scale, int causal,
+                                cudaStream_t s);
 
 cudaError_t launch_attn_fwd_bf16_tc(const void* Q, const void* K, const void* V, void* O, int B,
-                                    int H, int Lq, int Lk, int d, float scale, unsigned* err,
-                                    cudaStream_t s);
+                                    int H, int Lq, int Lk, int d, float scale, int causal,
+                                    unsigned* err, cudaStream_t s);
+
+// Packed variable-length layout: Q/O [total_q][H][d], K/V [total_k][H][d],
+// sequence b = tokens cu_q[b] .. cu_q[b+1]-1 (device arrays of B + 1 int32).
+cudaError_t launch_attn_fwd_f32_varlen(const float* Q, const float* K, const float* V, float* O,
+                                       const int* cu_q, const int* cu_k, int B, int H,
+                                       int max_q, int total_q, int total_k, int d, float scale,
+                                       int causal, unsigned* err, cudaStream_t s);
+cudaError_t launch_attn_fwd_bf16_tc_varlen(const void* Q, const void* K, const void* V, void* O,
+                                           const int* cu_q, const int* cu_k, int B, int H,
+                                           int max_q, int total_q, int total_k, float scale,
+                                           int causal, unsigned* err, cudaStream_t s);
 
 int decode_num_splits(int B, int Hq, int Hkv, int Lk, int d, int requested);
 size_t decode_workspace_bytes(int B, int Hq, int d, int S);

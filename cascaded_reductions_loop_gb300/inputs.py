@@ -10,6 +10,9 @@ are built for):
 
 * attention: Q, K, V ~ N(0, 1) drawn in fp32 from a seeded torch CPU
   generator, then cast to the kernel dtype (round-to-nearest-even for bf16).
+* variable-length prefill: per-sequence lengths drawn uniformly from a range
+  with a seeded generator; Q, K, V ~ N(0, 1) packed token-major
+  [total, H, d] (no padding), with the cumulative lengths as int32.
 * MoE gate: x and W_gate hold integers drawn uniformly from {-2, ..., 2}, cast
   to bf16 (exact).  W_gate is stored expert-major, [E][D] (the layout of a
   linear layer's weight), so that both GEMM operands are contiguous along D.
@@ -113,6 +116,45 @@ def decode_inputs(shape: AttnShape):
     assert shape.Lq == 1
     q, k, v = attention_inputs(shape)
     return q.reshape(shape.B, shape.Hq, shape.d).contiguous(), k, v
+
+
+@dataclass(frozen=True)
+class VarlenShape:
+    """A batch of B sequences (query length = key length per sequence) with
+    lengths drawn uniformly from [len_lo, len_hi], or given in ``lens``."""
+    B: int
+    H: int
+    d: int
+    len_lo: int
+    len_hi: int
+    dtype: str
+    seed: int
+    lens: tuple = ()
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+
+# A packed batch of BERT-style sequences of mixed length (no padding).
+PREFILL_VARLEN = VarlenShape(B=16, H=16, d=64, len_lo=64, len_hi=1024, dtype="bf16", seed=6)
+
+
+def varlen_inputs(shape: VarlenShape):
+    """q, k, v [total, H, d] and cu_seqlens int32 [B + 1] (queries and keys
+    share the lengths)."""
+    g = _gen(shape.seed)
+    if shape.lens:
+        lens = torch.tensor(shape.lens, dtype=torch.int64)
+    else:
+        lens = torch.randint(shape.len_lo, shape.len_hi + 1, (shape.B,), generator=g)
+    cu = torch.zeros(len(lens) + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(lens, 0).to(torch.int32)
+    total = int(cu[-1])
+    q = _cast(_normal(g, (total, shape.H, shape.d)), shape.dtype)
+    k = _cast(_normal(g, (total, shape.H, shape.d)), shape.dtype)
+    v = _cast(_normal(g, (total, shape.H, shape.d)), shape.dtype)
+    return q, k, v, cu
 
 
 def moe_inputs(shape: MoEShape):

@@ -50,7 +50,8 @@ typedef enum {
   RF_ERR_UNSUPPORTED = 2,     /* valid request this build does not cover    */
   RF_ERR_WORKSPACE = 3,       /* workspace missing or too small             */
   RF_ERR_CUDA = 4,            /* a CUDA runtime call or launch failed       */
-  RF_ERR_DEVICE_TIMEOUT = 5   /* a kernel's bounded wait ran out            */
+  RF_ERR_DEVICE_TIMEOUT = 5,  /* a kernel's bounded wait ran out            */
+  RF_ERR_DEVICE_INPUT = 6     /* device-resident sizes were inconsistent    */
 } rf_status;
 
 typedef enum { RF_F32 = 0, RF_BF16 = 1 } rf_dtype;
@@ -64,7 +65,10 @@ int rf_version(void);
 /*
  * Synchronises `stream`, then reads and clears the device-side error word of
  * the current device.  Returns RF_OK, RF_ERR_DEVICE_TIMEOUT (some kernel gave
- * up on a bounded wait and returned early; its outputs are incomplete) or
+ * up on a bounded wait and returned early; its outputs are incomplete),
+ * RF_ERR_DEVICE_INPUT (a kernel found device-resident sizes, such as the
+ * cumulative sequence lengths of rf_attn_fwd_varlen, inconsistent with the
+ * host-side sizes; it skipped that work and wrote nothing out of bounds) or
  * RF_ERR_CUDA (the synchronisation itself failed).
  */
 rf_status rf_get_device_status(rf_stream_t stream);
@@ -85,13 +89,41 @@ rf_status rf_get_device_status(rf_stream_t stream);
  *   Sizes   B, H, Lq, Lk >= 1 (B*H*Lq and B*H*Lk below 2^31);
  *           d = 64 (both dtypes) or 128 (RF_F32 only).
  *   scale   finite and > 0 (the usual 1/sqrt(d)).
- *   causal  must be 0 (the cascade as defined has no mask).
- * Errors: RF_ERR_INVALID_ARG (null/misaligned pointer, size < 1, causal != 0,
- * bad dtype), RF_ERR_UNSUPPORTED (d not covered), RF_ERR_CUDA.
+ *   causal  0: every row reads every key.  1: autoregressive mask aligned
+ *           to the end of the keys (the pages define no mask; this is the
+ *           usual reading): row i reads keys j <= i + (Lk - Lq) only, so the
+ *           last row reads all Lk keys; a row that reads no key (possible
+ *           only when Lq > Lk) is written as zeros.
+ * Errors: RF_ERR_INVALID_ARG (null/misaligned pointer, size < 1, causal not
+ * 0 or 1, bad dtype), RF_ERR_UNSUPPORTED (d not covered), RF_ERR_CUDA.
  */
 rf_status rf_attn_fwd(int dtype, const void* Q, const void* K, const void* V, void* O,
                       int B, int H, int Lq, int Lk, int d, float scale, int causal,
                       rf_stream_t stream);
+
+/*
+ * rf_attn_fwd over a batch of sequences of different lengths, packed
+ * token-major without padding (the same computation per sequence and head,
+ * including the causal option):
+ *   Q, O   [total_q][H][d];  K, V  [total_k][H][d]  (bf16 or fp32 as dtype).
+ *   cu_seqlens_q, cu_seqlens_k   DEVICE int32 arrays of B + 1 cumulative
+ *          lengths: sequence b owns query tokens cu_seqlens_q[b] ..
+ *          cu_seqlens_q[b+1]-1 and key tokens cu_seqlens_k[b] ..
+ *          cu_seqlens_k[b+1]-1; entry 0 is 0, entries never decrease, the
+ *          last equals total_q (total_k).  Lengths may be 0; a sequence with
+ *          no keys gives zero rows.
+ *   max_seqlen_q   >= every query length (sizes the grid).
+ *   total_q, total_k >= 1.  d = 64 (both dtypes) or 128 (RF_F32 only).
+ * The host does not read the device arrays.  A kernel that finds them
+ * inconsistent with max_seqlen_q / total_q / total_k skips that sequence,
+ * touches nothing out of bounds and makes rf_get_device_status report
+ * RF_ERR_DEVICE_INPUT.
+ * Errors: RF_ERR_INVALID_ARG, RF_ERR_UNSUPPORTED, RF_ERR_CUDA.
+ */
+rf_status rf_attn_fwd_varlen(int dtype, const void* Q, const void* K, const void* V, void* O,
+                             const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int B,
+                             int H, int max_seqlen_q, int total_q, int total_k, int d,
+                             float scale, int causal, rf_stream_t stream);
 
 /*
  * Number of key segments rf_attn_decode_splitkv uses for this shape when its
@@ -107,20 +139,22 @@ size_t rf_attn_decode_splitkv_workspace_size(int B, int Hq, int Hkv, int Lk, int
 
 /*
  * Multi-segment (split-KV) fused decode attention ([S] Methodologie 3,
- * multi-segment strategy; [E] §3.3 inter-block merge and multi-kernel
- * cooperation).  One query token per (b, query head):
+ * multi-segment strategy; [E] §3.3 inter-block merge).  One query token per
+ * (b, query head):
  *   Q   [B][Hq][d] bf16;  K, V  [B][Hkv][Lk][d] bf16;  O  [B][Hq][d] bf16.
  * Grouped-query attention: query head hq reads K/V head hq / (Hq / Hkv).
- * Kernel 1 splits each (b, kv head) sequence into S key segments and writes,
- * per (b, hq, segment), the partial state (m, l, o) with o unnormalised
- * (m in log2 units); kernel 2 merges them: M = max m_j,
- * L = sum l_j 2^(m_j - M), O = sum o_j 2^(m_j - M) / L.
+ * Kernel 1 (persistent) splits each (b, kv head) sequence into S key
+ * segments and writes, per (b, hq, segment, warp), the partial state
+ * (m, l, o) with o unnormalised (m in log2 units); kernel 2 merges the
+ * states of each (b, hq): M = max m_j, L = sum l_j 2^(m_j - M),
+ * O = sum o_j 2^(m_j - M) / L.
  *   Sizes   B, Lk >= 1; d = 128; Hq / Hkv in {1, 2, 4, 8}; scale finite, > 0.
  *   num_splits  0 = automatic, else 1..Lk segments.
  *   workspace   device buffer of at least
  *               rf_attn_decode_splitkv_workspace_size(...) bytes, 16-byte
  *               aligned, owned by the caller; holds the partial states
- *               between the two kernels (contents on return unspecified).
+ *               between the two kernels.  Its contents need not be
+ *               initialised and are unspecified on return.
  * Errors: RF_ERR_INVALID_ARG, RF_ERR_UNSUPPORTED, RF_ERR_WORKSPACE, RF_ERR_CUDA.
  */
 rf_status rf_attn_decode_splitkv(const void* Q, const void* K, const void* V, void* O,
@@ -166,10 +200,11 @@ rf_status rf_attn_decode_splitkv_noalloc(const void* Q, const void* K, const voi
  *   idx    [T][k] int32 out: selected experts by descending score, equal
  *          scores by ascending expert index.
  *   w      [T][k] fp32 out: softmax of the selected scores (same order).
- *   Sizes  T >= 1; D >= 1 with D % 8 == 0; E = 64; 1 <= k <= 8.
+ *   Sizes  T >= 1; D >= 1 with D % 8 == 0; 1 <= E <= 256; 1 <= k <= min(8, E).
  * Scores are accumulated in fp32 on the tensor cores (exact when every
  * partial sum is an integer below 2^24, e.g. small-integer inputs).
- * Errors: RF_ERR_INVALID_ARG, RF_ERR_UNSUPPORTED, RF_ERR_CUDA.
+ * Errors: RF_ERR_INVALID_ARG (null/misaligned pointer, size < 1, k > E,
+ * D % 8 != 0), RF_ERR_UNSUPPORTED (E > 256 or k > 8), RF_ERR_CUDA.
  */
 rf_status rf_moe_gate_topk_softmax(const void* X, const void* Wg, int T, int D, int E, int k,
                                    int32_t* idx, float* w, rf_stream_t stream);

@@ -113,6 +113,29 @@ def attention(q, k, v, scale: float, rows=None, causal: bool = False) -> np.ndar
     return res
 
 
+def attention_varlen(q, k, v, cu_q, cu_k, scale: float, causal: bool = False) -> np.ndarray:
+    """Packed variable-length batch: q [total_q, H, d], k/v [total_k, H, d];
+    sequence b owns query tokens cu_q[b]..cu_q[b+1]-1 and key tokens
+    cu_k[b]..cu_k[b+1]-1.  Each sequence is the three-pass attention of its
+    own tokens (with the causal option); a sequence without keys gives zero
+    rows.  Returns fp64 [total_q, H, d]."""
+    q64, k64, v64 = _f64(q), _f64(k), _f64(v)
+    cq = [int(x) for x in _f64(cu_q)]
+    ck = [int(x) for x in _f64(cu_k)]
+    out = np.zeros_like(q64)
+    for b in range(len(cq) - 1):
+        if cq[b + 1] == cq[b]:
+            continue
+        Qb = q64[cq[b]:cq[b + 1]].transpose(1, 0, 2)[None]      # [1, H, Lq, d]
+        Kb = k64[ck[b]:ck[b + 1]].transpose(1, 0, 2)[None]
+        Vb = v64[ck[b]:ck[b + 1]].transpose(1, 0, 2)[None]
+        Lq = Qb.shape[2]
+        rows = [(0, h, i) for h in range(Qb.shape[1]) for i in range(Lq)]
+        ob = attention(Qb, Kb, Vb, scale, rows=rows, causal=causal)   # [H*Lq, d]
+        out[cq[b]:cq[b + 1]] = ob.reshape(Qb.shape[1], Lq, -1).transpose(1, 0, 2)
+    return out
+
+
 def decode_attention(q, k, v, scale: float, rows=None) -> np.ndarray:
     """Decode layout: q [B, Hq, d] (one query token), k/v [B, Hkv, Lk, d].
     Returns [B, Hq, d], or [len(rows), d] for a list of (b, hq) pairs."""

@@ -57,11 +57,20 @@ def test_validation_rejects_bad_arguments_without_a_gpu(rf):
     assert L.rf_attn_fwd(1, null, p, p, p, 1, 1, 64, 64, 64, 0.125, 0, None) == rf.RF_ERR_INVALID_ARG
     assert L.rf_attn_fwd(1, mis, p, p, p, 1, 1, 64, 64, 64, 0.125, 0, None) == rf.RF_ERR_INVALID_ARG
     assert L.rf_attn_fwd(1, p, p, p, p, 0, 1, 64, 64, 64, 0.125, 0, None) == rf.RF_ERR_INVALID_ARG
-    assert L.rf_attn_fwd(1, p, p, p, p, 1, 1, 64, 64, 64, 0.125, 1, None) == rf.RF_ERR_INVALID_ARG
+    assert L.rf_attn_fwd(1, p, p, p, p, 1, 1, 64, 64, 64, 0.125, 2, None) == rf.RF_ERR_INVALID_ARG
+    assert L.rf_attn_fwd(1, p, p, p, p, 1, 1, 64, 64, 64, 0.125, -1, None) == rf.RF_ERR_INVALID_ARG
     assert L.rf_attn_fwd(7, p, p, p, p, 1, 1, 64, 64, 64, 0.125, 0, None) == rf.RF_ERR_INVALID_ARG
     assert L.rf_attn_fwd(1, p, p, p, p, 1, 1, 64, 64, 64, -1.0, 0, None) == rf.RF_ERR_INVALID_ARG
     assert L.rf_attn_fwd(1, p, p, p, p, 1, 1, 64, 64, 96, 0.125, 0, None) == rf.RF_ERR_UNSUPPORTED
     assert L.rf_attn_fwd(0, p, p, p, p, 1, 1, 64, 64, 48, 0.125, 0, None) == rf.RF_ERR_UNSUPPORTED
+    # varlen attention: missing cumulative lengths, bad totals, causal, head dim
+    V = L.rf_attn_fwd_varlen
+    assert V(1, p, p, p, p, null, p, 2, 4, 64, 100, 100, 64, 0.125, 0, None) == rf.RF_ERR_INVALID_ARG
+    assert V(1, p, p, p, p, p, p, 2, 4, 64, 0, 100, 64, 0.125, 0, None) == rf.RF_ERR_INVALID_ARG
+    assert V(1, p, p, p, p, p, p, 2, 4, 0, 100, 100, 64, 0.125, 0, None) == rf.RF_ERR_INVALID_ARG
+    assert V(1, p, p, p, p, p, p, 2, 4, 64, 100, 100, 64, 0.125, 3, None) == rf.RF_ERR_INVALID_ARG
+    assert V(1, p, p, p, p, p, p, 2, 4, 64, 100, 100, 128, 0.125, 0, None) == rf.RF_ERR_UNSUPPORTED
+    assert V(0, p, p, p, p, p, p, 2, 4, 64, 100, 100, 96, 0.125, 0, None) == rf.RF_ERR_UNSUPPORTED
     # decode: Hq not a multiple of Hkv, unsupported group / head dim, too many splits
     assert L.rf_attn_decode_splitkv(p, p, p, p, 1, 6, 4, 64, 128, 0.1, 0, p, 1 << 20, None) == rf.RF_ERR_INVALID_ARG
     assert L.rf_attn_decode_splitkv(p, p, p, p, 1, 12, 4, 64, 128, 0.1, 0, p, 1 << 20, None) == rf.RF_ERR_UNSUPPORTED
@@ -76,7 +85,8 @@ def test_validation_rejects_bad_arguments_without_a_gpu(rf):
     # MoE: D not a multiple of 8, k out of range, E not covered
     assert L.rf_moe_gate_topk_softmax(p, p, 16, 100, 64, 2, p, p, None) == rf.RF_ERR_INVALID_ARG
     assert L.rf_moe_gate_topk_softmax(p, p, 16, 128, 64, 0, p, p, None) == rf.RF_ERR_INVALID_ARG
-    assert L.rf_moe_gate_topk_softmax(p, p, 16, 128, 32, 2, p, p, None) == rf.RF_ERR_UNSUPPORTED
+    assert L.rf_moe_gate_topk_softmax(p, p, 16, 128, 257, 2, p, p, None) == rf.RF_ERR_UNSUPPORTED
+    assert L.rf_moe_gate_topk_softmax(p, p, 16, 128, 4, 5, p, p, None) == rf.RF_ERR_INVALID_ARG
     assert L.rf_moe_gate_topk_softmax(p, p, 16, 128, 64, 9, p, p, None) == rf.RF_ERR_UNSUPPORTED
     # FP8: K not a multiple of 16, missing workspace
     assert L.rf_absmax_fp8_gemm(p, p, p, p, 16, 16, 40, p, p, null, 0, None) == rf.RF_ERR_INVALID_ARG

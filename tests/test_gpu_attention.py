@@ -20,10 +20,10 @@ def rf():
     return m
 
 
-def _run(rf, q, k, v, scale):
+def _run(rf, q, k, v, scale, causal=0):
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     o = torch.full_like(qd, float("nan"))
-    rf.rf_attn_fwd(qd, kd, vd, o, scale)
+    rf.rf_attn_fwd(qd, kd, vd, o, scale, causal)
     assert rf.rf_get_device_status() == rf.RF_OK
     return o.cpu()
 
@@ -79,3 +79,49 @@ def test_bf16_large_scores_stay_finite(rf):
     q = (q.float() * 8).to(torch.bfloat16)
     o = _run(rf, q, k, v, 1.0 / math.sqrt(64))
     assert_bf16_close(o, A.attention(q, k, v, 1.0 / math.sqrt(64)), "large scores")
+
+
+# ------------------------------------------------------------- causal mask
+# Row i reads keys j <= i + (Lk - Lq); rows that read no key are zero.
+
+
+@pytest.mark.parametrize("shape", [(1, 2, 64, 256, 64), (2, 1, 37, 37, 128), (1, 1, 50, 20, 64),
+                                   (1, 1, 1, 1, 64), (1, 1, 33, 1000, 64)])
+def test_fp32_causal(rf, shape):
+    B, H, Lq, Lk, d = shape
+    sh = I.AttnShape(B, H, H, Lq, Lk, d, "f32", seed=300 + Lq + Lk)
+    q, k, v = I.attention_inputs(sh)
+    o = _run(rf, q, k, v, sh.scale, causal=1)
+    assert_f32_close(o, A.attention(q, k, v, sh.scale, causal=True), f"fp32 causal {shape}")
+    if Lq > Lk:
+        assert (o[:, :, :Lq - Lk] == 0).all()
+
+
+def test_bert_prefill_bf16_causal(rf):
+    s = I.BERT_PREFILL
+    q, k, v = I.attention_inputs(s)
+    o = _run(rf, q, k, v, s.scale, causal=1)
+    assert_bf16_close(o, A.attention(q, k, v, s.scale, causal=True), "BERT prefill causal")
+
+
+@pytest.mark.parametrize("shape", [(2, 3, 200, 333, 64), (1, 2, 300, 300, 64), (1, 1, 500, 130, 64),
+                                   (1, 1, 129, 129, 64), (1, 1, 1, 700, 64), (3, 1, 640, 640, 64),
+                                   (1, 1, 256, 1, 64)])
+def test_bf16_causal_ragged(rf, shape):
+    B, H, Lq, Lk, d = shape
+    sh = I.AttnShape(B, H, H, Lq, Lk, d, "bf16", seed=400 + Lq + Lk)
+    q, k, v = I.attention_inputs(sh)
+    o = _run(rf, q, k, v, sh.scale, causal=1)
+    assert_bf16_close(o, A.attention(q, k, v, sh.scale, causal=True), f"bf16 causal {shape}")
+    if Lq > Lk:
+        assert (o[:, :, :Lq - Lk].float() == 0).all()
+
+
+def test_bf16_causal_last_row_equals_unmasked(rf):
+    """The last query row reads every key, so it must equal the unmasked
+    kernel's last row bit for bit (same tiles, same arithmetic order)."""
+    sh = I.AttnShape(1, 4, 4, 384, 384, 64, "bf16", seed=77)
+    q, k, v = I.attention_inputs(sh)
+    oc = _run(rf, q, k, v, sh.scale, causal=1)
+    on = _run(rf, q, k, v, sh.scale, causal=0)
+    np.testing.assert_array_equal(to64(oc[:, :, -1]), to64(on[:, :, -1]))

@@ -70,3 +70,20 @@ def test_segment_count_does_not_change_the_result_much(rf):
     outs = [_run(rf, q, k, v, sh.scale, s).float() for s in (1, 2, 64)]
     for o in outs[1:]:
         assert (o - outs[0]).abs().max().item() <= 8e-3
+
+
+def test_workspace_reuse_gives_identical_results(rf):
+    """Nothing carries over between calls through the workspace: calling
+    twice with the same workspace (and once with a fresh one) gives the
+    same bits."""
+    sh = I.AttnShape(4, 32, 8, 1, 3000, 128, "bf16", seed=5)
+    q, k, v = (t.cuda() for t in I.decode_inputs(sh))
+    nbytes = rf.rf_attn_decode_splitkv_workspace_size(4, 32, 8, 3000, 128, 0)
+    ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device="cuda")
+    outs = []
+    for w in (ws, ws, torch.zeros_like(ws)):
+        o = torch.full_like(q, float("nan"))
+        rf.rf_attn_decode_splitkv(q, k, v, o, sh.scale, w, 0)
+        outs.append(o)
+    assert rf.rf_get_device_status() == rf.RF_OK
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])

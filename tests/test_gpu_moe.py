@@ -75,3 +75,29 @@ def test_moe_gate_dense_ties(rf, k):
     w = torch.randint(-2, 3, (64, D), generator=g).to(torch.bfloat16)
     idx, wts = _run(rf, x, w, k)
     _check(x, w, k, idx, wts, f"dense ties k={k}")
+
+
+# ------------------------------------------------ other expert counts
+# The MMA width is E rounded up to 32, 64, 128 or 256; columns past E are
+# never read.  Small D keeps scores in a narrow range so ties are common.
+
+
+@pytest.mark.parametrize("T,D,E,k", [(300, 256, 8, 2), (257, 1024, 8, 8), (129, 512, 20, 4),
+                                     (1000, 2048, 32, 1), (200, 4096, 100, 8), (513, 1024, 128, 4),
+                                     (300, 2048, 256, 8), (129, 64, 256, 1), (64, 8192, 250, 2),
+                                     (100, 128, 1, 1), (4096, 4096, 256, 8)])
+def test_moe_gate_expert_counts(rf, T, D, E, k):
+    x, w = I.moe_inputs(I.MoEShape(T=T, D=D, E=E, k=k, seed=5 * T + D + E + k))
+    idx, wts = _run(rf, x, w, k)
+    _check(x, w, k, idx, wts, f"MoE {T}x{D} E={E} k={k}")
+
+
+@pytest.mark.parametrize("E,k", [(8, 8), (128, 4), (256, 8)])
+def test_moe_gate_dense_ties_expert_counts(rf, E, k):
+    T, D = 512, 8
+    g = torch.Generator().manual_seed(91 + E + k)
+    x = torch.zeros(T, D, dtype=torch.bfloat16)
+    x[torch.arange(T), torch.arange(T) % D] = 1
+    w = torch.randint(-2, 3, (E, D), generator=g).to(torch.bfloat16)
+    idx, wts = _run(rf, x, w, k)
+    _check(x, w, k, idx, wts, f"dense ties E={E} k={k}")

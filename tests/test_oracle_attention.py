@@ -200,3 +200,45 @@ def test_causal_rows_without_keys_are_zero():
     np.testing.assert_array_equal(o[Lq - Lk:], sq)
     rows = [(0, 0, i) for i in range(Lq)]
     np.testing.assert_array_equal(A.attention(q, k, v, 0.5, causal=True, rows=rows), o)
+
+
+# ------------------------------------------------------ variable lengths
+
+
+def test_varlen_equal_lengths_match_fixed_layout():
+    B, H, L, d = 3, 2, 11, 8
+    q, k, v = _rand(60, B, H, L, d), _rand(61, B, H, L, d), _rand(62, B, H, L, d)
+    pack = lambda t: t.transpose(0, 2, 1, 3).reshape(B * L, H, d)     # [B,H,L,d] -> [B*L,H,d]
+    cu = np.arange(B + 1) * L
+    for causal in (False, True):
+        got = A.attention_varlen(pack(q), pack(k), pack(v), cu, cu, 0.3, causal=causal)
+        np.testing.assert_allclose(got, pack(A.attention(q, k, v, 0.3, causal=causal)),
+                                   rtol=1e-13, atol=1e-14)
+
+
+def test_varlen_sequences_match_library_sdpa():
+    """Every sequence of a ragged batch against torch's fp64 SDPA on its own
+    tokens (with is_causal for the causal case, square sequences)."""
+    lens = [5, 1, 17, 0, 9]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    H, d = 3, 8
+    q, k, v = (_rand(63 + i, cu[-1], H, d) for i in range(3))
+    for causal in (False, True):
+        got = A.attention_varlen(q, k, v, cu, cu, 0.45, causal=causal)
+        for b, n in enumerate(lens):
+            if n == 0:
+                continue
+            sl = slice(cu[b], cu[b + 1])
+            t = lambda x: torch.from_numpy(x[sl].transpose(1, 0, 2)[None].copy())
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                t(q), t(k), t(v), is_causal=causal, scale=0.45)[0].numpy().transpose(1, 0, 2)
+            np.testing.assert_allclose(got[sl], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_varlen_sequence_without_keys_is_zero():
+    cu_q = np.array([0, 3, 7])
+    cu_k = np.array([0, 0, 5])          # sequence 0 has no keys
+    q, k, v = _rand(70, 7, 2, 4), _rand(71, 5, 2, 4), _rand(72, 5, 2, 4)
+    o = A.attention_varlen(q, k, v, cu_q, cu_k, 1.0)
+    np.testing.assert_array_equal(o[:3], 0.0)
+    assert np.abs(o[3:]).max() > 0

@@ -1,6 +1,7 @@
 """Pins for the MoE gate oracle (CPU only): exact integer scores, brute-force
 top-k enumeration, the closed form of a two-way softmax, and a worked
 example with ties."""
+import itertools
 import json
 import math
 import os
@@ -100,3 +101,38 @@ def test_softmax_after_topk_not_before():
     w = G.softmax_selected(np.take_along_axis(s, idx.astype(np.int64), axis=1))
     assert idx.tolist() == [[0, 1]]
     np.testing.assert_allclose(w[0], [1 / (1 + math.exp(-1)), math.exp(-1) / (1 + math.exp(-1))])
+
+
+@pytest.mark.parametrize("E,k", [(8, 3), (5, 5), (12, 1)])
+def test_topk_equals_brute_force_small_expert_counts(E, k):
+    """Every ordered k-tuple of distinct experts is enumerated; the oracle's
+    choice must be the tuple whose keys (score, -index) are in strictly
+    descending order and that no other such tuple beats lexicographically."""
+    x, w = _int_inputs(20 + E + k, 60, 6, E)
+    s = G.gate_scores(x.astype(float), w.astype(float))
+    idx = G.topk_select(s, k)
+    for t in range(s.shape[0]):
+        best = None
+        for tup in itertools.permutations(range(E), k):
+            keys = [(s[t, e], -e) for e in tup]
+            if any(keys[i] <= keys[i + 1] for i in range(k - 1)):
+                continue
+            if best is None or keys > best[0]:
+                best = (keys, tup)
+        assert tuple(idx[t]) == best[1]
+
+
+def test_topk_values_match_library_256_experts():
+    x, w = _int_inputs(31, 100, 64, 256)
+    s = G.gate_scores(x.astype(float), w.astype(float))
+    idx = G.topk_select(s, 8)
+    vals = np.take_along_axis(s, idx.astype(np.int64), axis=1)
+    np.testing.assert_array_equal(vals, torch.topk(torch.from_numpy(s), 8).values.numpy())
+    exact = x.astype(np.int64) @ w.astype(np.int64).T
+    np.testing.assert_array_equal(s, exact.astype(float))
+
+
+def test_single_expert_gets_weight_one():
+    x, w = _int_inputs(32, 10, 16, 1)
+    idx, wts, _ = G.moe_gate(x.astype(float), w.astype(float), 1)
+    assert (idx == 0).all() and (wts == 1.0).all()
