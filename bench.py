@@ -123,6 +123,9 @@ def make_extra_ops():
     for name, m in MOE_EXTRA.items():
         ops.append(Op(name, m.T * m.D * 2 + m.E * m.D * 2 + m.T * m.k * 8, 2 * m.T * m.D * m.E,
                       "bf16", 1))
+    for name, (sh, _mode) in SHORT_EXTRA.items():
+        ops.append(Op(name, 4 * sh.B * sh.Hq * sh.Lq * sh.d * 2,
+                      4 * sh.B * sh.Hq * sh.Lq * sh.Lk * sh.d, "bf16", 1))
     v = I.PREFILL_VARLEN
     lens = varlen_lengths()
     ops.append(Op("prefill_varlen", 4 * sum(lens) * v.H * v.d * 2,
@@ -134,6 +137,15 @@ def varlen_lengths():
     cu = I.varlen_inputs(I.PREFILL_VARLEN)[3]
     return (cu[1:] - cu[:-1]).tolist()
 
+
+# Short prefill under both evaluation orders of the cascade (mode 1 =
+# incremental, 2 = two-pass).
+SHORT_EXTRA = {
+    "short256_incremental": (I.SHORT_PREFILL_256, 1),
+    "short256_two_pass": (I.SHORT_PREFILL_256, 2),
+    "short128_incremental": (I.SHORT_PREFILL_128, 1),
+    "short128_two_pass": (I.SHORT_PREFILL_128, 2),
+}
 
 # Gate shapes outside the step: the step's token count and width with 8
 # experts / top-2 and 256 experts / top-8.
@@ -149,6 +161,7 @@ GENERATORS = {
     "bert_prefill": lambda: list(I.attention_inputs(I.BERT_PREFILL)),
     "bert_prefill_causal": lambda: list(I.attention_inputs(I.BERT_PREFILL)),
     "prefill_varlen": lambda: list(I.varlen_inputs(I.PREFILL_VARLEN)),
+    **{name: (lambda sh=sh: list(I.attention_inputs(sh))) for name, (sh, _m) in SHORT_EXTRA.items()},
     "moe_gate_e8_k2": lambda: list(I.moe_inputs(MOE_EXTRA["moe_gate_e8_k2"])),
     "moe_gate_e256_k8": lambda: list(I.moe_inputs(MOE_EXTRA["moe_gate_e256_k8"])),
     "moe_gate": lambda: list(I.moe_inputs(I.MOE_GATE)),
@@ -209,6 +222,12 @@ class Step:
             maxlen = int((cuv[1:] - cuv[:-1]).max().item())
             self.calls["prefill_varlen"] = lambda: rf.rf_attn_fwd_varlen(
                 qv, kv_, vv, self.ov, cuv, cuv, maxlen, I.PREFILL_VARLEN.scale)
+        for name, (sh, mode) in SHORT_EXTRA.items():
+            if name in d:
+                ob = torch.empty_like(d[name][0])
+                self.calls[name] = (lambda name=name, sh=sh, mode=mode, ob=ob:
+                                    rf.rf_attn_fwd_ex(*d[name], ob, sh.scale, 0, mode))
+                setattr(self, "out_" + name, [ob])
         for name, m in MOE_EXTRA.items():
             ix = torch.empty(m.T, m.k, dtype=torch.int32, device=cuda)
             wt = torch.empty(m.T, m.k, dtype=torch.float32, device=cuda)
@@ -223,6 +242,9 @@ class Step:
             self.outputs[name] = getattr(self, "out_" + name)
         if "prefill_varlen" in d:
             self.outputs["prefill_varlen"] = [self.ov]
+        for name in SHORT_EXTRA:
+            if name in d:
+                self.outputs[name] = getattr(self, "out_" + name)
 
 
 # ------------------------------------------------------------------ clocks
@@ -536,6 +558,17 @@ def oracle_sample_seconds(host, frac):
         G.moe_gate(x, w, s.k, rows=range(nt))
         out["moe_gate"] = (time.perf_counter() - t, nt / s.T)
 
+    for name, (sh, _mode) in SHORT_EXTRA.items():
+        if name not in host:
+            continue
+        q, k, v = host[name]
+        nh = max(1, int(round(frac * 4 * sh.B * sh.Hq)))
+        t = time.perf_counter()
+        for i in range(nh):
+            b, h = divmod(i % (sh.B * sh.Hq), sh.Hq)
+            A.attention(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1], sh.scale)
+        out[name] = (time.perf_counter() - t, nh / (sh.B * sh.Hq))
+
     if "prefill_varlen" in host:
         q, k, v, cu = host["prefill_varlen"]
         nseq = len(cu) - 1
@@ -633,7 +666,8 @@ def main():
     ap.add_argument("--only", default="",
                     help="comma-separated subset of ops (decode_32k, bert_prefill, moe_gate, "
                          "fp8_gemm, decode_2k) or calls outside the step (bert_prefill_causal, prefill_varlen, "
-                         "moe_gate_e8_k2, moe_gate_e256_k8); "
+                         "moe_gate_e8_k2, moe_gate_e256_k8, short256_incremental, short256_two_pass, "
+                         "short128_incremental, short128_two_pass); "
                          "default: the whole step")
     ap.add_argument("--splits", default="",
                     help="explicit decode split counts, e.g. 32768:64,2048:8 (default: automatic)")

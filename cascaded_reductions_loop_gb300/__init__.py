@@ -20,18 +20,20 @@ from . import _build
 
 __all__ = [
     "RFError", "lib", "rf_status_string", "rf_version", "rf_get_device_status",
-    "rf_attn_fwd", "rf_attn_fwd_varlen", "rf_attn_decode_splitkv",
+    "rf_attn_fwd", "rf_attn_fwd_ex", "rf_attn_fwd_varlen", "rf_attn_decode_splitkv",
     "rf_attn_decode_splitkv_num_splits",
     "rf_attn_decode_splitkv_workspace_size", "rf_attn_decode_splitkv_noalloc",
     "RF_DECODE_NOALLOC_SCRATCH_BYTES", "rf_moe_gate_topk_softmax",
     "rf_absmax_fp8_gemm", "rf_absmax_fp8_gemm_workspace_size", "rf_selftest_wait_timeout",
     "RF_OK", "RF_ERR_INVALID_ARG", "RF_ERR_UNSUPPORTED", "RF_ERR_WORKSPACE", "RF_ERR_CUDA",
     "RF_ERR_DEVICE_TIMEOUT", "RF_ERR_DEVICE_INPUT", "RF_F32", "RF_BF16",
+    "RF_ATTN_AUTO", "RF_ATTN_INCREMENTAL", "RF_ATTN_TWO_PASS",
 ]
 
 RF_OK, RF_ERR_INVALID_ARG, RF_ERR_UNSUPPORTED, RF_ERR_WORKSPACE, RF_ERR_CUDA, \
     RF_ERR_DEVICE_TIMEOUT, RF_ERR_DEVICE_INPUT = range(7)
 RF_F32, RF_BF16 = 0, 1
+RF_ATTN_AUTO, RF_ATTN_INCREMENTAL, RF_ATTN_TWO_PASS = 0, 1, 2
 RF_DECODE_NOALLOC_SCRATCH_BYTES = 16 << 20   # as in rf.h
 
 LIB_PATH = _build.LIB_PATH
@@ -54,6 +56,7 @@ _SIGS = {
     "rf_version": (_I, []),
     "rf_get_device_status": (_I, [_P]),
     "rf_attn_fwd": (_I, [_I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "rf_attn_fwd_ex": (_I, [_I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
     "rf_attn_fwd_varlen": (_I, [_I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "rf_attn_decode_splitkv_num_splits": (_I, [_I, _I, _I, _I, _I, _I]),
     "rf_attn_decode_splitkv_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I]),
@@ -121,6 +124,16 @@ def rf_get_device_status(stream=None) -> int:
 def rf_attn_fwd(q, k, v, o, scale: float, causal: int = 0, stream=None) -> None:
     """Single-segment fused attention.  q, o: [B,H,Lq,d]; k, v: [B,H,Lk,d];
     all fp32 (exact SIMT path) or all bf16 (tcgen05 path)."""
+    _attn_fwd(q, k, v, o, scale, causal, None, stream)
+
+
+def rf_attn_fwd_ex(q, k, v, o, scale: float, causal: int, mode: int, stream=None) -> None:
+    """rf_attn_fwd with an explicit evaluation order: RF_ATTN_AUTO,
+    RF_ATTN_INCREMENTAL or RF_ATTN_TWO_PASS (bf16, Lk <= 256)."""
+    _attn_fwd(q, k, v, o, scale, causal, mode, stream)
+
+
+def _attn_fwd(q, k, v, o, scale, causal, mode, stream):
     B, H, Lq, d = q.shape
     Lk = k.shape[2]
     dt = q.dtype
@@ -131,8 +144,13 @@ def rf_attn_fwd(q, k, v, o, scale: float, causal: int = 0, stream=None) -> None:
     _need(v, dt, (B, H, Lk, d), "v")
     _need(o, dt, (B, H, Lq, d), "o")
     code = RF_F32 if dt == torch.float32 else RF_BF16
-    _check(lib.rf_attn_fwd(code, _ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, Lq, Lk, d,
-                           float(scale), int(causal), _stream(stream)), "rf_attn_fwd")
+    if mode is None:
+        _check(lib.rf_attn_fwd(code, _ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, Lq, Lk, d,
+                               float(scale), int(causal), _stream(stream)), "rf_attn_fwd")
+    else:
+        _check(lib.rf_attn_fwd_ex(code, _ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, Lq, Lk, d,
+                                  float(scale), int(causal), int(mode), _stream(stream)),
+               "rf_attn_fwd_ex")
 
 
 def rf_attn_fwd_varlen(q, k, v, o, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, scale: float,

@@ -168,9 +168,21 @@ rf_status rf_get_device_status(rf_stream_t stream) {
   return (v & kDevErrInput) ? RF_ERR_DEVICE_INPUT : RF_OK;
 }
 
+// Longest key sequence for which RF_ATTN_AUTO takes the non-incremental
+// (two-pass) bf16 kernel; 0 = always incremental.
+static constexpr int kAutoTwoPassMaxLk = 0;
+
 rf_status rf_attn_fwd(int dtype, const void* Q, const void* K, const void* V, void* O, int B,
                       int H, int Lq, int Lk, int d, float scale, int causal, rf_stream_t stream) {
+  return rf_attn_fwd_ex(dtype, Q, K, V, O, B, H, Lq, Lk, d, scale, causal, RF_ATTN_AUTO, stream);
+}
+
+rf_status rf_attn_fwd_ex(int dtype, const void* Q, const void* K, const void* V, void* O, int B,
+                         int H, int Lq, int Lk, int d, float scale, int causal, int mode,
+                         rf_stream_t stream) {
   if (dtype != RF_F32 && dtype != RF_BF16) return RF_ERR_INVALID_ARG;
+  if (mode != RF_ATTN_AUTO && mode != RF_ATTN_INCREMENTAL && mode != RF_ATTN_TWO_PASS)
+    return RF_ERR_INVALID_ARG;
   if (!ptr_ok(Q) || !ptr_ok(K) || !ptr_ok(V) || !ptr_ok(O)) return RF_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || Lq < 1 || Lk < 1 || d < 1 || (causal != 0 && causal != 1))
     return RF_ERR_INVALID_ARG;
@@ -180,15 +192,19 @@ rf_status rf_attn_fwd(int dtype, const void* Q, const void* K, const void* V, vo
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (dtype == RF_F32) {
     if (d != 64 && d != 128) return RF_ERR_UNSUPPORTED;
+    if (mode == RF_ATTN_TWO_PASS) return RF_ERR_UNSUPPORTED;
     return from_cuda(launch_attn_fwd_f32(static_cast<const float*>(Q),
                                          static_cast<const float*>(K),
                                          static_cast<const float*>(V), static_cast<float*>(O), B,
                                          H, Lq, Lk, d, scale, causal, s));
   }
   if (d != 64) return RF_ERR_UNSUPPORTED;
+  if (mode == RF_ATTN_TWO_PASS && Lk > 256) return RF_ERR_UNSUPPORTED;
+  const int two_pass = mode == RF_ATTN_TWO_PASS || (mode == RF_ATTN_AUTO && Lk <= kAutoTwoPassMaxLk);
   unsigned* err = device_error_word();
   if (!err) return RF_ERR_CUDA;
-  return from_cuda(launch_attn_fwd_bf16_tc(Q, K, V, O, B, H, Lq, Lk, d, scale, causal, err, s));
+  return from_cuda(
+      launch_attn_fwd_bf16_tc(Q, K, V, O, B, H, Lq, Lk, d, scale, causal, two_pass, err, s));
 }
 
 rf_status rf_attn_fwd_varlen(int dtype, const void* Q, const void* K, const void* V, void* O,

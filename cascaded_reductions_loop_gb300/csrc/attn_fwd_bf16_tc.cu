@@ -25,6 +25,13 @@
 // the query tiles with the most key tiles are launched first.  A row that
 // reads no key is written as zero.
 //
+// Non-incremental (two-pass) mode, for Lk <= 256 ([E] §5.2 reports that short
+// reductions are better served without the incremental form): both S tiles
+// are computed into TMEM first, the exact row max over all keys is taken,
+// then every P is formed against it, so O needs no rescale and is read from
+// TMEM once.  P of the second tile is written over the K tiles, which the S
+// products have finished reading.
+//
 // Two layouts: fixed-length [B][H][L][64] (2-D tensor maps over rows of 128
 // bytes), and packed variable-length sequences [total][H][64] delimited by
 // cumulative lengths cu_seqlens[B + 1] (3-D tensor maps over (dim, head,
@@ -79,8 +86,6 @@ struct Bars {
 struct Seq {
   int Lq, Lk, h;
   int32_t q0, k0;       // first row (fixed) or first token (varlen)
-  int64_t o0;           // element offset of row 0 of O
-  int64_t o_stride;     // elements between consecutive rows of O
   bool ok;
 };
 
@@ -89,7 +94,7 @@ __device__ __forceinline__ Seq seq_of_cta(int Lq_, int Lk_, const int* cu_q, con
   Seq q;
   if (!cu_q) {
     const int64_t bh = blockIdx.y;
-    q = {Lq_, Lk_, 0, (int32_t)(bh * Lq_), (int32_t)(bh * Lk_), bh * Lq_ * kD, kD, true};
+    q = {Lq_, Lk_, 0, (int32_t)(bh * Lq_), (int32_t)(bh * Lk_), true};
     return q;
   }
   const int b = blockIdx.y / H, h = blockIdx.y % H;
@@ -105,17 +110,27 @@ __device__ __forceinline__ Seq seq_of_cta(int Lq_, int Lk_, const int* cu_q, con
   q.h = h;
   q.q0 = q0;
   q.k0 = k0;
-  q.o0 = ((int64_t)q0 * H + h) * kD;
-  q.o_stride = (int64_t)H * kD;
   return q;
 }
 
+// Output row `row` of the CTA's sequence (recomputed at the end rather than
+// kept live through the key loop).
 template <bool kVarlen>
+__device__ __forceinline__ __nv_bfloat16* out_row(__nv_bfloat16* O, const int* cu_q, int Lq_,
+                                                  int H, int row) {
+  if (kVarlen) {
+    const int b = blockIdx.y / H, h = blockIdx.y % H;
+    return O + ((int64_t)(cu_q[b] + row) * H + h) * kD;
+  }
+  return O + ((int64_t)blockIdx.y * Lq_ + row) * kD;
+}
+
+template <bool kVarlen, bool kTwoPass, bool causal>
 __global__ void __launch_bounds__(kThreads, 2)
     attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
-                         int Lq_, int Lk_, float c_log2, int causal, const int* __restrict__ cu_q,
+                         int Lq_, int Lk_, float c_log2, const int* __restrict__ cu_q,
                          const int* __restrict__ cu_k, int H, int total_q, int total_k,
                          unsigned* err) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -226,8 +241,42 @@ __global__ void __launch_bounds__(kThreads, 2)
         return true;
       };
       bool ok = mbar_wait(smem_u32(&bars->q_full), 0);
-      ok = ok && (nkv == 0 || issue_s(0));
-      for (int j = 0; ok && j < nkv; ++j) {
+      if constexpr (kTwoPass) {
+        // every S tile first (tile j in TMEM columns 128 j ..), then, once the
+        // softmax warps have turned S into P, both P.V products into one O
+        // accumulator in columns 0-63 (S is no longer read by then)
+        for (int j = 0; ok && j < nkv; ++j) {
+          if (!mbar_wait(smem_u32(&bars->kv_full[j]), 0)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t k_addr = smem_u32(smem + kKOff + j * kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            mma_bf16_ss(tmem_s + j * BKV, sw128_desc(q_addr + kk * 32, 1024, 16),
+                        sw128_desc(k_addr + kk * 32, 1024, 16), kIdescS, kk != 0);
+        }
+        if (ok && nkv > 0) {
+          mma_commit(smem_u32(&bars->s_full));
+          ok = mbar_wait(smem_u32(&bars->p_full), 0);
+          if (ok) {
+            tc_fence_after();
+            for (int j = 0; j < nkv; ++j) {
+              const uint32_t pj = j == 0 ? p_addr : smem_u32(smem + kKOff);
+              const uint32_t v_addr = smem_u32(smem + kVOff + j * kTileBytes);
+#pragma unroll
+              for (int kk = 0; kk < BKV / 16; ++kk)
+                mma_bf16_ss(tmem_s, sw128_desc(pj + (kk >> 2) * kTileBytes + (kk & 3) * 32, 1024, 16),
+                            sw128_desc(v_addr + kk * 16 * 128, 1024, kTileBytes), kIdescO,
+                            (j | kk) != 0);
+            }
+            mma_commit(smem_u32(&bars->o_full));
+          }
+        }
+      }
+      if (!kTwoPass) ok = ok && (nkv == 0 || issue_s(0));
+      for (int j = 0; !kTwoPass && ok && j < nkv; ++j) {
         const int slot = j % kKV;
         if (!mbar_wait(smem_u32(&bars->p_full), (uint32_t)(j & 1))) {
           ok = false;
@@ -266,7 +315,98 @@ __global__ void __launch_bounds__(kThreads, 2)
     bool ok = true;
     const uint64_t c2 = f2(c_log2, c_log2);
 
-    for (int j = 0; j < nkv; ++j) {
+    if constexpr (kTwoPass) {
+      // Non-incremental form for at most two key tiles: the exact row max over
+      // every key first, then P = 2^(S c - m) for all keys (P of tile 0 in the
+      // P buffer, of tile 1 over the consumed K tiles), one O with no rescale.
+      if (nkv > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full), 0) && !*abort_flag);
+        if (ok) {
+          tc_fence_after();
+          int valid[2];
+          bool full[2];
+          float mx = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            if (j >= nkv) break;
+            valid[j] = min(BKV, Lk - j * BKV);
+            full[j] = valid[j] == BKV;
+            if (causal) {
+              full[j] = full[j] && qt * BQ + off + 1 - j * BKV >= BKV;
+              valid[j] = max(0, min(valid[j], qt * BQ + r + off + 1 - j * BKV));
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t v[32];
+              tmem_ld32(tmem_s + lane_off + j * BKV + q * 32, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (full[j] || q * 32 + i < valid[j]) mx = fmaxf(mx, __uint_as_float(v[i]));
+            }
+          }
+          const float m = mx * c_log2;
+          const float m_use = m == -INFINITY ? 0.f : m;      // a row without keys
+          const uint64_t negm2 = f2(-m_use, -m_use);
+          uint64_t sum2 = 0ull;
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            if (j >= nkv) break;
+            uint8_t* pr = smem + (j == 0 ? kPOff : kKOff) + r * 128;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t v[32];
+              tmem_ld32(tmem_s + lane_off + j * BKV + q * 32, v);
+              tmem_ld_wait();
+              uint32_t pk[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                float t0, t1;
+                f2_split(ffma2(f2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), c2,
+                               negm2),
+                         t0, t1);
+                float p0 = ex2(t0), p1 = ex2(t1);
+                if (!full[j]) {
+                  const int c0 = q * 32 + 2 * i;
+                  p0 = c0 < valid[j] ? p0 : 0.f;
+                  p1 = c0 + 1 < valid[j] ? p1 : 0.f;
+                }
+                sum2 = fadd2(sum2, f2(p0, p1));
+                pk[i] = pack_bf16x2(p0, p1);
+              }
+              uint8_t* blk = pr + (q >> 1) * kTileBytes;
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                const int chunk = (q & 1) * 4 + c;
+                *reinterpret_cast<uint4*>(blk + ((chunk ^ (r & 7)) << 4)) =
+                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+              }
+            }
+          }
+          float s_lo, s_hi;
+          f2_split(sum2, s_lo, s_hi);
+          l_run = s_lo + s_hi;
+          fence_proxy_async_smem();                      // P visible to the tensor core
+          tc_fence_before();                             // S reads ordered before the arrive
+          mbar_arrive(smem_u32(&bars->p_full));
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->o_full), 0) && !*abort_flag);
+          if (ok) {
+            tc_fence_after();
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint32_t v[32];
+              tmem_ld32(tmem_s + lane_off + h * 32, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                o2[h * 16 + i] = f2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+            }
+          }
+        }
+      }
+    }
+
+    for (int j = 0; !kTwoPass && j < nkv; ++j) {
       // warp-uniform decision: the TMEM loads below are warp-collective
       if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full), (uint32_t)(j & 1)) &&
                                        !*abort_flag)) {
@@ -366,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       *abort_flag = 1;
     } else if (qt * BQ + r < Lq) {
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;   // no key read: O = 0
-      uint4* dst = reinterpret_cast<uint4*>(O + sq.o0 + (int64_t)(qt * BQ + r) * sq.o_stride);
+      uint4* dst = reinterpret_cast<uint4*>(out_row<kVarlen>(O, cu_q, Lq_, H, qt * BQ + r));
 #pragma unroll
       for (int c = 0; c < kD / 8; ++c) {
         float o[8];
@@ -390,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 cudaError_t launch_attn_fwd_bf16_tc(const void* Q, const void* K, const void* V, void* O, int B,
                                     int H, int Lq, int Lk, int d, float scale, int causal,
-                                    unsigned* err, cudaStream_t s) {
+                                    int two_pass, unsigned* err, cudaStream_t s) {
   (void)d;
   CUtensorMap tmQ, tmK, tmV;
   const uint64_t q_rows = (uint64_t)B * H * Lq, kv_rows = (uint64_t)B * H * Lk;
@@ -398,15 +538,18 @@ cudaError_t launch_attn_fwd_bf16_tc(const void* Q, const void* K, const void* V,
       !encode_tmap_2d(&tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, kD, kv_rows, kD * 2, kD, BKV, true) ||
       !encode_tmap_2d(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, kD, kv_rows, kD * 2, kD, BKV, true))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_bf16_kernel<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (two_pass && Lk > kKV * BKV) return cudaErrorInvalidValue;
+  auto kern = two_pass ? (causal ? attn_fwd_bf16_kernel<false, true, true>
+                                 : attn_fwd_bf16_kernel<false, true, false>)
+                       : (causal ? attn_fwd_bf16_kernel<false, false, true>
+                                 : attn_fwd_bf16_kernel<false, false, false>);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   dim3 grid((Lq + BQ - 1) / BQ, B * H);
   if (grid.y > 65535u) return cudaErrorInvalidValue;
   const float c_log2 = scale * 1.4426950408889634f;
-  attn_fwd_bf16_kernel<false><<<grid, kThreads, kSmem, s>>>(
-      tmQ, tmK, tmV, static_cast<__nv_bfloat16*>(O), Lq, Lk, c_log2, causal, nullptr, nullptr, H,
-      0, 0, err);
+  kern<<<grid, kThreads, kSmem, s>>>(tmQ, tmK, tmV, static_cast<__nv_bfloat16*>(O), Lq, Lk, c_log2,
+                                     nullptr, nullptr, H, 0, 0, err);
   return cudaGetLastError();
 }
 
@@ -423,15 +566,15 @@ cudaError_t launch_attn_fwd_bf16_tc_varlen(const void* Q, const void* K, const v
       !encode_tmap_3d(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, kD, H, total_k, kD * 2, pitch,
                       kD, 1, BKV, true))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_bf16_kernel<true>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  auto kern = causal ? attn_fwd_bf16_kernel<true, false, true>
+                     : attn_fwd_bf16_kernel<true, false, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   dim3 grid((max_q + BQ - 1) / BQ, B * H);
   if (grid.y > 65535u) return cudaErrorInvalidValue;
   const float c_log2 = scale * 1.4426950408889634f;
-  attn_fwd_bf16_kernel<true><<<grid, kThreads, kSmem, s>>>(
-      tmQ, tmK, tmV, static_cast<__nv_bfloat16*>(O), max_q, 0, c_log2, causal, cu_q, cu_k, H,
-      total_q, total_k, err);
+  kern<<<grid, kThreads, kSmem, s>>>(tmQ, tmK, tmV, static_cast<__nv_bfloat16*>(O), max_q, 0,
+                                     c_log2, cu_q, cu_k, H, total_q, total_k, err);
   return cudaGetLastError();
 }
 

@@ -39,9 +39,10 @@ cudaError_t launch_attn_fwd_f32(const float* Q, const float* K, const float* V, 
                                 int H, int Lq, int Lk, int d, float scale, int causal,
                                 cudaStream_t s);
 
+// two_pass = 1: non-incremental form (requires Lk <= 256).
 cudaError_t launch_attn_fwd_bf16_tc(const void* Q, const void* K, const void* V, void* O, int B,
                                     int H, int Lq, int Lk, int d, float scale, int causal,
-                                    unsigned* err, cudaStream_t s);
+                                    int two_pass, unsigned* err, cudaStream_t s);
 
 // Packed variable-length layout: Q/O [total_q][H][d], K/V [total_k][H][d],
 // sequence b = tokens cu_q[b] .. cu_q[b+1]-1 (device arrays of B + 1 int32).

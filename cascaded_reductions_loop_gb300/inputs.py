@@ -136,6 +136,11 @@ class VarlenShape:
         return 1.0 / math.sqrt(self.d)
 
 
+# Short sequences (the same number of query rows per head as the BERT-style
+# workload) for comparing the incremental and two-pass evaluation orders.
+SHORT_PREFILL_256 = AttnShape(B=16, Hq=16, Hkv=16, Lq=256, Lk=256, d=64, dtype="bf16", seed=7)
+SHORT_PREFILL_128 = AttnShape(B=32, Hq=16, Hkv=16, Lq=128, Lk=128, d=64, dtype="bf16", seed=8)
+
 # A packed batch of BERT-style sequences of mixed length (no padding).
 PREFILL_VARLEN = VarlenShape(B=16, H=16, d=64, len_lo=64, len_hi=1024, dtype="bf16", seed=6)
 

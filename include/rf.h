@@ -101,6 +101,26 @@ rf_status rf_attn_fwd(int dtype, const void* Q, const void* K, const void* V, vo
                       int B, int H, int Lq, int Lk, int d, float scale, int causal,
                       rf_stream_t stream);
 
+/* Evaluation order of the softmax cascade for rf_attn_fwd_ex. */
+typedef enum {
+  RF_ATTN_AUTO = 0,          /* the library's choice (what rf_attn_fwd uses)      */
+  RF_ATTN_INCREMENTAL = 1,   /* one loop over key tiles, running (m, l, o)
+                                rescaled per tile ([E] §2.3; [S] Methodologie 2) */
+  RF_ATTN_TWO_PASS = 2       /* non-incremental: exact row max over all keys,
+                                then P and O with no rescale; Lk <= 256, bf16
+                                only ([E] §5.2: short reductions)                */
+} rf_attn_mode;
+
+/*
+ * rf_attn_fwd with an explicit evaluation order `mode` (an rf_attn_mode).
+ * Both orders compute the same cascade; they differ in rounding only.
+ * Errors as rf_attn_fwd, plus RF_ERR_INVALID_ARG for an unknown mode and
+ * RF_ERR_UNSUPPORTED for RF_ATTN_TWO_PASS with RF_F32 or with Lk > 256.
+ */
+rf_status rf_attn_fwd_ex(int dtype, const void* Q, const void* K, const void* V, void* O,
+                         int B, int H, int Lq, int Lk, int d, float scale, int causal, int mode,
+                         rf_stream_t stream);
+
 /*
  * rf_attn_fwd over a batch of sequences of different lengths, packed
  * token-major without padding (the same computation per sequence and head,

@@ -63,6 +63,11 @@ def test_validation_rejects_bad_arguments_without_a_gpu(rf):
     assert L.rf_attn_fwd(1, p, p, p, p, 1, 1, 64, 64, 64, -1.0, 0, None) == rf.RF_ERR_INVALID_ARG
     assert L.rf_attn_fwd(1, p, p, p, p, 1, 1, 64, 64, 96, 0.125, 0, None) == rf.RF_ERR_UNSUPPORTED
     assert L.rf_attn_fwd(0, p, p, p, p, 1, 1, 64, 64, 48, 0.125, 0, None) == rf.RF_ERR_UNSUPPORTED
+    # explicit evaluation order: unknown mode, two-pass beyond 256 keys or in fp32
+    X = L.rf_attn_fwd_ex
+    assert X(1, p, p, p, p, 1, 1, 64, 64, 64, 0.125, 0, 3, None) == rf.RF_ERR_INVALID_ARG
+    assert X(1, p, p, p, p, 1, 1, 64, 257, 64, 0.125, 0, 2, None) == rf.RF_ERR_UNSUPPORTED
+    assert X(0, p, p, p, p, 1, 1, 64, 64, 64, 0.125, 0, 2, None) == rf.RF_ERR_UNSUPPORTED
     # varlen attention: missing cumulative lengths, bad totals, causal, head dim
     V = L.rf_attn_fwd_varlen
     assert V(1, p, p, p, p, null, p, 2, 4, 64, 100, 100, 64, 0.125, 0, None) == rf.RF_ERR_INVALID_ARG

@@ -125,3 +125,42 @@ def test_bf16_causal_last_row_equals_unmasked(rf):
     oc = _run(rf, q, k, v, sh.scale, causal=1)
     on = _run(rf, q, k, v, sh.scale, causal=0)
     np.testing.assert_array_equal(to64(oc[:, :, -1]), to64(on[:, :, -1]))
+
+
+# ----------------------------------------- non-incremental (two-pass) mode
+# Lk <= 256: exact row max over all keys first, then P and O, no rescale.
+
+
+@pytest.mark.parametrize("shape,causal", [((2, 3, 200, 256, 64), 0), ((1, 2, 256, 256, 64), 1),
+                                          ((1, 1, 129, 129, 64), 0), ((2, 1, 300, 100, 64), 1),
+                                          ((1, 1, 1, 1, 64), 0), ((1, 2, 500, 130, 64), 1),
+                                          ((4, 2, 128, 128, 64), 0), ((1, 1, 77, 200, 64), 1)])
+def test_bf16_two_pass(rf, shape, causal):
+    B, H, Lq, Lk, d = shape
+    sh = I.AttnShape(B, H, H, Lq, Lk, d, "bf16", seed=500 + Lq + Lk + causal)
+    q, k, v = I.attention_inputs(sh)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o = torch.full_like(qd, float("nan"))
+    rf.rf_attn_fwd_ex(qd, kd, vd, o, sh.scale, causal, rf.RF_ATTN_TWO_PASS)
+    assert rf.rf_get_device_status() == rf.RF_OK
+    assert_bf16_close(o.cpu(), A.attention(q, k, v, sh.scale, causal=bool(causal)),
+                      f"two-pass {shape} causal={causal}")
+
+
+def test_two_pass_short_workloads_and_mode_errors(rf):
+    for sh in (I.SHORT_PREFILL_256, I.SHORT_PREFILL_128):
+        q, k, v = I.attention_inputs(sh)
+        for mode in (rf.RF_ATTN_INCREMENTAL, rf.RF_ATTN_TWO_PASS):
+            o = torch.full_like(q, float("nan"), device="cuda")
+            rf.rf_attn_fwd_ex(q.cuda(), k.cuda(), v.cuda(), o, sh.scale, 0, mode)
+            assert rf.rf_get_device_status() == rf.RF_OK
+            rows = [(b, h, i) for b in (0, sh.B - 1) for h in (0, sh.Hq - 1) for i in range(sh.Lq)]
+            got = torch.stack([o[b, h, i].cpu() for b, h, i in rows])
+            assert_bf16_close(got, A.attention(q, k, v, sh.scale, rows=rows), f"mode {mode}")
+    x = torch.zeros(1, 1, 64, 64, device="cuda", dtype=torch.bfloat16)
+    kk = torch.zeros(1, 1, 300, 64, device="cuda", dtype=torch.bfloat16)
+    with pytest.raises(rf.RFError):                     # two-pass needs Lk <= 256
+        rf.rf_attn_fwd_ex(x, kk, kk, x.clone(), 0.125, 0, rf.RF_ATTN_TWO_PASS)
+    xf = torch.zeros(1, 1, 64, 64, device="cuda")
+    with pytest.raises(rf.RFError):                     # and the bf16 path
+        rf.rf_attn_fwd_ex(xf, xf, xf, xf.clone(), 0.125, 0, rf.RF_ATTN_TWO_PASS)
