@@ -40,14 +40,21 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
 // is within one ulp of x / s, the residual x - s q0 is exact under an FMA,
 // and one more FMA step q0 + r (x - s q0) rounds to RN(x / s) (Markstein's
 // correction, "Computation of elementary functions on the IBM RISC
-// System/6000 processor", IBM J. Res. Dev. 34(1), 1990).  The sign of a zero
-// quotient is taken from x.  Rows with a tiny scale use IEEE division instead
-// (see row_scale).  tests/test_gpu_fp8.py checks the codes against an IEEE
-// fp32 division over every (bf16 x, bf16 row max) pair.
-__device__ __forceinline__ float div_by_scale(float x, float s, float r) {
-  const float q0 = __fmul_rn(x, r);
-  const float e = __fmaf_rn(-q0, s, x);
-  return copysignf(__fmaf_rn(e, r, q0), x);
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990).  Done on pairs of
+// elements with the packed f32x2 FMA/MUL (each lane rounds as the scalar
+// instruction would).  The correction can turn a negative zero quotient into
+// +0, so the sign bit of every code is then OR-ed in from x's own sign bit
+// (a nonzero negative quotient already carries it; x >= 0 adds nothing).
+// Rows with a tiny scale use IEEE division instead (see row_scale).
+// tests/test_gpu_fp8.py checks the codes against an IEEE fp32 division over
+// every (bf16 x, bf16 row max) pair.
+__device__ __forceinline__ uint32_t quant2_recip(uint32_t w, uint64_t neg_s2, uint64_t r2) {
+  const uint64_t x2 = f2(bf16lo(w), bf16hi(w));
+  const uint64_t q0 = fmul2(x2, r2);
+  const uint64_t e = ffma2(q0, neg_s2, x2);          // x - s q0, exact
+  float lo, hi;
+  f2_split(ffma2(e, r2, q0), lo, hi);
+  return cvt_e4m3x2(lo, hi);
 }
 
 // 8 bf16 (one 16-byte vector) -> 8 E4M3 codes (little-endian in a uint2).
@@ -55,13 +62,22 @@ template <bool kRecip>
 __device__ __forceinline__ uint2 quant8(const uint4 v, float s, float r) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   uint32_t c[4];
+  if constexpr (kRecip) {
+    const uint64_t neg_s2 = f2(-s, -s), r2 = f2(r, r);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float lo = bf16lo(w[i]), hi = bf16hi(w[i]);
-    c[i] = kRecip ? cvt_e4m3x2(div_by_scale(lo, s, r), div_by_scale(hi, s, r))
-                  : cvt_e4m3x2(__fdiv_rn(lo, s), __fdiv_rn(hi, s));
+    for (int i = 0; i < 4; ++i) c[i] = quant2_recip(w[i], neg_s2, r2);
+    // byte k of a code word is element k; its sign is bit 7 of byte 1 or 3
+    // of the bf16 word holding it
+    const uint32_t sg0 = __byte_perm(w[0], w[1], 0x7531) & 0x80808080u;
+    const uint32_t sg1 = __byte_perm(w[2], w[3], 0x7531) & 0x80808080u;
+    return make_uint2(__byte_perm(c[0], c[1], 0x5410) | sg0, __byte_perm(c[2], c[3], 0x5410) | sg1);
+  } else {
+    (void)r;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      c[i] = cvt_e4m3x2(__fdiv_rn(bf16lo(w[i]), s), __fdiv_rn(bf16hi(w[i]), s));
+    return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
   }
-  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
 }
 
 __device__ __forceinline__ uint32_t absmax_bits(const uint4 v) {
@@ -100,6 +116,9 @@ __device__ __forceinline__ RowScale row_scale(uint32_t amax_bits) {
 __global__ void __launch_bounds__(kQuantWarps * 32)
     absmax_quant_regs_kernel(const uint4* __restrict__ X, uint8_t* __restrict__ Xq,
                              float* __restrict__ sx, int M, int K) {
+  // the GEMM (a programmatic dependent) may be scheduled onto SMs this grid
+  // leaves; it waits for this grid to finish before reading Xq or sx
+  asm volatile("griddepcontrol.launch_dependents;");
   const int lane = threadIdx.x & 31;
   const int nw = gridDim.x * kQuantWarps;
   const int nvec = K >> 3;
@@ -145,6 +164,7 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
 __global__ void __launch_bounds__(kQuantWarps * 32)
     absmax_quant_long_kernel(const uint4* __restrict__ X, uint8_t* __restrict__ Xq,
                              float* __restrict__ sx, int M, int K) {
+  asm volatile("griddepcontrol.launch_dependents;");
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * kQuantWarps + (threadIdx.x >> 5);
   if (row >= M) return;
@@ -237,6 +257,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   cluster_sync();            // both CTAs' barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem = bars->tmem;
+  // launched as a programmatic dependent of the quantisation kernel: the
+  // prologue above overlapped its tail; Xq and sx are read only after this
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp == 0) {
     if (lane == 0) {
@@ -428,13 +451,15 @@ cudaError_t launch_absmax_fp8_gemm(const void* X, const uint8_t* Wq, const float
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = kGemmSmem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, fp8_gemm_kernel, tmA, tmB, static_cast<const float*>(sx), sw,
                             static_cast<__nv_bfloat16*>(Y), M, N, K, tiles_n, (int)pairs, err);
 }
