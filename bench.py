@@ -609,13 +609,23 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+def calibrated_fraction(host, budget_s, frac=1.0 / 512, cap=0.25):
+    """Fraction of every op's rows whose oracle run takes about budget_s:
+    grown from a small sample until a run lands within a factor of two."""
+    for _ in range(4):
+        t0 = time.perf_counter()
+        oracle_sample_seconds(host, frac)
+        took = time.perf_counter() - t0
+        if took >= budget_s / 2 or frac >= cap:
+            break
+        frac = min(cap, frac * min(16.0, budget_s / max(took, 1e-3)))
+    return frac
+
+
 def cpu_baseline(ops, peaks, host, budget_s=15.0):
-    # calibrate the sample size on a tiny fraction, then size it to the budget
-    frac = 1.0 / 512
-    t0 = time.perf_counter()
-    oracle_sample_seconds(host, frac)
-    cal = time.perf_counter() - t0
-    frac = min(0.25, frac * max(1.0, budget_s / max(cal, 1e-3)))
+    # size the sample so that the timed oracle run takes about budget_s
+    frac = calibrated_fraction(host, budget_s / 2)
+    frac = min(0.25, frac * 2)
     res = oracle_sample_seconds(host, frac)
     full_s = sum(sec / f for sec, f in res.values())
     roof_s = sum(op.roofline_s(peaks) for op in ops)
@@ -634,8 +644,11 @@ def run_reference(args, world, rank):
     peaks = load_peaks()
     ops = select_ops(args)
     host = host_inputs([op.name for op in ops])
-    frac = 1.0 / 1024
-    for _ in range(max(1, min(args.warmup, 1))):
+    # each of the warm-up and timed steps is a sample sized so that the whole
+    # run takes about args.ref_budget seconds of CPU work
+    per_step = args.ref_budget / max(1, args.steps + args.warmup)
+    frac = calibrated_fraction(host, per_step, frac=1.0 / 4096)
+    for _ in range(args.warmup):
         oracle_sample_seconds(host, frac)
     t_full = []
     for _ in range(args.steps):
@@ -676,6 +689,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of CPU oracle work for the cpu_baseline sample")
+    ap.add_argument("--ref-budget", type=float, default=120.0,
+                    help="seconds of CPU oracle work for a whole --impl reference run")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: raising --warmup to 3 (minimum)", file=sys.stderr)
