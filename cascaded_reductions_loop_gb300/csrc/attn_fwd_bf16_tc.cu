@@ -16,8 +16,16 @@
 //                                            MN-major B operand)
 //   4. softmax warps: o = alpha*o + O_j in registers.
 // After the last tile each thread writes o / l as bf16.  S and P never
-// leave the SM.  A TMA warp streams Q once and K/V tiles through a 2-stage
-// ring; every wait is bounded.
+// leave the SM.  A TMA warp streams Q once and K and V tiles through two
+// 2-stage rings (a K slot is refilled as soon as its S product is done, a V
+// slot after its P.V product); every wait is bounded.
+//
+// Pipelining: S is double-buffered in TMEM (tile j in columns 128 (j % 2) ..),
+// and O_j is written into the first 64 columns of S_j's buffer once the
+// softmax warps have read S_j.  The softmax warps fold O_{j-1} into o right
+// after the max pass of tile j, so the tensor core computes P_{j-1} V_{j-1}
+// during that pass, and S_{j+1} = Q K_{j+1}^T as soon as O_{j-1} has been
+// read, while the exp pass of tile j runs.
 //
 // Causal mask: row i reads keys j <= i + (Lk - Lq).  A CTA walks only the
 // key tiles its rows can read; tiles below the diagonal take the unmasked
@@ -69,11 +77,12 @@ __device__ __forceinline__ float ex2(float x) {
 
 struct Bars {
   uint64_t q_full;
-  uint64_t kv_full[kKV];
-  uint64_t kv_empty[kKV];
-  uint64_t s_full;
-  uint64_t p_full;
-  uint64_t o_full;
+  uint64_t k_full[kKV], v_full[kKV];
+  uint64_t k_empty[kKV], v_empty[kKV];
+  uint64_t s_full[2];     // S_j in TMEM buffer j % 2
+  uint64_t o_full[2];     // O_j in TMEM buffer j % 2 (columns 0-63)
+  uint64_t o_free[2];     // O_j read by the softmax warps: the buffer may take S_{j+2}
+  uint64_t p_full;        // P_j in shared memory
   uint64_t drain;
   uint32_t tmem;
   int abort;
@@ -163,12 +172,17 @@ __global__ void __launch_bounds__(kThreads, 2)
     prefetch_tmap(&tmV);
     mbar_init(smem_u32(&bars->q_full), 1);
     for (int i = 0; i < kKV; ++i) {
-      mbar_init(smem_u32(&bars->kv_full[i]), 1);
-      mbar_init(smem_u32(&bars->kv_empty[i]), 1);
+      mbar_init(smem_u32(&bars->k_full[i]), 1);
+      mbar_init(smem_u32(&bars->v_full[i]), 1);
+      mbar_init(smem_u32(&bars->k_empty[i]), 1);
+      mbar_init(smem_u32(&bars->v_empty[i]), 1);
     }
-    mbar_init(smem_u32(&bars->s_full), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bars->s_full[i]), 1);
+      mbar_init(smem_u32(&bars->o_full[i]), 1);
+      mbar_init(smem_u32(&bars->o_free[i]), BQ);
+    }
     mbar_init(smem_u32(&bars->p_full), BQ);
-    mbar_init(smem_u32(&bars->o_full), 1);
     mbar_init(smem_u32(&bars->drain), 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -181,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem;
-  const uint32_t tmem_s = tmem, tmem_o = tmem + BKV;
+  const uint32_t tmem_s = tmem;                     // buffer b at columns 128 b
 
   if (warp == 0) {
     if (lane == 0) {
@@ -192,35 +206,42 @@ __global__ void __launch_bounds__(kThreads, 2)
         tma_load_3d(smem_u32(smem + kQOff), &tmQ, smem_u32(&bars->q_full), 0, sq.h, q_row0);
       else
         tma_load_2d(smem_u32(smem + kQOff), &tmQ, smem_u32(&bars->q_full), 0, q_row0);
-      int j = 0;
-      for (; j < nkv; ++j) {
+      // one K or V tile of key tile j into ring slot j % kKV
+      auto load = [&](const CUtensorMap* tm, int off, uint64_t* full, int j) {
         const int slot = j % kKV;
-        if (j >= kKV &&
-            !mbar_wait(smem_u32(&bars->kv_empty[slot]), (uint32_t)(((j / kKV) + 1) & 1))) {
-          raise_error(err, kDevErrTimeout);
+        const uint32_t bar = smem_u32(&full[slot]);
+        mbar_arrive_expect_tx(bar, kTileBytes);
+        if (kVarlen)
+          tma_load_3d_hint(smem_u32(smem + off + slot * kTileBytes), tm, bar, 0, sq.h,
+                           kv_row0 + j * BKV, pol_kv);
+        else
+          tma_load_2d_hint(smem_u32(smem + off + slot * kTileBytes), tm, bar, 0,
+                           kv_row0 + j * BKV, pol_kv);
+      };
+      int nk = 0, nv = 0;                              // K / V tiles issued
+      for (int j = 0; j < nkv && !*abort_flag; ++j) {
+        const uint32_t ph = (uint32_t)(((j / kKV) + 1) & 1);
+        if (j >= kKV && !mbar_wait(smem_u32(&bars->k_empty[j % kKV]), ph)) {
           *abort_flag = 1;
           break;
         }
-        if (*abort_flag) break;
-        const uint32_t bar = smem_u32(&bars->kv_full[slot]);
-        mbar_arrive_expect_tx(bar, 2 * kTileBytes);
-        if (kVarlen) {
-          tma_load_3d_hint(smem_u32(smem + kKOff + slot * kTileBytes), &tmK, bar, 0, sq.h,
-                           kv_row0 + j * BKV, pol_kv);
-          tma_load_3d_hint(smem_u32(smem + kVOff + slot * kTileBytes), &tmV, bar, 0, sq.h,
-                           kv_row0 + j * BKV, pol_kv);
-        } else {
-          tma_load_2d_hint(smem_u32(smem + kKOff + slot * kTileBytes), &tmK, bar, 0,
-                           kv_row0 + j * BKV, pol_kv);
-          tma_load_2d_hint(smem_u32(smem + kVOff + slot * kTileBytes), &tmV, bar, 0,
-                           kv_row0 + j * BKV, pol_kv);
+        load(&tmK, kKOff, bars->k_full, j);
+        ++nk;
+        if (j >= kKV && !mbar_wait(smem_u32(&bars->v_empty[j % kKV]), ph)) {
+          *abort_flag = 1;
+          break;
         }
+        load(&tmV, kVOff, bars->v_full, j);
+        ++nv;
       }
       if (*abort_flag) {
+        raise_error(err, kDevErrTimeout);
+        // let the copies still in flight land before shared memory is released
         (void)mbar_wait(smem_u32(&bars->q_full), 0, 1000000ull);
-        for (int i = j - kKV < 0 ? 0 : j - kKV; i < j; ++i)
-          (void)mbar_wait(smem_u32(&bars->kv_full[i % kKV]), (uint32_t)((i / kKV) & 1),
-                          1000000ull);
+        for (int i = nk - kKV < 0 ? 0 : nk - kKV; i < nk; ++i)
+          (void)mbar_wait(smem_u32(&bars->k_full[i % kKV]), (uint32_t)((i / kKV) & 1), 1000000ull);
+        for (int i = nv - kKV < 0 ? 0 : nv - kKV; i < nv; ++i)
+          (void)mbar_wait(smem_u32(&bars->v_full[i % kKV]), (uint32_t)((i / kKV) & 1), 1000000ull);
       }
     }
   } else if (warp == 1) {
@@ -228,16 +249,18 @@ __global__ void __launch_bounds__(kThreads, 2)
       // ------------------------------------------------ MMA issuer
       const uint32_t q_addr = smem_u32(smem + kQOff);
       const uint32_t p_addr = smem_u32(smem + kPOff);
+      // S_j = Q K_j^T into TMEM buffer j % 2; frees K slot j % kKV when done
       auto issue_s = [&](int j) -> bool {
         const int slot = j % kKV;
-        if (!mbar_wait(smem_u32(&bars->kv_full[slot]), (uint32_t)((j / kKV) & 1))) return false;
+        if (!mbar_wait(smem_u32(&bars->k_full[slot]), (uint32_t)((j / kKV) & 1))) return false;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(smem + kKOff + slot * kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
-          mma_bf16_ss(tmem_s, sw128_desc(q_addr + kk * 32, 1024, 16),
+          mma_bf16_ss(tmem_s + (j & 1) * BKV, sw128_desc(q_addr + kk * 32, 1024, 16),
                       sw128_desc(k_addr + kk * 32, 1024, 16), kIdescS, kk != 0);
-        mma_commit(smem_u32(&bars->s_full));
+        mma_commit(smem_u32(&bars->s_full[j & 1]));
+        mma_commit(smem_u32(&bars->k_empty[slot]));
         return true;
       };
       bool ok = mbar_wait(smem_u32(&bars->q_full), 0);
@@ -245,53 +268,55 @@ __global__ void __launch_bounds__(kThreads, 2)
         // every S tile first (tile j in TMEM columns 128 j ..), then, once the
         // softmax warps have turned S into P, both P.V products into one O
         // accumulator in columns 0-63 (S is no longer read by then)
+        for (int j = 0; ok && j < nkv; ++j) ok = issue_s(j);
+        if (ok && nkv > 0) {
+          ok = mbar_wait(smem_u32(&bars->p_full), 0);
+          for (int j = 0; ok && j < nkv; ++j) {
+            if (!mbar_wait(smem_u32(&bars->v_full[j]), 0)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t pj = j == 0 ? p_addr : smem_u32(smem + kKOff);
+            const uint32_t v_addr = smem_u32(smem + kVOff + j * kTileBytes);
+#pragma unroll
+            for (int kk = 0; kk < BKV / 16; ++kk)
+              mma_bf16_ss(tmem_s, sw128_desc(pj + (kk >> 2) * kTileBytes + (kk & 3) * 32, 1024, 16),
+                          sw128_desc(v_addr + kk * 16 * 128, 1024, kTileBytes), kIdescO,
+                          (j | kk) != 0);
+          }
+          if (ok) mma_commit(smem_u32(&bars->o_full[0]));
+        }
+      } else {
+        if (nkv > 0) ok = ok && issue_s(0);
+        if (nkv > 1) ok = ok && issue_s(1);
         for (int j = 0; ok && j < nkv; ++j) {
-          if (!mbar_wait(smem_u32(&bars->kv_full[j]), 0)) {
+          const int slot = j % kKV;
+          if (!mbar_wait(smem_u32(&bars->p_full), (uint32_t)(j & 1)) ||
+              !mbar_wait(smem_u32(&bars->v_full[slot]), (uint32_t)((j / kKV) & 1))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t k_addr = smem_u32(smem + kKOff + j * kTileBytes);
+          // O_j = P_j V_j into the first 64 columns of S_j's buffer (S_j has been read)
+          const uint32_t v_addr = smem_u32(smem + kVOff + slot * kTileBytes);
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk)
-            mma_bf16_ss(tmem_s + j * BKV, sw128_desc(q_addr + kk * 32, 1024, 16),
-                        sw128_desc(k_addr + kk * 32, 1024, 16), kIdescS, kk != 0);
-        }
-        if (ok && nkv > 0) {
-          mma_commit(smem_u32(&bars->s_full));
-          ok = mbar_wait(smem_u32(&bars->p_full), 0);
-          if (ok) {
-            tc_fence_after();
-            for (int j = 0; j < nkv; ++j) {
-              const uint32_t pj = j == 0 ? p_addr : smem_u32(smem + kKOff);
-              const uint32_t v_addr = smem_u32(smem + kVOff + j * kTileBytes);
-#pragma unroll
-              for (int kk = 0; kk < BKV / 16; ++kk)
-                mma_bf16_ss(tmem_s, sw128_desc(pj + (kk >> 2) * kTileBytes + (kk & 3) * 32, 1024, 16),
-                            sw128_desc(v_addr + kk * 16 * 128, 1024, kTileBytes), kIdescO,
-                            (j | kk) != 0);
+          for (int kk = 0; kk < BKV / 16; ++kk)
+            mma_bf16_ss(tmem_s + (j & 1) * BKV,
+                        sw128_desc(p_addr + (kk >> 2) * kTileBytes + (kk & 3) * 32, 1024, 16),
+                        sw128_desc(v_addr + kk * 16 * 128, 1024, kTileBytes), kIdescO, kk != 0);
+          mma_commit(smem_u32(&bars->o_full[j & 1]));
+          mma_commit(smem_u32(&bars->v_empty[slot]));
+          if (j + 2 < nkv) {
+            // the buffer takes S_{j+2} once the softmax warps have read O_j
+            if (!mbar_wait(smem_u32(&bars->o_free[j & 1]), (uint32_t)((j >> 1) & 1))) {
+              ok = false;
+              break;
             }
-            mma_commit(smem_u32(&bars->o_full));
+            tc_fence_after();
+            ok = issue_s(j + 2);
           }
         }
-      }
-      if (!kTwoPass) ok = ok && (nkv == 0 || issue_s(0));
-      for (int j = 0; !kTwoPass && ok && j < nkv; ++j) {
-        const int slot = j % kKV;
-        if (!mbar_wait(smem_u32(&bars->p_full), (uint32_t)(j & 1))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t v_addr = smem_u32(smem + kVOff + slot * kTileBytes);
-#pragma unroll
-        for (int kk = 0; kk < BKV / 16; ++kk)
-          mma_bf16_ss(tmem_o,
-                      sw128_desc(p_addr + (kk >> 2) * kTileBytes + (kk & 3) * 32, 1024, 16),
-                      sw128_desc(v_addr + kk * 16 * 128, 1024, kTileBytes), kIdescO, kk != 0);
-        mma_commit(smem_u32(&bars->o_full));
-        mma_commit(smem_u32(&bars->kv_empty[slot]));
-        if (j + 1 < nkv && !issue_s(j + 1)) ok = false;
       }
       if (!ok) {
         raise_error(err, kDevErrTimeout);
@@ -320,7 +345,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       // every key first, then P = 2^(S c - m) for all keys (P of tile 0 in the
       // P buffer, of tile 1 over the consumed K tiles), one O with no rescale.
       if (nkv > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full), 0) && !*abort_flag);
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[0]), 0) &&
+                                         (nkv < 2 || mbar_wait(smem_u32(&bars->s_full[1]), 0)) &&
+                                         !*abort_flag);
         if (ok) {
           tc_fence_after();
           int valid[2];
@@ -389,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           fence_proxy_async_smem();                      // P visible to the tensor core
           tc_fence_before();                             // S reads ordered before the arrive
           mbar_arrive(smem_u32(&bars->p_full));
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->o_full), 0) && !*abort_flag);
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->o_full[0]), 0) && !*abort_flag);
           if (ok) {
             tc_fence_after();
 #pragma unroll
@@ -406,14 +433,36 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
 
+    // o = alpha * o + O_t for the tile t whose P.V product is in buffer t % 2
+    auto fold_o = [&](int t, float alpha) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->o_full[t & 1]), (uint32_t)((t >> 1) & 1)) &&
+                                       !*abort_flag))
+        return false;
+      tc_fence_after();
+      const uint64_t a2 = f2(alpha, alpha);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t v[32];
+        tmem_ld32(tmem_s + (t & 1) * BKV + lane_off + h * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          o2[h * 16 + i] =
+              ffma2(o2[h * 16 + i], a2, f2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])));
+      }
+      return true;
+    };
+    float alpha_prev = 0.f;
     for (int j = 0; !kTwoPass && j < nkv; ++j) {
       // warp-uniform decision: the TMEM loads below are warp-collective
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full), (uint32_t)(j & 1)) &&
-                                       !*abort_flag)) {
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(smem_u32(&bars->s_full[j & 1]), (uint32_t)((j >> 1) & 1)) &&
+                          !*abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      const uint32_t sbuf = tmem_s + (j & 1) * BKV + lane_off;
       int valid = min(BKV, Lk - j * BKV);              // keys of this tile that exist
       bool full = valid == BKV;                        // uniform over the CTA
       if (causal) {
@@ -426,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint32_t v[32];
-        tmem_ld32(tmem_s + lane_off + q * 32, v);
+        tmem_ld32(sbuf + q * 32, v);
         tmem_ld_wait();
         if (full) {
 #pragma unroll
@@ -444,12 +493,22 @@ __global__ void __launch_bounds__(kThreads, 2)
       const float m_use = m_new == -INFINITY ? 0.f : m_new;
       const float alpha = ex2(m_run - m_use);          // 0 on the first tile
       const uint64_t negm2 = f2(-m_use, -m_use);
+      // O_{j-1} (its P.V ran during the max pass); then its buffer may take
+      // S_{j+1}, and P_{j-1} has been read, so P_j may overwrite it
+      if (j > 0) {
+        if (!fold_o(j - 1, alpha_prev)) {
+          ok = false;
+          break;
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars->o_free[(j - 1) & 1]));
+      }
       // pass 2: P = 2^(S c - m'), row sum, P -> swizzled bf16 tile
       uint64_t sum2 = 0ull;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint32_t v[32];
-        tmem_ld32(tmem_s + lane_off + q * 32, v);
+        tmem_ld32(sbuf + q * 32, v);
         tmem_ld_wait();
         uint32_t pk[16];
 #pragma unroll
@@ -479,28 +538,12 @@ __global__ void __launch_bounds__(kThreads, 2)
       f2_split(sum2, s_lo, s_hi);
       l_run = l_run * alpha + (s_lo + s_hi);
       m_run = m_new;
+      alpha_prev = alpha;
       fence_proxy_async_smem();                        // P visible to the tensor core
       tc_fence_before();                               // S reads ordered before the arrive
       mbar_arrive(smem_u32(&bars->p_full));
-
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->o_full), (uint32_t)(j & 1)) &&
-                                       !*abort_flag)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint64_t a2 = f2(alpha, alpha);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t v[32];
-        tmem_ld32(tmem_o + lane_off + h * 32, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          o2[h * 16 + i] =
-              ffma2(o2[h * 16 + i], a2, f2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])));
-      }
     }
+    if (!kTwoPass && ok && nkv > 0 && !fold_o(nkv - 1, alpha_prev)) ok = false;
     if (!ok) {
       raise_error(err, kDevErrTimeout);
       *abort_flag = 1;
