@@ -392,8 +392,10 @@ def run_ours(args, world, rank, local):
 
     total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
     ms_per_step = total_ms / args.steps
-    per_op_ms = {op.name: statistics.median(evs[s][i].elapsed_time(evs[s][i + 1])
-                                            for s in range(args.steps))
+    # per call: mean of the middle 90 % of the K event intervals (a single
+    # interval is quantised to about a microsecond; the mean over many is not)
+    per_op_ms = {op.name: trimmed_mean([evs[s][i].elapsed_time(evs[s][i + 1])
+                                        for s in range(args.steps)])
                  for i, op in enumerate(ops)}
     roof_s = sum(op.roofline_s(peaks) for op in ops)
     value = 100.0 * world * roof_s / (ms_per_step * 1e-3)
@@ -447,6 +449,13 @@ def run_ours(args, world, rank, local):
     if not args.no_cpu_baseline and rank == 0 and world == 1:
         result["cpu_baseline"] = cpu_baseline(ops, peaks, host, budget_s=args.cpu_budget)
     return result
+
+
+def trimmed_mean(xs, cut=0.05):
+    xs = sorted(xs)
+    k = int(len(xs) * cut)
+    core = xs[k:len(xs) - k] or xs
+    return sum(core) / len(core)
 
 
 def select_ops(args):

@@ -470,8 +470,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         full = full && qt * BQ + off + 1 - j * BKV >= BKV;
         valid = max(0, min(valid, qt * BQ + r + off + 1 - j * BKV));   // per row
       }
-      // pass 1: row max of the raw scores
-      float mx = -INFINITY;
+      // pass 1: row max of the raw scores (four independent max chains)
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint32_t v[32];
@@ -480,13 +480,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (full) {
 #pragma unroll
           for (int i = 0; i < 32; i += 2)
-            mx = fmax3(mx, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+            mx4[(i >> 1) & 3] = fmax3(mx4[(i >> 1) & 3], __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            if (q * 32 + i < valid) mx = fmaxf(mx, __uint_as_float(v[i]));
+            if (q * 32 + i < valid) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(v[i]));
         }
       }
+      const float mx = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]);
       const float m_new = fmaxf(m_run, mx * c_log2);
       // -inf only while the row has read no key (a causal row above the
       // first visible key): then every P is masked to 0 and alpha is 0
@@ -503,8 +504,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         tc_fence_before();
         mbar_arrive(smem_u32(&bars->o_free[(j - 1) & 1]));
       }
-      // pass 2: P = 2^(S c - m'), row sum, P -> swizzled bf16 tile
-      uint64_t sum2 = 0ull;
+      // pass 2: P = 2^(S c - m'), row sum (four independent chains), P ->
+      // swizzled bf16 tile
+      uint64_t sum4[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint32_t v[32];
@@ -522,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             p0 = c0 < valid ? p0 : 0.f;
             p1 = c0 + 1 < valid ? p1 : 0.f;
           }
-          sum2 = fadd2(sum2, f2(p0, p1));
+          sum4[i & 3] = fadd2(sum4[i & 3], f2(p0, p1));
           pk[i] = pack_bf16x2(p0, p1);
         }
         // keys 32q..32q+31 = block q/2, 16-byte chunks (q%2)*4 .. +3
@@ -535,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
       float s_lo, s_hi;
-      f2_split(sum2, s_lo, s_hi);
+      f2_split(fadd2(fadd2(sum4[0], sum4[1]), fadd2(sum4[2], sum4[3])), s_lo, s_hi);
       l_run = l_run * alpha + (s_lo + s_hi);
       m_run = m_new;
       alpha_prev = alpha;
