@@ -111,9 +111,9 @@ __device__ __forceinline__ RowScale row_scale(uint32_t amax_bits) {
 }
 
 // Rows of up to 4096 elements: one warp per row, the row held in registers
-// (16 x 16-byte loads per lane); the next row of the warp is loaded while the
-// current one is quantised.
-__global__ void __launch_bounds__(kQuantWarps * 32)
+// (16 x 16-byte loads per lane).  Memory parallelism comes from occupancy:
+// four 4-warp CTAs per SM, each warp with its whole row in flight.
+__global__ void __launch_bounds__(kQuantWarps * 32, 4)
     absmax_quant_regs_kernel(const uint4* __restrict__ X, uint8_t* __restrict__ Xq,
                              float* __restrict__ sx, int M, int K) {
   // the GEMM (a programmatic dependent) may be scheduled onto SMs this grid
@@ -132,15 +132,13 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
       v[i] = j < nvec ? __ldcs(xr + j) : make_uint4(0, 0, 0, 0);
     }
   };
-  if (row < M) load(cur, row);
   for (; row < M; row += nw) {
+    load(cur, row);
     uint32_t amax = 0;
 #pragma unroll
     for (int i = 0; i < kVecPerLaneMax; ++i) amax = max(amax, absmax_bits(cur[i]));
     const RowScale rs = row_scale(amax);
     if (lane == 0) sx[row] = rs.s;
-    uint4 nxt[kVecPerLaneMax];
-    if (row + nw < M) load(nxt, row + nw);           // prefetch the warp's next row
     uint2* qr = reinterpret_cast<uint2*>(Xq + (size_t)row * K);
     if (rs.s == 0.f) {                                // all-zero row: codes 0x00
 #pragma unroll
@@ -155,8 +153,6 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
       for (int i = 0; i < kVecPerLaneMax; ++i)
         if (lane + 32 * i < nvec) __stcs(qr + lane + 32 * i, quant8<false>(cur[i], rs.s, rs.r));
     }
-#pragma unroll
-    for (int i = 0; i < kVecPerLaneMax; ++i) cur[i] = nxt[i];
   }
 }
 
@@ -423,7 +419,7 @@ cudaError_t launch_absmax_fp8_gemm(const void* X, const uint8_t* Wq, const float
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidValue;
   if (K <= 32 * kVecPerLaneMax * 8) {
-    const int resident = 3 * sms;                      // three 4-warp CTAs per SM
+    const int resident = 4 * sms;                      // four 4-warp CTAs per SM
     absmax_quant_regs_kernel<<<qblocks < resident ? qblocks : resident, kQuantWarps * 32, 0, s>>>(
         static_cast<const uint4*>(X), xq, sx, M, K);
   } else {
