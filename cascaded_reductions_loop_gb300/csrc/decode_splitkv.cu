@@ -2,12 +2,14 @@
 //
 // Multi-segment strategy ([S] Methodologie 3; [E] §3.3 inter-block merge and
 // multi-kernel cooperation): the keys of every (batch, kv head) are cut into
-// S segments.  Kernel 1 (decode_partial_kernel) gives each segment to one
-// CTA, whose four warps each run the incremental safe-softmax loop ([E] §2.3,
-// §4.1) over every fourth chunk of the segment and write their partial state
+// S segments.  Kernel 1 (decode_partial_kernel, a persistent grid of one CTA
+// per SM) takes the segments as work items; the four warps of the CTA that
+// takes an item each run the incremental safe-softmax loop ([E] §2.3, §4.1)
+// over every fourth chunk of the segment and write their partial state
 // (m, l, o) -- o unnormalised, m in log2 units -- for each of the G query heads
-// that share the kv head.  Kernel 2 (decode_merge_kernel) combines the 4 S
-// partial states of every (batch, query head): M = max m_j,
+// that share the kv head.  Kernel 2 (decode_merge_kernel, launched as a
+// programmatic dependent of kernel 1) combines the 4 S partial states of
+// every (batch, query head): M = max m_j,
 // L = sum l_j 2^(m_j - M), O = sum o_j 2^(m_j - M) / L.  (Merging inside
 // kernel 1, by the last warp to finish a group, was measured slower: each
 // warp must make its states visible with a fence before taking a ticket, and

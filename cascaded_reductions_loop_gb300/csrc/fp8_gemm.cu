@@ -6,17 +6,20 @@
 // cannot be folded into the GEMM loop incrementally the way the softmax max
 // can.  It therefore runs as two cooperating kernels ([E] §3.3 multi-kernel
 // level):
-//   1. absmax_quant_kernel: one warp per row of X reads the row once into
-//      registers, reduces |x| to the row max, sets sx = max / 448 (IEEE fp32
-//      division) and writes the E4M3 codes of x / sx (IEEE division, then
-//      cvt.rn.satfinite) plus sx.  X is read from HBM once.
+//   1. absmax_quant_regs_kernel (rows up to 4096 elements; longer rows use
+//      absmax_quant_long_kernel, which reads each row twice): one warp per
+//      row of X reads the row once into registers, reduces |x| to the row
+//      max, sets sx = max / 448 (IEEE fp32 division) and writes the E4M3
+//      codes of the correctly rounded x / sx (cvt.rn.satfinite) plus sx.
+//      X is read from HBM once.
 //   2. fp8_gemm_kernel: a tcgen05 GEMM (kind::f8f6f4, E4M3 x E4M3 -> fp32 in
 //      tensor memory) over TMA-staged 128-byte-swizzled tiles, warp
 //      specialised (TMA producer warp, single-thread MMA issuer, four
 //      epilogue warps), whose epilogue applies sx[m] * sw[n] and rounds to
-//      bf16.  The codes travel through HBM as 1 byte per element, half the
-//      size of the bf16 input, so the pair moves as many bytes as a fused
-//      kernel that re-reads X would.
+//      bf16.  It is launched as a programmatic dependent of kernel 1.  The
+//      codes travel through memory as 1 byte per element, half the size of
+//      the bf16 input, so the pair moves as many bytes as a fused kernel
+//      that re-reads X would.
 #include <math.h>
 
 #include "rf_device.cuh"

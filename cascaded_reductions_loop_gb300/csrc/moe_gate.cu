@@ -1,11 +1,12 @@
 // moe_gate.cu -- fused MoE gate: scores = x . W_gate^T -> top-k -> softmax of
 // the selected scores ([E] §4.2), one kernel, no score matrix in HBM.
 //
-// Each CTA owns 128 tokens and one slice of the reduction dimension D; the
-// CTAs covering the slices of the same 128 tokens form a thread-block
-// cluster (split-K).  Per CTA: a TMA producer warp streams 128x64 tiles of x
-// and Ex64 tiles of W_gate (both K-major, 128-byte swizzled) through a ring
-// of stages (for E <= 64 two adjacent tiles of each per stage, so that every
+// Each CTA owns a tile of bm <= 128 tokens (bm chosen on the host so that the
+// tiles fill the SMs evenly) and one slice of the reduction dimension D; the
+// CTAs covering the slices of the same tile form a thread-block cluster
+// (split-K).  Per CTA: a TMA producer warp streams bm x 64 tiles of x and
+// E x 64 tiles of W_gate (both K-major, 128-byte swizzled) through a ring of
+// stages (for E <= 64 two adjacent tiles of each per stage, so that every
 // row's 256 bytes are fetched together); one thread issues tcgen05.mma
 // kind::f16 (bf16 x bf16 -> fp32, M = 128, N = NE, the expert count rounded
 // up to 32, 64, 128 or 256) into tensor memory.  The epilogue warps copy the
@@ -26,7 +27,7 @@
 namespace rf {
 namespace {
 
-constexpr int BM = 128;            // tokens per CTA
+constexpr int BM = 128;            // the MMA's M: the largest tile of tokens
 constexpr int BK = 64;             // bf16 elements per TMA box (one 128-byte swizzle row)
 constexpr int kThreads = 192;      // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kRing = 200 * 1024;    // stages (runtime count) and, afterwards, the score tile
