@@ -531,7 +531,7 @@ def oracle_sample_seconds(host, frac):
             continue
         q, k, v = host[name]
         scale_rows = 1 if name == "decode_32k" else 4
-        nrows = max(1, int(round(frac * scale_rows * s.B * s.Hq)))
+        nrows = min(s.B * s.Hq, max(1, int(round(frac * scale_rows * s.B * s.Hq))))
         rows = [(int(b), int(h)) for b, h in
                 zip(rng.integers(0, s.B, nrows), rng.integers(0, s.Hq, nrows))]
         t = time.perf_counter()
@@ -541,7 +541,7 @@ def oracle_sample_seconds(host, frac):
     if "bert_prefill" in host:
         s = I.BERT_PREFILL
         q, k, v = host["bert_prefill"]
-        nh = max(1, int(round(frac * 4 * s.B * s.Hq)))
+        nh = min(s.B * s.Hq, max(1, int(round(frac * 4 * s.B * s.Hq))))
         t = time.perf_counter()
         for i in range(nh):
             b, h = divmod(i % (s.B * s.Hq), s.Hq)
@@ -551,7 +551,7 @@ def oracle_sample_seconds(host, frac):
     if "bert_prefill_causal" in host:
         s = I.BERT_PREFILL
         q, k, v = host["bert_prefill_causal"]
-        nh = max(1, int(round(frac * 4 * s.B * s.Hq)))
+        nh = min(s.B * s.Hq, max(1, int(round(frac * 4 * s.B * s.Hq))))
         t = time.perf_counter()
         for i in range(nh):
             b, h = divmod(i % (s.B * s.Hq), s.Hq)
@@ -562,7 +562,7 @@ def oracle_sample_seconds(host, frac):
     if "moe_gate" in host:
         s = I.MOE_GATE
         x, w = host["moe_gate"]
-        nt = max(1, int(round(frac * 4 * s.T)))
+        nt = min(s.T, max(1, int(round(frac * 4 * s.T))))
         t = time.perf_counter()
         G.moe_gate(x, w, s.k, rows=range(nt))
         out["moe_gate"] = (time.perf_counter() - t, nt / s.T)
@@ -571,7 +571,7 @@ def oracle_sample_seconds(host, frac):
         if name not in host:
             continue
         q, k, v = host[name]
-        nh = max(1, int(round(frac * 4 * sh.B * sh.Hq)))
+        nh = min(sh.B * sh.Hq, max(1, int(round(frac * 4 * sh.B * sh.Hq))))
         t = time.perf_counter()
         for i in range(nh):
             b, h = divmod(i % (sh.B * sh.Hq), sh.Hq)
@@ -596,7 +596,7 @@ def oracle_sample_seconds(host, frac):
         if name not in host:
             continue
         x, w = host[name]
-        nt = max(1, int(round(frac * 4 * m.T)))
+        nt = min(m.T, max(1, int(round(frac * 4 * m.T))))
         t = time.perf_counter()
         G.moe_gate(x, w, m.k, rows=range(nt))
         out[name] = (time.perf_counter() - t, nt / m.T)
@@ -604,7 +604,7 @@ def oracle_sample_seconds(host, frac):
     if "fp8_gemm" in host:
         s = I.FP8_GEMM
         x, wq, sw = host["fp8_gemm"]
-        nr = max(1, int(round(frac * s.M)))
+        nr = min(s.M, max(1, int(round(frac * s.M))))
         t = time.perf_counter()
         F.absmax_fp8_gemm(x, wq, sw, rows=range(nr))
         out["fp8_gemm"] = (time.perf_counter() - t, nr / s.M)
@@ -618,30 +618,33 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
-def calibrated_fraction(host, budget_s, frac=1.0 / 512, cap=0.25):
-    """Fraction of every op's rows whose oracle run takes about budget_s:
-    grown from a small sample until a run lands within a factor of two."""
-    for _ in range(4):
+def calibrated_fraction(host, budget_s, lo=1.0 / 1024, hi=1.0 / 64, cap=1.0):
+    """Fraction of every op's rows whose oracle run takes about budget_s.
+    The sample time is a fixed part (conversions of whole operands) plus a
+    part proportional to the fraction, so both are fitted from two samples."""
+    def run(frac):
         t0 = time.perf_counter()
         oracle_sample_seconds(host, frac)
-        took = time.perf_counter() - t0
-        if took >= budget_s / 2 or frac >= cap:
-            break
-        frac = min(cap, frac * min(16.0, budget_s / max(took, 1e-3)))
-    return frac
+        return time.perf_counter() - t0
+    t_lo, t_hi = run(lo), run(hi)
+    slope = max((t_hi - t_lo) / (hi - lo), 1e-6)
+    fixed = max(t_lo - slope * lo, 0.0)
+    frac = (budget_s - fixed) / slope
+    return min(cap, max(lo, frac))
 
 
 def cpu_baseline(ops, peaks, host, budget_s=15.0):
     # size the sample so that the timed oracle run takes about budget_s
-    frac = calibrated_fraction(host, budget_s / 2)
-    frac = min(0.25, frac * 2)
+    frac = calibrated_fraction(host, budget_s)
     res = oracle_sample_seconds(host, frac)
     full_s = sum(sec / f for sec, f in res.values())
     roof_s = sum(op.roofline_s(peaks) for op in ops)
     return {"value": 100.0 * roof_s / full_s, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
             "seconds_per_full_step": round(full_s, 2),
-            "sample": (f"{frac:.4f} of each op's rows/heads/tokens (fp64 numpy oracle, BLAS "
-                       f"threads up to the core count); full step extrapolated linearly"),
+            "sample": ("fraction of each op's rows/heads/tokens run by the fp64 numpy oracle "
+                       "(BLAS threads up to the core count): "
+                       + ", ".join(f"{k} {f:.3f}" for k, (_, f) in res.items())
+                       + "; full step extrapolated linearly"),
             "sample_seconds": round(sum(sec for sec, _ in res.values()), 2)}
 
 
@@ -656,7 +659,7 @@ def run_reference(args, world, rank):
     # each of the warm-up and timed steps is a sample sized so that the whole
     # run takes about args.ref_budget seconds of CPU work
     per_step = args.ref_budget / max(1, args.steps + args.warmup)
-    frac = calibrated_fraction(host, per_step, frac=1.0 / 4096)
+    frac = calibrated_fraction(host, per_step, lo=1.0 / 8192, hi=1.0 / 1024)
     for _ in range(args.warmup):
         oracle_sample_seconds(host, frac)
     t_full = []
