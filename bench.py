@@ -516,9 +516,12 @@ def run_e2e(rf, ops, peaks, host, step, world, args):
 # ------------------------------------------------------------------ CPU oracle
 
 
-def oracle_sample_seconds(host, frac):
+def oracle_sample_seconds(host, frac, only=None):
     """Times the fp64 oracle on a bounded sample of every op present in
-    ``host``; returns {op: (seconds, fraction of the op's full work covered)}."""
+    ``host`` (or of the ops in ``only``); returns {op: (seconds, fraction of
+    the op's full work covered)}."""
+    if only is not None:
+        host = {k: v for k, v in host.items() if k in only}
     from oracle import attention as A
     from oracle import fp8_quant_gemm as F
     from oracle import moe_gate as G
@@ -633,42 +636,76 @@ def calibrated_fraction(host, budget_s, lo=1.0 / 1024, hi=1.0 / 64, cap=1.0):
     return min(cap, max(lo, frac))
 
 
+def oracle_cost_fits(host, lo, hi):
+    """Per op: (fixed seconds, seconds per unit of the op's own fraction,
+    the op's fraction per unit of the sampling fraction), from two samples.
+    The fixed part (whole-operand conversions and decodes the oracle does on
+    every call) must not be scaled up with the sample."""
+    r_lo, r_hi = oracle_sample_seconds(host, lo), oracle_sample_seconds(host, hi)
+    fits = {}
+    for k in r_lo:
+        (t1, f1), (t2, f2) = r_lo[k], r_hi[k]
+        slope = (t2 - t1) / (f2 - f1) if f2 > f1 else t2 / max(f2, 1e-9)
+        slope = max(slope, 1e-9)
+        fits[k] = (max(0.0, t1 - slope * f1), slope, f1 / lo)
+    return fits
+
+
+def full_op_seconds(sample_s, f, fixed):
+    """Oracle time for a whole op from a sample covering fraction f."""
+    return fixed + max(sample_s - fixed, 0.0) / f
+
+
 def cpu_baseline(ops, peaks, host, budget_s=15.0):
-    # size the sample so that the timed oracle run takes about budget_s
+    # size the sample so that the timed oracle run takes about budget_s; the
+    # per-op fixed parts come from two small samples
+    fits = oracle_cost_fits(host, 1.0 / 1024, 1.0 / 64)
     frac = calibrated_fraction(host, budget_s)
     res = oracle_sample_seconds(host, frac)
-    full_s = sum(sec / f for sec, f in res.values())
+    full_s = sum(full_op_seconds(sec, f, fits[k][0]) for k, (sec, f) in res.items())
     roof_s = sum(op.roofline_s(peaks) for op in ops)
     return {"value": 100.0 * roof_s / full_s, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
             "seconds_per_full_step": round(full_s, 2),
             "sample": ("fraction of each op's rows/heads/tokens run by the fp64 numpy oracle "
                        "(BLAS threads up to the core count): "
                        + ", ".join(f"{k} {f:.3f}" for k, (_, f) in res.items())
-                       + "; full step extrapolated linearly"),
+                       + "; full step = per op, the fixed per-call part plus the rest scaled "
+                         "to the whole op"),
             "sample_seconds": round(sum(sec for sec, _ in res.values()), 2)}
 
 
 def run_reference(args, world, rank):
     """The reference arm: the CPU fp64 oracle as it stands, on the same
-    workload and metric, each step a bounded sample."""
+    workload and metric.  Each warm-up and timed step samples one op (in
+    turn), sized so that the whole run takes about args.ref_budget seconds;
+    a step's time is the sum over ops of each op's latest whole-op estimate."""
     if rank != 0:
         return None
     peaks = load_peaks()
     ops = select_ops(args)
     host = host_inputs([op.name for op in ops])
-    # each of the warm-up and timed steps is a sample sized so that the whole
-    # run takes about args.ref_budget seconds of CPU work
+    fits = oracle_cost_fits(host, 1.0 / 8192, 1.0 / 1024)
+    names = list(fits)
+    est = {k: fixed + slope for k, (fixed, slope, _) in fits.items()}
     per_step = args.ref_budget / max(1, args.steps + args.warmup)
-    frac = calibrated_fraction(host, per_step, lo=1.0 / 8192, hi=1.0 / 1024)
-    for _ in range(args.warmup):
-        oracle_sample_seconds(host, frac)
-    t_full = []
-    for _ in range(args.steps):
-        res = oracle_sample_seconds(host, frac)
-        t_full.append(sum(sec / f for sec, f in res.values()))
-    full_s = statistics.median(t_full)
+    t_full, fracs = [], {}
+    for s in range(args.warmup + args.steps):
+        k = names[s % len(names)]
+        fixed, slope, mult = fits[k]
+        f_op = min(1.0, max(1.0 / 8192, (per_step - fixed) / slope))
+        frac = f_op / max(mult, 1e-9)
+        sec, f = oracle_sample_seconds(host, frac, only={k})[k]
+        est[k] = full_op_seconds(sec, f, fixed)
+        fracs[k] = f
+        if s >= args.warmup:
+            t_full.append(sum(est.values()))
+    full_s = statistics.median(t_full) if t_full else sum(est.values())
     roof_s = sum(op.roofline_s(peaks) for op in ops)
     value = 100.0 * roof_s / full_s
+    sample = ("one op per step, in turn, by the fp64 numpy oracle; fraction of the op's "
+              "rows/heads/tokens: " + ", ".join(f"{k} {f:.4f}" for k, f in fracs.items())
+              + "; full step = sum of each op's latest estimate (fixed per-call part plus the "
+                "rest scaled to the whole op)")
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(full_s * 1e3, 1),
@@ -677,8 +714,7 @@ def run_reference(args, world, rank):
         "config": {"workload": workload_name(ops),
                    "parallelism": "CPU oracle, rank 0 only"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-                         "sample": f"{frac:.5f} of each op's rows/heads/tokens per step, "
-                                   "full step extrapolated linearly"},
+                         "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
