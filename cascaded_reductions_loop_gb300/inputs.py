@@ -13,6 +13,7 @@ are built for):
 * variable-length prefill: per-sequence lengths drawn uniformly from a range
   with a seeded generator; Q, K, V ~ N(0, 1) packed token-major
   [total, H, d] (no padding), with the cumulative lengths as int32.
+* latent-KV decode: the query and the latent cache ~ N(0, 1), cast to bf16.
 * MoE gate: x and W_gate hold integers drawn uniformly from {-2, ..., 2}, cast
   to bf16 (exact).  W_gate is stored expert-major, [E][D] (the layout of a
   linear layer's weight), so that both GEMM operands are contiguous along D.
@@ -160,6 +161,35 @@ def varlen_inputs(shape: VarlenShape):
     k = _cast(_normal(g, (total, shape.H, shape.d)), shape.dtype)
     v = _cast(_normal(g, (total, shape.H, shape.d)), shape.dtype)
     return q, k, v, cu
+
+
+@dataclass(frozen=True)
+class MLAShape:
+    """Latent-KV (multi-latent attention) decode: B sequences of Lk cached
+    latent rows of d_qk dims (d_v latent dims, which also serve as the
+    values, then d_qk - d_v positional dims), Hq query heads, one query token.
+    Defaults: the published DeepSeek-V3 attention (128 heads, latent rank
+    512, positional width 64) with the softmax scale of its un-absorbed
+    192-wide query-key heads."""
+    B: int
+    Hq: int
+    Lk: int
+    seed: int
+    d_qk: int = 576
+    d_v: int = 512
+    scale: float = 1.0 / math.sqrt(192.0)
+
+
+MLA_DECODE = MLAShape(B=64, Hq=128, Lk=4096, seed=9)
+
+
+def mla_inputs(shape: MLAShape):
+    """q [B, Hq, d_qk] and the latent cache ckv [B, Lk, d_qk], both ~ N(0, 1)
+    in bf16."""
+    g = _gen(shape.seed)
+    q = _cast(_normal(g, (shape.B, shape.Hq, shape.d_qk)), "bf16")
+    ckv = _cast(_normal(g, (shape.B, shape.Lk, shape.d_qk)), "bf16")
+    return q, ckv
 
 
 def moe_inputs(shape: MoEShape):

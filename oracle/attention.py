@@ -149,6 +149,32 @@ def decode_attention(q, k, v, scale: float, rows=None) -> np.ndarray:
     return out.reshape(B, Hq, d) if rows is None else out
 
 
+def mla_decode(q, ckv, scale: float, dv: int, rows=None) -> np.ndarray:
+    """Latent-KV (multi-latent) attention decode, absorbed form.
+
+    The technical summary reports the fused kernels on multi-latent
+    attention against a hand-written latent-attention decode library ([S]
+    "Resultaten") but does not define the operation; its public definition
+    is taken: every query head of batch b attends to the one
+    latent cache of b, ckv[b] [Lk, Dqk].  Scores use all Dqk dims (latent
+    part and positional part); the values are the first dv dims of the same
+    rows.  The cascade is the three-pass one of ``attention``.
+
+    q: [B, Hq, Dqk]; ckv: [B, Lk, Dqk].  Returns fp64 [B, Hq, dv], or
+    [len(rows), dv] for a list of (b, hq) pairs.
+    """
+    B, Hq, _ = q.shape
+    pairs = [(b, h) for b in range(B) for h in range(Hq)] if rows is None else list(rows)
+    res = np.empty((len(pairs), dv), dtype=np.float64)
+    cache_b, C = -1, None
+    for i, (b, h) in enumerate(pairs):
+        if b != cache_b:
+            C = _f64(ckv[b])
+            cache_b = b
+        res[i] = three_pass_row(_f64(q[b, h]), C, C[:, :dv], scale)
+    return res.reshape(B, Hq, dv) if rows is None else res
+
+
 # ------------------------------------------------- the method's own forms
 
 
