@@ -130,7 +130,29 @@ def make_extra_ops():
     lens = varlen_lengths()
     ops.append(Op("prefill_varlen", 4 * sum(lens) * v.H * v.d * 2,
                   4 * v.H * v.d * sum(n * n for n in lens), "bf16", 1))
+    ops.append(mla_op())
     return ops
+
+
+def mla_op():
+    """Latent-KV decode: the cache is read once (B * Lk rows of d_qk bf16),
+    plus Q and O; FLOPs count the scores over d_qk dims and P.V over d_v."""
+    s = I.MLA_DECODE
+    cache = s.B * s.Lk * s.d_qk * 2
+    qo = s.B * s.Hq * (s.d_qk + s.d_v) * 2
+    return Op("mla_decode", cache + qo, 2 * s.B * s.Hq * s.Lk * (s.d_qk + s.d_v), "bf16",
+              1 + (mla_splits() > 1))
+
+
+def mla_splits():
+    """Segments per batch the library takes for the latent-KV workload (1
+    where the library cannot tell without a device)."""
+    try:
+        import cascaded_reductions_loop_gb300 as rf
+        s = I.MLA_DECODE
+        return max(1, rf.rf_mla_decode_num_splits(s.B, s.Hq, s.Lk, s.d_qk, s.d_v, 0))
+    except (ImportError, OSError):
+        return 1
 
 
 def varlen_lengths():
@@ -165,6 +187,7 @@ GENERATORS = {
     "moe_gate_e8_k2": lambda: list(I.moe_inputs(MOE_EXTRA["moe_gate_e8_k2"])),
     "moe_gate_e256_k8": lambda: list(I.moe_inputs(MOE_EXTRA["moe_gate_e256_k8"])),
     "moe_gate": lambda: list(I.moe_inputs(I.MOE_GATE)),
+    "mla_decode": lambda: list(I.mla_inputs(I.MLA_DECODE)),
     "fp8_gemm": lambda: list(I.fp8_inputs(I.FP8_GEMM)),
 }
 
@@ -228,6 +251,13 @@ class Step:
                 self.calls[name] = (lambda name=name, sh=sh, mode=mode, ob=ob:
                                     rf.rf_attn_fwd_ex(*d[name], ob, sh.scale, 0, mode))
                 setattr(self, "out_" + name, [ob])
+        if "mla_decode" in d:
+            sl = I.MLA_DECODE
+            self.oml = torch.empty(sl.B, sl.Hq, sl.d_v, dtype=torch.bfloat16, device=cuda)
+            nb = rf.rf_mla_decode_workspace_size(sl.B, sl.Hq, sl.Lk, sl.d_qk, sl.d_v, 0)
+            self.wsml = torch.empty(nb, dtype=torch.uint8, device=cuda) if nb else None
+            self.calls["mla_decode"] = lambda: rf.rf_mla_decode(*d["mla_decode"], self.oml,
+                                                                sl.scale, self.wsml)
         for name, m in MOE_EXTRA.items():
             ix = torch.empty(m.T, m.k, dtype=torch.int32, device=cuda)
             wt = torch.empty(m.T, m.k, dtype=torch.float32, device=cuda)
@@ -242,6 +272,8 @@ class Step:
             self.outputs[name] = getattr(self, "out_" + name)
         if "prefill_varlen" in d:
             self.outputs["prefill_varlen"] = [self.ov]
+        if "mla_decode" in d:
+            self.outputs["mla_decode"] = [self.oml]
         for name in SHORT_EXTRA:
             if name in d:
                 self.outputs[name] = getattr(self, "out_" + name)
@@ -604,6 +636,15 @@ def oracle_sample_seconds(host, frac, only=None):
         G.moe_gate(x, w, m.k, rows=range(nt))
         out[name] = (time.perf_counter() - t, nt / m.T)
 
+    if "mla_decode" in host:
+        s = I.MLA_DECODE
+        q, c = host["mla_decode"]
+        nrows = min(s.B * s.Hq, max(1, int(round(frac * 4 * s.B * s.Hq))))
+        rows = [divmod(i, s.Hq) for i in range(nrows)]     # whole batches first
+        t = time.perf_counter()
+        A.mla_decode(q, c, s.scale, s.d_v, rows=rows)
+        out["mla_decode"] = (time.perf_counter() - t, nrows / (s.B * s.Hq))
+
     if "fp8_gemm" in host:
         s = I.FP8_GEMM
         x, wq, sw = host["fp8_gemm"]
@@ -727,7 +768,7 @@ def main():
     ap.add_argument("--only", default="",
                     help="comma-separated subset of ops (decode_32k, bert_prefill, moe_gate, "
                          "fp8_gemm, decode_2k) or calls outside the step (bert_prefill_causal, prefill_varlen, "
-                         "moe_gate_e8_k2, moe_gate_e256_k8, short256_incremental, short256_two_pass, "
+                         "moe_gate_e8_k2, moe_gate_e256_k8, mla_decode, short256_incremental, short256_two_pass, "
                          "short128_incremental, short128_two_pass); "
                          "default: the whole step")
     ap.add_argument("--splits", default="",

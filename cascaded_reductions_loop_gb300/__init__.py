@@ -23,7 +23,8 @@ __all__ = [
     "rf_attn_fwd", "rf_attn_fwd_ex", "rf_attn_fwd_varlen", "rf_attn_decode_splitkv",
     "rf_attn_decode_splitkv_num_splits",
     "rf_attn_decode_splitkv_workspace_size", "rf_attn_decode_splitkv_noalloc",
-    "RF_DECODE_NOALLOC_SCRATCH_BYTES", "rf_moe_gate_topk_softmax",
+    "RF_DECODE_NOALLOC_SCRATCH_BYTES", "rf_mla_decode", "rf_mla_decode_num_splits",
+    "rf_mla_decode_workspace_size", "rf_moe_gate_topk_softmax",
     "rf_absmax_fp8_gemm", "rf_absmax_fp8_gemm_workspace_size", "rf_selftest_wait_timeout",
     "RF_OK", "RF_ERR_INVALID_ARG", "RF_ERR_UNSUPPORTED", "RF_ERR_WORKSPACE", "RF_ERR_CUDA",
     "RF_ERR_DEVICE_TIMEOUT", "RF_ERR_DEVICE_INPUT", "RF_F32", "RF_BF16",
@@ -62,6 +63,9 @@ _SIGS = {
     "rf_attn_decode_splitkv_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I]),
     "rf_attn_decode_splitkv": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
     "rf_attn_decode_splitkv_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "rf_mla_decode_num_splits": (_I, [_I, _I, _I, _I, _I, _I]),
+    "rf_mla_decode_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I]),
+    "rf_mla_decode": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
     "rf_moe_gate_topk_softmax": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "rf_absmax_fp8_gemm_workspace_size": (_Z, [_I, _I, _I]),
     "rf_absmax_fp8_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _Z, _P]),
@@ -217,6 +221,32 @@ def rf_attn_decode_splitkv_noalloc(q, k, v, o, scale: float, num_splits: int = 0
     _check(lib.rf_attn_decode_splitkv_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, Hq, Hkv, Lk,
                                               d, float(scale), int(num_splits), _stream(stream)),
            "rf_attn_decode_splitkv_noalloc")
+
+
+def rf_mla_decode_num_splits(B, Hq, Lk, d_qk=576, d_v=512, num_splits=0) -> int:
+    return lib.rf_mla_decode_num_splits(B, Hq, Lk, d_qk, d_v, num_splits)
+
+
+def rf_mla_decode_workspace_size(B, Hq, Lk, d_qk=576, d_v=512, num_splits=0) -> int:
+    return lib.rf_mla_decode_workspace_size(B, Hq, Lk, d_qk, d_v, num_splits)
+
+
+def rf_mla_decode(q, ckv, o, scale: float, workspace=None, num_splits: int = 0,
+                  stream=None) -> None:
+    """Latent-KV (multi-latent attention) decode.  q: [B,Hq,d_qk] bf16; ckv:
+    [B,Lk,d_qk] bf16 latent cache (its first d_v dims are the values); o:
+    [B,Hq,d_v] bf16 out; workspace: a uint8 CUDA tensor of at least
+    rf_mla_decode_workspace_size(...) bytes, or None when that size is 0."""
+    B, Hq, d_qk = q.shape
+    Lk = ckv.shape[1]
+    d_v = o.shape[2]
+    _need(q, torch.bfloat16, (B, Hq, d_qk), "q")
+    _need(ckv, torch.bfloat16, (B, Lk, d_qk), "ckv")
+    _need(o, torch.bfloat16, (B, Hq, d_v), "o")
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.rf_mla_decode(_ptr(q), _ptr(ckv), _ptr(o), B, Hq, Lk, d_qk, d_v, float(scale),
+                             int(num_splits), _ptr(workspace), ws_bytes, _stream(stream)),
+           "rf_mla_decode")
 
 
 def rf_moe_gate_topk_softmax(x, w_gate, k: int, idx, weights, stream=None) -> None:

@@ -278,6 +278,44 @@ rf_status rf_attn_decode_splitkv(const void* Q, const void* K, const void* V, vo
                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
+static rf_status mla_shape_check(int B, int Hq, int Lk, int d_qk, int d_v, int num_splits) {
+  if (B < 1 || Hq < 1 || Lk < 1 || d_qk < 1 || d_v < 1 || num_splits < 0)
+    return RF_ERR_INVALID_ARG;
+  if ((int64_t)B * Lk >= (1ll << 31) || (int64_t)B * Hq >= (1ll << 31)) return RF_ERR_INVALID_ARG;
+  if (d_qk != 576 || d_v != 512 || Hq > 128) return RF_ERR_UNSUPPORTED;
+  return RF_OK;
+}
+
+int rf_mla_decode_num_splits(int B, int Hq, int Lk, int d_qk, int d_v, int num_splits) {
+  if (mla_shape_check(B, Hq, Lk, d_qk, d_v, num_splits) != RF_OK) return 0;
+  const int S = mla_num_splits(B, Hq, Lk, num_splits);
+  if (S < 1 || (int64_t)B * S * 2 >= (1ll << 31)) return 0;
+  return S;
+}
+
+size_t rf_mla_decode_workspace_size(int B, int Hq, int Lk, int d_qk, int d_v, int num_splits) {
+  const int S = rf_mla_decode_num_splits(B, Hq, Lk, d_qk, d_v, num_splits);
+  return S < 1 ? 0 : mla_workspace_bytes(B, Hq, S);
+}
+
+rf_status rf_mla_decode(const void* Q, const void* CKV, void* O, int B, int Hq, int Lk, int d_qk,
+                        int d_v, float scale, int num_splits, void* workspace,
+                        size_t workspace_bytes, rf_stream_t stream) {
+  if (!ptr_ok(Q) || !ptr_ok(CKV) || !ptr_ok(O)) return RF_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !(scale < INFINITY)) return RF_ERR_INVALID_ARG;
+  rf_status st = mla_shape_check(B, Hq, Lk, d_qk, d_v, num_splits);
+  if (st != RF_OK) return st;
+  const int S = rf_mla_decode_num_splits(B, Hq, Lk, d_qk, d_v, num_splits);
+  if (S < 1) return RF_ERR_CUDA;   // the automatic choice needs the device's SM count
+  const size_t need = mla_workspace_bytes(B, Hq, S);
+  if (need > 0 && (!workspace || !aligned16(workspace) || workspace_bytes < need))
+    return RF_ERR_WORKSPACE;
+  unsigned* err = device_error_word();
+  if (!err) return RF_ERR_CUDA;
+  return from_cuda(launch_mla_decode(Q, CKV, O, B, Hq, Lk, scale, S, workspace, err,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
 rf_status rf_moe_gate_topk_softmax(const void* X, const void* Wg, int T, int D, int E, int k,
                                    int32_t* idx, float* w, rf_stream_t stream) {
   if (!ptr_ok(X) || !ptr_ok(Wg) || !ptr_ok(idx) || !ptr_ok(w)) return RF_ERR_INVALID_ARG;

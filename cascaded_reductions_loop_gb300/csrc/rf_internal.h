@@ -61,6 +61,12 @@ cudaError_t launch_decode_splitkv(const void* Q, const void* K, const void* V, v
                                   int Hq, int Hkv, int Lk, int d, float scale, int S,
                                   void* workspace, unsigned* err, cudaStream_t s);
 
+// Latent-KV decode: Q [B][Hq][576], CKV [B][Lk][576], O [B][Hq][512] (bf16).
+int mla_num_splits(int B, int Hq, int Lk, int requested);
+size_t mla_workspace_bytes(int B, int Hq, int S);
+cudaError_t launch_mla_decode(const void* Q, const void* CKV, void* O, int B, int Hq, int Lk,
+                              float scale, int S, void* workspace, unsigned* err, cudaStream_t s);
+
 cudaError_t launch_moe_gate(const void* X, const void* Wg, int T, int D, int E, int k,
                             int32_t* idx, float* w, unsigned* err, cudaStream_t s);
 

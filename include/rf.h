@@ -212,6 +212,52 @@ rf_status rf_attn_decode_splitkv_noalloc(const void* Q, const void* K, const voi
                                          int num_splits, rf_stream_t stream);
 
 /*
+ * Number of key segments per batch that rf_mla_decode uses for this shape
+ * when its num_splits argument is `num_splits` (0 = automatic: one segment
+ * unless the batches alone leave most SMs idle).  Returns 0 for an invalid
+ * or unsupported shape.
+ */
+int rf_mla_decode_num_splits(int B, int Hq, int Lk, int d_qk, int d_v, int num_splits);
+
+/* Workspace bytes rf_mla_decode needs for the same arguments (0 when it
+ * uses one segment per batch). */
+size_t rf_mla_decode_workspace_size(int B, int Hq, int Lk, int d_qk, int d_v, int num_splits);
+
+/*
+ * Latent-KV (multi-latent attention) decode, absorbed form -- the
+ * technical summary's MLA workload ([S] "Resultaten"), whose operation the
+ * pages do not define; the public definition is used.  One query token per
+ * (b, head); every head of batch b attends to the one latent cache of b:
+ *   Q    [B][Hq][d_qk] bf16   (latent part, then positional part)
+ *   CKV  [B][Lk][d_qk] bf16   (cache rows: the first d_v dims are the latent
+ *                              vector, which also serves as the value)
+ *   O    [B][Hq][d_v]  bf16
+ *   s_j = scale * Q[b,h,:] . CKV[b,j,:]   (all d_qk dims)
+ *   O[b,h,:] = sum_j softmax(s)_j CKV[b,j,0:d_v]
+ * computed as the safe-softmax cascade in one incremental loop over tiles
+ * of 32 cache rows ([E] §2.3, §4.1), on a cluster of two CTAs per (batch,
+ * segment) that exchange partial scores; with more than one segment, the
+ * partial states (m, l, o) of the segments are merged by a second kernel
+ * ([S] Methodologie 3).
+ *   Sizes   B, Lk >= 1; 1 <= Hq <= 128; d_qk = 576 and d_v = 512 (else
+ *           RF_ERR_UNSUPPORTED); scale finite, > 0.
+ *   num_splits  0 = automatic, else the requested number of segments
+ *           (clamped to whole 32-row tiles: rf_mla_decode_num_splits tells
+ *           the count used).
+ *   workspace   device buffer of at least rf_mla_decode_workspace_size(...)
+ *           bytes, 16-byte aligned, owned by the caller; may be NULL when
+ *           that size is 0.  Contents need not be initialised and are
+ *           unspecified on return.
+ * All pointers are device pointers, 16-byte aligned.
+ * Errors: RF_ERR_INVALID_ARG, RF_ERR_UNSUPPORTED, RF_ERR_WORKSPACE,
+ * RF_ERR_CUDA; a bounded wait that runs out on the device (or cluster peer)
+ * is reported by rf_get_device_status as RF_ERR_DEVICE_TIMEOUT.
+ */
+rf_status rf_mla_decode(const void* Q, const void* CKV, void* O, int B, int Hq, int Lk, int d_qk,
+                        int d_v, float scale, int num_splits, void* workspace,
+                        size_t workspace_bytes, rf_stream_t stream);
+
+/*
  * Fused MoE gate ([E] §4.2): scores = x . W_gate^T, top-k experts per token,
  * softmax over the k selected scores; the score matrix never reaches
  * global memory.

@@ -5,6 +5,10 @@ Tolerances (written here once, used by every parity test):
   max-abs error <= 2e-2 and relative L2 error <= 5e-3 against the fp64
   oracle.  Sources of error: bf16 P (2^-9 relative per weight), fp32
   accumulation, bf16 output rounding (2^-9 relative).
+* bf16 attention outputs that the test's own input construction makes large
+  (|O| well above the ~1 of N(0, 1) workloads, e.g. cache rows scaled up):
+  the same bounds with the max-abs one scaled, |O - O_ref| <= 2e-2 *
+  max(1, |O_ref|), since both bf16 roundings (P and O) are relative.
 * fp32 tiny attention: relative L2 <= 1e-5 and
   |O - O_ref| <= 1e-5 * max(1, |O_ref|) elementwise.
 * FP8 GEMM output Y (magnitudes up to ~1e3, where one bf16 ulp is 4 or
@@ -44,6 +48,15 @@ def assert_bf16_close(got, ref, what=""):
     r = rel_l2(got, ref)
     assert err <= BF16_MAX_ABS, f"{what}: max-abs {err:.3e} > {BF16_MAX_ABS}"
     assert r <= BF16_REL_L2, f"{what}: rel-L2 {r:.3e} > {BF16_REL_L2}"
+
+
+def assert_bf16_close_scaled(got, ref, what=""):
+    got, ref = to64(got), to64(ref)
+    assert np.isfinite(got).all(), f"{what}: non-finite output (unwritten element?)"
+    bound = BF16_MAX_ABS * np.maximum(1.0, np.abs(ref))
+    bad = np.abs(got - ref) > bound
+    assert not bad.any(), f"{what}: {bad.sum()} elements outside 2e-2 * max(1, |ref|)"
+    assert rel_l2(got, ref) <= BF16_REL_L2, f"{what}: rel-L2 {rel_l2(got, ref):.3e}"
 
 
 def assert_f32_close(got, ref, what=""):

@@ -28,7 +28,7 @@ def _declared():
 
 def test_header_declares_the_boundary():
     names = _declared()
-    for n in ("rf_attn_fwd", "rf_attn_decode_splitkv", "rf_moe_gate_topk_softmax",
+    for n in ("rf_attn_fwd", "rf_attn_decode_splitkv", "rf_mla_decode", "rf_moe_gate_topk_softmax",
               "rf_absmax_fp8_gemm", "rf_status_string", "rf_get_device_status"):
         assert n in names
 
@@ -87,6 +87,27 @@ def test_validation_rejects_bad_arguments_without_a_gpu(rf):
     # one (m, l, o) partial state per (batch, query head, segment, warp of 4)
     assert rf.rf_attn_decode_splitkv_workspace_size(2, 8, 2, 64, 128, 4) == 2 * 8 * 4 * 4 * (128 + 2) * 4
     assert rf.rf_attn_decode_splitkv_num_splits(1, 6, 4, 64, 128, 0) == 0
+    # latent-KV decode: sizes, head count, latent widths, workspace of a split request
+    M = L.rf_mla_decode
+    assert M(null, p, p, 2, 128, 100, 576, 512, 0.1, 1, null, 0, None) == rf.RF_ERR_INVALID_ARG
+    assert M(p, mis, p, 2, 128, 100, 576, 512, 0.1, 1, null, 0, None) == rf.RF_ERR_INVALID_ARG
+    assert M(p, p, p, 0, 128, 100, 576, 512, 0.1, 1, null, 0, None) == rf.RF_ERR_INVALID_ARG
+    assert M(p, p, p, 2, 128, 0, 576, 512, 0.1, 1, null, 0, None) == rf.RF_ERR_INVALID_ARG
+    assert M(p, p, p, 2, 128, 100, 576, 512, 0.0, 1, null, 0, None) == rf.RF_ERR_INVALID_ARG
+    assert M(p, p, p, 2, 128, 100, 576, 512, 0.1, -1, null, 0, None) == rf.RF_ERR_INVALID_ARG
+    assert M(p, p, p, 2, 129, 100, 576, 512, 0.1, 1, null, 0, None) == rf.RF_ERR_UNSUPPORTED
+    assert M(p, p, p, 2, 128, 100, 192, 128, 0.1, 1, null, 0, None) == rf.RF_ERR_UNSUPPORTED
+    assert M(p, p, p, 2, 128, 100, 576, 512, 0.1, 2, null, 0, None) == rf.RF_ERR_WORKSPACE
+    assert M(p, p, p, 2, 128, 100, 576, 512, 0.1, 2, p, 1024, None) == rf.RF_ERR_WORKSPACE
+    # segments hold whole 32-row tiles: 100 rows = 4 tiles; a request of 3
+    # gives tiles of 2 and so 2 segments; of 9, one tile each
+    assert rf.rf_mla_decode_num_splits(2, 128, 100, 576, 512, 3) == 2
+    assert rf.rf_mla_decode_num_splits(2, 128, 100, 576, 512, 9) == 4
+    assert rf.rf_mla_decode_num_splits(2, 128, 100, 576, 512, 1) == 1
+    assert rf.rf_mla_decode_workspace_size(2, 128, 100, 576, 512, 1) == 0
+    n = 2 * 128 * 2
+    assert rf.rf_mla_decode_workspace_size(2, 128, 100, 576, 512, 2) == n * 512 * 4 + n * 2 * 4
+    assert rf.rf_mla_decode_num_splits(2, 129, 100, 576, 512, 1) == 0
     # MoE: D not a multiple of 8, k out of range, E not covered
     assert L.rf_moe_gate_topk_softmax(p, p, 16, 100, 64, 2, p, p, None) == rf.RF_ERR_INVALID_ARG
     assert L.rf_moe_gate_topk_softmax(p, p, 16, 128, 64, 0, p, p, None) == rf.RF_ERR_INVALID_ARG
