@@ -6,7 +6,7 @@
 // latent cache rows C_b [Lk, 576]: s = scale * q . c over all 576 dims (512
 // latent + 64 positional) and o = softmax(s) . C_b[:, 0:512].  This is the
 // safe-softmax cascade ([E] §2.2) in the single-loop incremental form ([E]
-// §2.3, §4.1; [S] Methodologie 2) over tiles of 32 cache rows, and, when the
+// §2.3, §4.1; [S] Methodologie 2) over tiles of 64 cache rows, and, when the
 // rows of a batch are cut into segments, the multi-segment form with a merge
 // kernel ([S] Methodologie 3; [E] §3.3).
 //
@@ -15,20 +15,28 @@
 // it: a cluster of two CTAs, CTA r owning the value dims 256 r .. 256 r + 255.
 // Each CTA loads only its own 64-dim blocks of every cache row (CTA 0: blocks
 // 0-3 and the positional block 8; CTA 1: blocks 4-7) and computes a partial
-// score tile over them.  The two fp32 partial tiles (128 heads x 32 rows) are
-// swapped through distributed shared memory (st.async, whose bytes complete a
-// barrier in the receiving CTA), and both CTAs form s = S_0 + S_1 -- the same
+// score tile over them.  The two fp32 partial tiles (128 heads x 64 rows) are
+// swapped through distributed shared memory (bulk copies, whose bytes complete
+// a barrier in the receiving CTA), and both CTAs form s = S_0 + S_1 -- the same
 // bits on both sides, as a + b = b + a exactly -- so they run the identical
 // softmax: the same maxima, the same P, the same l.  The value block of a CTA
 // is the latent part of what it loaded, so P . V needs no further exchange.
 //
 // Per CTA: its Q dims sit in tensor memory (written once by the softmax
 // warps) as the A operand of the score products; the cache rows stream by TMA
-// through an 8-stage ring (32 rows x 64 dims per block, 128-byte swizzle);
-// S is triple-buffered in tensor memory and P (bf16) double-buffered in
-// shared memory; O accumulates in tensor memory.  The softmax warps ship the
-// partial scores of tile j + 2 right after handing P_j to the tensor core, so
-// the peer's scores of a tile are in place before they are needed.
+// through a 3-stage ring (64 rows x 64 dims per block, 128-byte swizzle), with
+// the tiles beyond the ring prefetched into L2; S has one buffer in tensor
+// memory, P (bf16) two in shared memory, O accumulates in tensor memory.  The
+// MMA warp issues whichever product is ready (S_t once the softmax warps have
+// taken S_{t-1} and the tile has landed; P_j V_j once P_j is written).  The
+// softmax warps, at tile j, add the peer's partial S_j to their own, then at
+// once take their own S_{j+1} out of tensor memory (freeing it for S_{j+2}) and
+// ship it to the peer, so the exchange of tile j+1 runs under the softmax of
+// tile j.  Two exchange slots per CTA suffice, each serving in turn as the
+// landing place of a peer tile and the staging place of an own tile: the peer
+// reads our S_{j-1} before it ships its S_j, so its S_j landing here frees the
+// peer slot our S_{j+1} goes to; and the peer ships S_{j+2} into the slot our
+// S_{j+1} was staged in only after that copy has landed.
 //
 // Lazy rescaling: a row's reference maximum m moves only when a tile's
 // maximum exceeds it by more than 8 (log2 units); only then are O (in tensor
@@ -36,7 +44,7 @@
 // dependent factor makes the result independent of the reference chosen ([S]
 // Methodologie 1), and P <= 2^8 keeps bf16 P and fp32 sums far from overflow.
 //
-// Tensor memory (512 columns): O 0-255, S buffers 256-351, Q 352-511.
+// Tensor memory (512 columns): O 0-255, S 256-319, Q 352-511.
 #include <math.h>
 
 #include "rf_device.cuh"
@@ -47,17 +55,18 @@ namespace {
 
 constexpr int kDqk = 576, kDv = 512;
 constexpr int BH = 128;                            // head rows (MMA M)
-constexpr int BN = 32;                             // cache rows per tile
+constexpr int BN = 64;                             // cache rows per tile
 constexpr int kMaxBlk = 5;                         // 64-dim blocks per CTA
-constexpr int kStages = 8;
-constexpr int kNX = 3;                             // S buffers, exchange slots
-constexpr int kChBytes = BN * 128;                 // one 64-dim block of a tile: 4 KB
-constexpr int kStageBytes = kMaxBlk * kChBytes;    // 20 KB
-constexpr int kXBytes = BH * BN * 4;               // one partial score tile: 16 KB
+constexpr int kStages = 3;
+constexpr int kPrefetch = 4;                       // tiles beyond the ring prefetched into L2
+constexpr int kChBytes = BN * 128;                 // one 64-dim block of a tile: 8 KB
+constexpr int kStageBytes = kMaxBlk * kChBytes;    // 40 KB
+constexpr int kPBytes = BH * 128;                  // P of one tile: 16 KB
+constexpr int kXBytes = BH * BN * 4;               // one partial score tile: 32 KB
 constexpr int kStOff = 0;
-constexpr int kPOff = kStOff + kStages * kStageBytes;   // 160 KB
-constexpr int kXOff = kPOff + BH * 128;                 // 176 KB
-constexpr int kBarOff = kXOff + kNX * kXBytes;          // 224 KB
+constexpr int kPOff = kStOff + kStages * kStageBytes;   // 120 KB
+constexpr int kXOff = kPOff + 2 * kPBytes;              // 152 KB
+constexpr int kBarOff = kXOff + 2 * kXBytes;            // 216 KB
 constexpr int kSmem = kBarOff + 512;
 constexpr int kThreads = 192;                      // warp 0 TMA, 1 MMA, 2-5 softmax
 constexpr int kTmemCols = 512;
@@ -76,11 +85,11 @@ __device__ __forceinline__ float ex2(float x) {
 struct Bars {
   uint64_t q_full;                  // Q in tensor memory (128 softmax threads)
   uint64_t full[kStages], empty[kStages];
-  uint64_t s_full[kNX];             // own partial S_t in buffer t % 3
-  uint64_t s_free[kNX];             // buffer read by the softmax warps
-  uint64_t p_full[2];               // P_j in half j % 2 of the P tile
+  uint64_t s_full;                  // own partial S_t in tensor memory
+  uint64_t s_free;                  // S_t taken by the softmax warps
+  uint64_t p_full[2];               // P_j in P buffer j % 2
   uint64_t pv_done[2];              // P_j V_j accumulated into O
-  uint64_t x_full[kNX];             // the peer's partial S_t in slot t % 3 (st.async bytes)
+  uint64_t x_full[2];               // the peer's partial S_t in slot t % 2 (st.async bytes)
   uint64_t drain;
   uint32_t tmem;
   int abort;
@@ -124,20 +133,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bars->full[i]), 1);
       mbar_init(smem_u32(&bars->empty[i]), 1);
     }
-    for (int i = 0; i < kNX; ++i) {
-      mbar_init(smem_u32(&bars->s_full[i]), 1);
-      mbar_init(smem_u32(&bars->s_free[i]), BH);
-      mbar_init(smem_u32(&bars->x_full[i]), 1);
-    }
+    mbar_init(smem_u32(&bars->s_full), 1);
+    mbar_init(smem_u32(&bars->s_free), BH);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars->p_full[i]), BH);
       mbar_init(smem_u32(&bars->pv_done[i]), 1);
+      mbar_init(smem_u32(&bars->x_full[i]), 1);
     }
     mbar_init(smem_u32(&bars->drain), 1);
     bars->abort = 0;
     fence_mbar_init();
-    // armed for the peer's first partial tiles; re-armed as slots are read
-    for (int i = 0; i < kNX && i < nt; ++i)
+    // armed for the peer's first two partial tiles; re-armed as slots are read
+    for (int i = 0; i < 2 && i < nt; ++i)
       mbar_arrive_expect_tx(smem_u32(&bars->x_full[i]), kXBytes);
   }
   if (warp == 1) {
@@ -156,8 +163,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ------------------------------------------------ TMA producer
       const uint64_t pol = policy_evict_first();       // every cache row is read once
       const int32_t row0 = b * Lk + lo;
-      int issued = 0;
+      // next tile to prefetch into L2; never the segment's last tile, the one
+      // that can reach past the end of the tensor
+      int issued = 0, pf = kStages;
       for (int t = 0; t < nt && !*abort_flag; ++t) {
+        for (; pf < nt - 1 && pf < t + kStages + kPrefetch; ++pf)
+          for (int c = 0; c < nblk; ++c) tma_prefetch_2d(&tmC, 64 * dim_block(rank, c), row0 + pf * BN);
         const int st = t % kStages;
         if (t >= kStages &&
             !mbar_wait(smem_u32(&bars->empty[st]), (uint32_t)(((t / kStages) - 1) & 1))) {
@@ -181,50 +192,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0 && nt > 0) {
-      // ------------------------------------------------ MMA issuer
+      // ------------------------------------------------ MMA issuer (event loop)
       const uint32_t p_addr = smem_u32(smem + kPOff);
-      // partial S_t = Q_r C_t,r^T over this CTA's dims into buffer t % 3
-      auto issue_s = [&](int t) -> bool {
-        const int u = t % kNX, st = t % kStages;
-        if (t >= kNX &&
-            !mbar_wait(smem_u32(&bars->s_free[u]), (uint32_t)(((t / kNX) - 1) & 1)))
-          return false;
-        if (!mbar_wait(smem_u32(&bars->full[st]), (uint32_t)((t / kStages) & 1))) return false;
-        tc_fence_after();
-        const uint32_t sb = smem_u32(smem + kStOff + st * kStageBytes);
-        for (int c = 0; c < nblk; ++c) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ts(tm + kTmemS + u * BN, tm + kTmemQ + c * 32 + kk * 8,
-                        sw128_desc(sb + c * kChBytes + kk * 32, 1024, 16), kIdescS, (c | kk) != 0);
-        }
-        mma_commit(smem_u32(&bars->s_full[u]));
-        return true;
-      };
       bool ok = mbar_wait(smem_u32(&bars->q_full), 0);
       if (ok) tc_fence_after();
-      for (int t = 0; ok && t < kNX && t < nt; ++t) ok = issue_s(t);
-      for (int j = 0; ok && j < nt; ++j) {
-        if (!mbar_wait(smem_u32(&bars->p_full[j & 1]), (uint32_t)((j >> 1) & 1))) {
+      int ns = 0, npv = 0;                             // next S / next P.V to issue
+      uint64_t t_prog = globaltimer_ns();
+      uint32_t idle = 0;
+      while (ok && npv < nt) {
+        if (npv < ns && mbar_test_wait(smem_u32(&bars->p_full[npv & 1]), (uint32_t)((npv >> 1) & 1))) {
+          // O[:, 64 blk ..] (+)= P_j V_j,blk
+          tc_fence_after();
+          const int st = npv % kStages;
+          const uint32_t sb = smem_u32(smem + kStOff + st * kStageBytes);
+          const uint32_t pj = p_addr + (npv & 1) * kPBytes;
+#pragma unroll
+          for (int blk = 0; blk < 4; ++blk) {
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_bf16_ss(tm + 64 * blk, sw128_desc(pj + kk * 32, 1024, 16),
+                          sw128_desc(sb + blk * kChBytes + kk * 16 * 128, 1024, kChBytes), kIdescO,
+                          (npv | kk) != 0);
+          }
+          mma_commit(smem_u32(&bars->pv_done[npv & 1]));
+          mma_commit(smem_u32(&bars->empty[st]));
+          ++npv;
+          t_prog = globaltimer_ns();
+        } else if (ns < nt &&
+                   (ns == 0 || mbar_test_wait(smem_u32(&bars->s_free), (uint32_t)((ns - 1) & 1))) &&
+                   mbar_test_wait(smem_u32(&bars->full[ns % kStages]), (uint32_t)((ns / kStages) & 1))) {
+          // partial S_t = Q_r C_t,r^T over this CTA's dims
+          tc_fence_after();
+          const uint32_t sb = smem_u32(smem + kStOff + (ns % kStages) * kStageBytes);
+          for (int c = 0; c < nblk; ++c) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16_ts(tm + kTmemS, tm + kTmemQ + c * 32 + kk * 8,
+                          sw128_desc(sb + c * kChBytes + kk * 32, 1024, 16), kIdescS,
+                          (c | kk) != 0);
+          }
+          mma_commit(smem_u32(&bars->s_full));
+          ++ns;
+          t_prog = globaltimer_ns();
+        } else if ((++idle & 63u) == 0 &&
+                   (*abort_flag || globaltimer_ns() - t_prog > kDefaultWaitNs)) {
           ok = false;
-          break;
         }
-        tc_fence_after();
-        // O[:, 64 blk ..] (+)= P_j V_j,blk
-        const int st = j % kStages;
-        const uint32_t sb = smem_u32(smem + kStOff + st * kStageBytes);
-        const uint32_t pj = p_addr + (j & 1) * 64;
-#pragma unroll
-        for (int blk = 0; blk < 4; ++blk) {
-#pragma unroll
-          for (int kk = 0; kk < 2; ++kk)
-            mma_bf16_ss(tm + 64 * blk, sw128_desc(pj + kk * 32, 1024, 16),
-                        sw128_desc(sb + blk * kChBytes + kk * 16 * 128, 1024, kChBytes), kIdescO,
-                        (j | kk) != 0);
-        }
-        mma_commit(smem_u32(&bars->pv_done[j & 1]));
-        mma_commit(smem_u32(&bars->empty[st]));
-        if (j + kNX < nt) ok = issue_s(j + kNX);
       }
       if (!ok) {
         raise_error(err, kDevErrTimeout);
@@ -264,83 +277,89 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(smem_u32(&bars->q_full));
     }
 
-    // own partial S_t -> the peer's exchange slot t % 3.  The slot held our
-    // S_{t-3}; the peer reads it before it sends its own S_{t-1}, so once the
-    // peer's S_{t-1} has landed here (all 128 rows) the slot is free: no
-    // separate release message is needed.
-    auto send = [&](int t) -> bool {
-      const int u = t % kNX;
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[u]), (uint32_t)((t / kNX) & 1)) &&
-                                       !*abort_flag))
+    // own partial S_t out of tensor memory (which may then take S_{t+1}) and
+    // into the peer's exchange slot t % 2.  The rows are staged in this CTA's
+    // slot (t + 1) % 2 -- the one whose peer tile S_{t-1} each thread has just
+    // read (its own row) -- and each warp bulk-copies its 32 rows (8 KB): a
+    // copy engine moves them several times faster than per-thread remote
+    // stores.  The peer writes its S_{t+1} into that slot only after our S_t
+    // has landed there, i.e. after the copy has read it.
+    auto take_and_send = [&](int t, float (&own)[BN]) -> bool {
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(smem_u32(&bars->s_full), (uint32_t)(t & 1)) && !*abort_flag))
         return false;
       tc_fence_after();
       uint32_t v[32];
-      tmem_ld32(tm + lane_off + kTmemS + u * BN, v);
-      tmem_ld_wait();
-      if (t >= kNX &&
-          !__all_sync(0xffffffffu, mbar_wait_cluster(smem_u32(&bars->x_full[(t - 1) % kNX]),
-                                                     (uint32_t)(((t - 1) / kNX) & 1)) &&
-                                       !*abort_flag))
-        return false;
-      const uint32_t dst = x_peer + u * kXBytes + r * 128;
-      const uint32_t rbar = mapa_shared(smem_u32(&bars->x_full[u]), (uint32_t)peer);
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        st_async_v4(dst + ((c ^ swz) << 4), v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3],
-                    rbar);
+      for (int h = 0; h < 2; ++h) {
+        tmem_ld32(tm + lane_off + kTmemS + 32 * h, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) own[32 * h + i] = __uint_as_float(v[i]);
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars->s_free));
+      uint8_t* stage = smem + kXOff + ((t + 1) & 1) * kXBytes;
+#pragma unroll
+      for (int c = 0; c < BN / 4; ++c)
+        *reinterpret_cast<uint4*>(stage + r * (BN * 4) + ((c ^ swz) << 4)) =
+            make_uint4(__float_as_uint(own[4 * c]), __float_as_uint(own[4 * c + 1]),
+                       __float_as_uint(own[4 * c + 2]), __float_as_uint(own[4 * c + 3]));
+      fence_proxy_async_smem();                      // rows visible to the copy engine
+      __syncwarp();
+      if (lane == 0) {
+        const uint32_t blk = (uint32_t)(sub * 32 * BN * 4);   // this warp's 32 rows
+        bulk_copy_to_peer(x_peer + (t & 1) * kXBytes + blk, smem_u32(stage) + blk, 32 * BN * 4,
+                          mapa_shared(smem_u32(&bars->x_full[t & 1]), (uint32_t)peer));
+      }
       return true;
     };
 
     float m_run = -INFINITY, l_run = 0.f;
     const uint64_t c2 = f2(c_log2, c_log2);
-    bool ok = send(0) && (nt < 2 || send(1));
+    float own[BN];
+    bool ok = take_and_send(0, own);
     for (int j = 0; ok && j < nt; ++j) {
-      const int u = j % kNX;
-      // (a) the peer's partial scores of tile j
+      // (a) s = own + the peer's partial scores of tile j
       if (!__all_sync(0xffffffffu,
-                      mbar_wait_cluster(smem_u32(&bars->x_full[u]), (uint32_t)((j / kNX) & 1)) &&
+                      mbar_wait_cluster(smem_u32(&bars->x_full[j & 1]), (uint32_t)((j >> 1) & 1)) &&
                           !*abort_flag)) {
         ok = false;
         break;
       }
-      // armed for the peer's S_{j+3}, which it sends only after our S_{j+2}
-      // has reached it (the phase of S_j is complete here by then)
-      if (sub == 0 && lane == 0 && j + kNX < nt)
-        mbar_arrive_expect_tx(smem_u32(&bars->x_full[u]), kXBytes);
-      float sc[32];
+      // armed for the peer's S_{j+2}, which it ships only after our S_{j+1}
+      // has reached it (the phase of S_j here is complete by then)
+      if (sub == 0 && lane == 0 && j + 2 < nt)
+        mbar_arrive_expect_tx(smem_u32(&bars->x_full[j & 1]), kXBytes);
+      float sc[BN];
       {
-        const uint8_t* src = smem + kXOff + u * kXBytes + r * 128;
+        const uint8_t* src = smem + kXOff + (j & 1) * kXBytes + r * (BN * 4);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < BN / 4; ++c) {
           const uint4 w = *reinterpret_cast<const uint4*>(src + ((c ^ swz) << 4));
-          sc[4 * c] = __uint_as_float(w.x);
-          sc[4 * c + 1] = __uint_as_float(w.y);
-          sc[4 * c + 2] = __uint_as_float(w.z);
-          sc[4 * c + 3] = __uint_as_float(w.w);
+          sc[4 * c] = own[4 * c] + __uint_as_float(w.x);
+          sc[4 * c + 1] = own[4 * c + 1] + __uint_as_float(w.y);
+          sc[4 * c + 2] = own[4 * c + 2] + __uint_as_float(w.z);
+          sc[4 * c + 3] = own[4 * c + 3] + __uint_as_float(w.w);
         }
       }
-      // (b) plus the own partial scores (complete: waited for before sending)
-      tc_fence_after();
-      {
-        uint32_t v[32];
-        tmem_ld32(tm + lane_off + kTmemS + u * BN, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sc[i] = __uint_as_float(v[i]) + sc[i];
+      // (b) the next tile's own partial goes to the peer now, under this
+      // tile's softmax (the peer's S_j landing here freed slot (j + 1) % 2)
+      if (j + 1 < nt && !take_and_send(j + 1, own)) {
+        ok = false;
+        break;
       }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bars->s_free[u]));
 
       // (c) online softmax with a lazily moved reference maximum
       const int valid = min(BN, hi - (lo + j * BN));   // rows of this tile in the segment
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (valid == BN) {
 #pragma unroll
-        for (int i = 0; i < 32; i += 2)
+        for (int i = 0; i < BN; i += 2)
           mx4[(i >> 1) & 3] = fmax3(mx4[(i >> 1) & 3], sc[i], sc[i + 1]);
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
+        for (int i = 0; i < BN; ++i)
           if (i < valid) mx4[i & 3] = fmaxf(mx4[i & 3], sc[i]);
       }
       const float mt = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]) * c_log2;
@@ -355,10 +374,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         need = true;
       }
       const uint64_t negm2 = f2(-m_run, -m_run);
-      uint32_t pk[16];
-      uint64_t sum2[2] = {0ull, 0ull};
+      uint32_t pk[BN / 2];
+      uint64_t sum4[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
+      for (int i = 0; i < BN / 2; ++i) {
         float e0, e1;
         f2_split(ffma2(f2(sc[2 * i], sc[2 * i + 1]), c2, negm2), e0, e1);
         float p0 = ex2(e0), p1 = ex2(e1);
@@ -366,14 +385,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           p0 = 2 * i < valid ? p0 : 0.f;
           p1 = 2 * i + 1 < valid ? p1 : 0.f;
         }
-        sum2[i & 1] = fadd2(sum2[i & 1], f2(p0, p1));
+        sum4[i & 3] = fadd2(sum4[i & 3], f2(p0, p1));
         pk[i] = pack_bf16x2(p0, p1);
       }
       float s_lo, s_hi;
-      f2_split(fadd2(sum2[0], sum2[1]), s_lo, s_hi);
+      f2_split(fadd2(fadd2(sum4[0], sum4[1]), fadd2(sum4[2], sum4[3])), s_lo, s_hi);
       l_run += s_lo + s_hi;
 
-      // P half j % 2 is free once P_{j-2} V_{j-2} is done
+      // P buffer j % 2 is free once P_{j-2} V_{j-2} is done
       if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->pv_done[j & 1]),
                                                        (uint32_t)(((j - 2) >> 1) & 1)) &&
                                                  !*abort_flag)) {
@@ -400,22 +419,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st_wait();
       }
-      // keys 8c .. 8c+7 of this tile = 16-byte chunk (j % 2) * 4 + c of row r
-      uint8_t* prow = smem + kPOff + r * 128;
+      // keys 8c .. 8c+7 of this tile = 16-byte chunk c of row r (128-byte swizzle)
+      uint8_t* prow = smem + kPOff + (j & 1) * kPBytes + r * 128;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int chunk = (j & 1) * 4 + c;
-        *reinterpret_cast<uint4*>(prow + ((chunk ^ swz) << 4)) =
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(prow + ((c ^ swz) << 4)) =
             make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      }
       fence_proxy_async_smem();                        // P visible to the tensor core
       tc_fence_before();
       mbar_arrive(smem_u32(&bars->p_full[j & 1]));
-      // (d) ship the own partial scores of tile j + 2
-      if (j + 2 < nt && !send(j + 2)) {
-        ok = false;
-        break;
-      }
     }
 
     // epilogue: O of this CTA's 256 dims, normalised (one segment) or as a
@@ -478,8 +490,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tm, kTmemCols);
   }
-  // the peer may still write into this CTA's exchange slots or arrive on its
-  // barriers until both CTAs are done
+  // the peer may still write into this CTA's exchange slots until both CTAs
+  // are done
   cluster_sync();
 }
 

@@ -66,6 +66,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking probe: true if the phase with the given parity has completed.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits until the barrier's phase with the given parity has completed, for at
 // most `limit_ns` nanoseconds.  Returns false if the limit ran out; the caller
 // then records the timeout and takes its exit path.  Never spins unbounded.
@@ -125,6 +138,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z)
       : "memory");
+}
+
+// Hint to bring a 2-D box of a tensor into L2 (no shared-memory destination,
+// no completion tracking).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* m, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(x), "r"(y)
+               : "memory");
 }
 
 // 2-D tiled load multicast to every CTA of the cluster in `cta_mask`: the
@@ -328,22 +350,16 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
   return r;
 }
 
-// 16 bytes into another CTA's shared memory (address from mapa_shared); the
-// bytes count towards the transaction count of the barrier `remote_bar` in
-// that CTA, which completes its phase once every expected byte has landed.
-__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint32_t a, uint32_t b,
-                                            uint32_t c, uint32_t d, uint32_t remote_bar) {
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
+// this CTA's shared memory to another CTA's (dst and remote_bar from
+// mapa_shared); the bytes complete the transaction count of remote_bar.  The
+// source must have been written before a fence_proxy_async_smem().
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                  uint32_t remote_bar) {
   asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
-      ::"r"(remote_addr), "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar)
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "r"(src), "r"(bytes), "r"(remote_bar)
       : "memory");
-}
-
-// Arrival on a barrier of another CTA of the cluster, ordered after this
-// thread's earlier memory accesses at cluster scope.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
-               : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
@@ -358,8 +374,8 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return ok != 0;
 }
 
-// mbar_wait for a barrier completed by another CTA (remote arrivals or
-// st.async bytes): acquires at cluster scope.  Bounded like mbar_wait.
+// mbar_wait for a barrier completed from another CTA (bytes of a bulk copy
+// to this CTA): acquires at cluster scope.  Bounded like mbar_wait.
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
                                                   uint64_t limit_ns = kDefaultWaitNs) {
   if (mbar_try_wait_cluster(bar, parity)) return true;

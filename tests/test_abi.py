@@ -99,10 +99,12 @@ def test_validation_rejects_bad_arguments_without_a_gpu(rf):
     assert M(p, p, p, 2, 128, 100, 192, 128, 0.1, 1, null, 0, None) == rf.RF_ERR_UNSUPPORTED
     assert M(p, p, p, 2, 128, 100, 576, 512, 0.1, 2, null, 0, None) == rf.RF_ERR_WORKSPACE
     assert M(p, p, p, 2, 128, 100, 576, 512, 0.1, 2, p, 1024, None) == rf.RF_ERR_WORKSPACE
-    # segments hold whole 32-row tiles: 100 rows = 4 tiles; a request of 3
-    # gives tiles of 2 and so 2 segments; of 9, one tile each
-    assert rf.rf_mla_decode_num_splits(2, 128, 100, 576, 512, 3) == 2
-    assert rf.rf_mla_decode_num_splits(2, 128, 100, 576, 512, 9) == 4
+    # segments hold whole 64-row tiles: 300 rows = 5 tiles; a request of 3
+    # gives segments of 2 tiles and so 3 segments, of 4 also 3, of 9 five
+    assert rf.rf_mla_decode_num_splits(2, 128, 300, 576, 512, 3) == 3
+    assert rf.rf_mla_decode_num_splits(2, 128, 300, 576, 512, 4) == 3
+    assert rf.rf_mla_decode_num_splits(2, 128, 300, 576, 512, 9) == 5
+    assert rf.rf_mla_decode_num_splits(2, 128, 100, 576, 512, 9) == 2
     assert rf.rf_mla_decode_num_splits(2, 128, 100, 576, 512, 1) == 1
     assert rf.rf_mla_decode_workspace_size(2, 128, 100, 576, 512, 1) == 0
     n = 2 * 128 * 2

@@ -34,7 +34,8 @@ def _run(rf, q, ckv, scale, num_splits=0):
 @pytest.mark.parametrize("B,Hq,Lk,splits", [
     (2, 128, 100, 1), (2, 128, 100, 2), (2, 128, 100, 4), (1, 128, 1, 0), (1, 128, 31, 1),
     (1, 128, 32, 1), (1, 128, 33, 2), (3, 16, 257, 0), (2, 1, 64, 1), (1, 100, 1000, 3),
-    (1, 128, 2048, 0), (2, 128, 4096, 5), (4, 64, 700, 0)])
+    (1, 128, 2048, 0), (2, 128, 4096, 5), (4, 64, 700, 0), (1, 128, 63, 1), (1, 128, 65, 2),
+    (2, 128, 129, 3), (1, 128, 192, 3)])
 def test_mla_small(rf, B, Hq, Lk, splits):
     sh = I.MLAShape(B, Hq, Lk, seed=2000 + Lk + splits)
     q, c = I.mla_inputs(sh)
