@@ -23,20 +23,24 @@
 // is the latent part of what it loaded, so P . V needs no further exchange.
 //
 // Per CTA: its Q dims sit in tensor memory (written once by the softmax
-// warps) as the A operand of the score products; the cache rows stream by TMA
-// through a 3-stage ring (64 rows x 64 dims per block, 128-byte swizzle), with
-// the tiles beyond the ring prefetched into L2; S has one buffer in tensor
-// memory, P (bf16) two in shared memory, O accumulates in tensor memory.  The
-// MMA warp issues whichever product is ready (S_t once the softmax warps have
-// taken S_{t-1} and the tile has landed; P_j V_j once P_j is written).  The
-// softmax warps, at tile j, add the peer's partial S_j to their own, then at
-// once take their own S_{j+1} out of tensor memory (freeing it for S_{j+2}) and
-// ship it to the peer, so the exchange of tile j+1 runs under the softmax of
-// tile j.  Two exchange slots per CTA suffice, each serving in turn as the
-// landing place of a peer tile and the staging place of an own tile: the peer
-// reads our S_{j-1} before it ships its S_j, so its S_j landing here frees the
-// peer slot our S_{j+1} goes to; and the peer ships S_{j+2} into the slot our
-// S_{j+1} was staged in only after that copy has landed.
+// warps) as the A operand of the score products, and so does P (bf16) for the
+// P . V products; the cache rows stream by TMA through a 4-stage ring (64 rows
+// x 64 dims per block, 128-byte swizzle), with the tiles beyond the ring
+// prefetched into L2; S has one buffer in tensor memory, O accumulates there.
+// The MMA warp issues whichever product is ready (S_t once the softmax warps
+// have taken S_{t-1} and the tile has landed; P_j V_j once P_j is written).
+//
+// Exchange, one tile ahead: at tile j the softmax warps add the peer's
+// partial S_j to their own, then at once take their own S_{j+1} out of tensor
+// memory (freeing it for S_{j+2}) and ship it, so its copy runs under the
+// softmax of tile j.  Each CTA has two 32 KB slots, each in turn the landing
+// place of a peer tile and the staging place of an own tile: S_{j+1} is
+// staged in slot j % 2, whose peer tile S_j each thread has just read (its own
+// row), and each warp bulk-copies its 32 rows to the peer's slot (j + 1) % 2.
+// Ordering needs no extra messages: the peer's S_j landing here shows that
+// the peer has read our S_{j-1} from its slot (j + 1) % 2; the peer ships its
+// S_{j+2} into the slot our S_{j+1} was staged in only after our S_{j+1} has
+// landed there, i.e. after the copy has read it.
 //
 // Lazy rescaling: a row's reference maximum m moves only when a tile's
 // maximum exceeds it by more than 8 (log2 units); only then are O (in tensor
@@ -44,7 +48,7 @@
 // dependent factor makes the result independent of the reference chosen ([S]
 // Methodologie 1), and P <= 2^8 keeps bf16 P and fp32 sums far from overflow.
 //
-// Tensor memory (512 columns): O 0-255, S 256-319, Q 352-511.
+// Tensor memory (512 columns): O 0-255, S 256-319, P 320-351, Q 352-511.
 #include <math.h>
 
 #include "rf_device.cuh"
@@ -57,20 +61,19 @@ constexpr int kDqk = 576, kDv = 512;
 constexpr int BH = 128;                            // head rows (MMA M)
 constexpr int BN = 64;                             // cache rows per tile
 constexpr int kMaxBlk = 5;                         // 64-dim blocks per CTA
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kPrefetch = 4;                       // tiles beyond the ring prefetched into L2
 constexpr int kChBytes = BN * 128;                 // one 64-dim block of a tile: 8 KB
 constexpr int kStageBytes = kMaxBlk * kChBytes;    // 40 KB
-constexpr int kPBytes = BH * 128;                  // P of one tile: 16 KB
 constexpr int kXBytes = BH * BN * 4;               // one partial score tile: 32 KB
+constexpr int kNX = 2;                             // exchange slots
 constexpr int kStOff = 0;
-constexpr int kPOff = kStOff + kStages * kStageBytes;   // 120 KB
-constexpr int kXOff = kPOff + 2 * kPBytes;              // 152 KB
-constexpr int kBarOff = kXOff + 2 * kXBytes;            // 216 KB
+constexpr int kXOff = kStOff + kStages * kStageBytes;   // 160 KB
+constexpr int kBarOff = kXOff + kNX * kXBytes;          // 224 KB
 constexpr int kSmem = kBarOff + 512;
 constexpr int kThreads = 192;                      // warp 0 TMA, 1 MMA, 2-5 softmax
 constexpr int kTmemCols = 512;
-constexpr int kTmemS = 256, kTmemQ = 352;
+constexpr int kTmemS = 256, kTmemP = 320, kTmemQ = 352;
 constexpr float kLazy = 8.f;
 constexpr uint32_t kIdescS = make_idesc(BH, BN, /*bf16*/ 1, 0, 0);
 constexpr uint32_t kIdescO = make_idesc(BH, 64, /*bf16*/ 1, 0, /*V MN-major*/ 1);
@@ -87,9 +90,9 @@ struct Bars {
   uint64_t full[kStages], empty[kStages];
   uint64_t s_full;                  // own partial S_t in tensor memory
   uint64_t s_free;                  // S_t taken by the softmax warps
-  uint64_t p_full[2];               // P_j in P buffer j % 2
-  uint64_t pv_done[2];              // P_j V_j accumulated into O
-  uint64_t x_full[2];               // the peer's partial S_t in slot t % 2 (st.async bytes)
+  uint64_t p_full;                  // P_j in tensor memory
+  uint64_t pv_done;                 // P_j V_j accumulated into O (P_j read)
+  uint64_t x_full[kNX];             // the peer's partial S_t in slot t % 2
   uint64_t drain;
   uint32_t tmem;
   int abort;
@@ -135,16 +138,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(smem_u32(&bars->s_full), 1);
     mbar_init(smem_u32(&bars->s_free), BH);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&bars->p_full[i]), BH);
-      mbar_init(smem_u32(&bars->pv_done[i]), 1);
-      mbar_init(smem_u32(&bars->x_full[i]), 1);
-    }
+    mbar_init(smem_u32(&bars->p_full), BH);
+    mbar_init(smem_u32(&bars->pv_done), 1);
+    for (int i = 0; i < kNX; ++i) mbar_init(smem_u32(&bars->x_full[i]), 1);
     mbar_init(smem_u32(&bars->drain), 1);
     bars->abort = 0;
     fence_mbar_init();
     // armed for the peer's first two partial tiles; re-armed as slots are read
-    for (int i = 0; i < 2 && i < nt; ++i)
+    for (int i = 0; i < kNX && i < nt; ++i)
       mbar_arrive_expect_tx(smem_u32(&bars->x_full[i]), kXBytes);
   }
   if (warp == 1) {
@@ -193,28 +194,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && nt > 0) {
       // ------------------------------------------------ MMA issuer (event loop)
-      const uint32_t p_addr = smem_u32(smem + kPOff);
       bool ok = mbar_wait(smem_u32(&bars->q_full), 0);
       if (ok) tc_fence_after();
       int ns = 0, npv = 0;                             // next S / next P.V to issue
       uint64_t t_prog = globaltimer_ns();
       uint32_t idle = 0;
       while (ok && npv < nt) {
-        if (npv < ns && mbar_test_wait(smem_u32(&bars->p_full[npv & 1]), (uint32_t)((npv >> 1) & 1))) {
-          // O[:, 64 blk ..] (+)= P_j V_j,blk
+        if (npv < ns && mbar_test_wait(smem_u32(&bars->p_full), (uint32_t)(npv & 1))) {
+          // O[:, 64 blk ..] (+)= P_j V_j,blk, P_j from tensor memory
           tc_fence_after();
           const int st = npv % kStages;
           const uint32_t sb = smem_u32(smem + kStOff + st * kStageBytes);
-          const uint32_t pj = p_addr + (npv & 1) * kPBytes;
 #pragma unroll
           for (int blk = 0; blk < 4; ++blk) {
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk)
-              mma_bf16_ss(tm + 64 * blk, sw128_desc(pj + kk * 32, 1024, 16),
+              mma_bf16_ts(tm + 64 * blk, tm + kTmemP + kk * 8,
                           sw128_desc(sb + blk * kChBytes + kk * 16 * 128, 1024, kChBytes), kIdescO,
                           (npv | kk) != 0);
           }
-          mma_commit(smem_u32(&bars->pv_done[npv & 1]));
+          mma_commit(smem_u32(&bars->pv_done));
           mma_commit(smem_u32(&bars->empty[st]));
           ++npv;
           t_prog = globaltimer_ns();
@@ -277,14 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(smem_u32(&bars->q_full));
     }
 
-    // own partial S_t out of tensor memory (which may then take S_{t+1}) and
-    // into the peer's exchange slot t % 2.  The rows are staged in this CTA's
-    // slot (t + 1) % 2 -- the one whose peer tile S_{t-1} each thread has just
-    // read (its own row) -- and each warp bulk-copies its 32 rows (8 KB): a
-    // copy engine moves them several times faster than per-thread remote
-    // stores.  The peer writes its S_{t+1} into that slot only after our S_t
-    // has landed there, i.e. after the copy has read it.
-    auto take_and_send = [&](int t, float (&own)[BN]) -> bool {
+    // own partial S_t out of tensor memory, which may then take S_{t+1}
+    auto take = [&](int t, float (&own)[BN]) -> bool {
       if (!__all_sync(0xffffffffu,
                       mbar_wait(smem_u32(&bars->s_full), (uint32_t)(t & 1)) && !*abort_flag))
         return false;
@@ -299,58 +292,64 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&bars->s_free));
-      uint8_t* stage = smem + kXOff + ((t + 1) & 1) * kXBytes;
+      return true;
+    };
+    // S_t staged in this CTA's slot (t + 1) % 2, then each warp bulk-copies
+    // its 32 rows (8 KB) to the peer's slot t % 2 once the peer's S_{t-1} has
+    // landed here (t >= 1; observed already by the caller)
+    auto ship = [&](int t, const float (&own)[BN]) -> bool {
+      uint8_t* stage = smem + kXOff + ((t + 1) % kNX) * kXBytes;
 #pragma unroll
       for (int c = 0; c < BN / 4; ++c)
         *reinterpret_cast<uint4*>(stage + r * (BN * 4) + ((c ^ swz) << 4)) =
             make_uint4(__float_as_uint(own[4 * c]), __float_as_uint(own[4 * c + 1]),
                        __float_as_uint(own[4 * c + 2]), __float_as_uint(own[4 * c + 3]));
       fence_proxy_async_smem();                      // rows visible to the copy engine
+      if (t >= 1 && !__all_sync(0xffffffffu,
+                                mbar_wait_cluster(smem_u32(&bars->x_full[(t - 1) % kNX]),
+                                                  (uint32_t)(((t - 1) / kNX) & 1)) &&
+                                    !*abort_flag))
+        return false;
       __syncwarp();
       if (lane == 0) {
         const uint32_t blk = (uint32_t)(sub * 32 * BN * 4);   // this warp's 32 rows
-        bulk_copy_to_peer(x_peer + (t & 1) * kXBytes + blk, smem_u32(stage) + blk, 32 * BN * 4,
-                          mapa_shared(smem_u32(&bars->x_full[t & 1]), (uint32_t)peer));
+        bulk_copy_to_peer(x_peer + (t % kNX) * kXBytes + blk, smem_u32(stage) + blk, 32 * BN * 4,
+                          mapa_shared(smem_u32(&bars->x_full[t % kNX]), (uint32_t)peer));
       }
       return true;
     };
 
     float m_run = -INFINITY, l_run = 0.f;
     const uint64_t c2 = f2(c_log2, c_log2);
-    float own[BN];
-    bool ok = take_and_send(0, own);
-    for (int j = 0; ok && j < nt; ++j) {
+    float own_a[BN], own_b[BN];                       // own partial S_j and S_{j+1}, in turn
+    bool ok = take(0, own_a) && ship(0, own_a);
+    // tile j with cur = own S_j and nxt = own S_{j+1} (taken here)
+    auto step = [&](int j, float (&cur)[BN], float (&nxt)[BN]) -> bool {
       // (a) s = own + the peer's partial scores of tile j
-      if (!__all_sync(0xffffffffu,
-                      mbar_wait_cluster(smem_u32(&bars->x_full[j & 1]), (uint32_t)((j >> 1) & 1)) &&
-                          !*abort_flag)) {
-        ok = false;
-        break;
-      }
+      if (!__all_sync(0xffffffffu, mbar_wait_cluster(smem_u32(&bars->x_full[j % kNX]),
+                                                     (uint32_t)((j / kNX) & 1)) &&
+                                       !*abort_flag))
+        return false;
       // armed for the peer's S_{j+2}, which it ships only after our S_{j+1}
       // has reached it (the phase of S_j here is complete by then)
-      if (sub == 0 && lane == 0 && j + 2 < nt)
-        mbar_arrive_expect_tx(smem_u32(&bars->x_full[j & 1]), kXBytes);
-      float sc[BN];
+      if (sub == 0 && lane == 0 && j + kNX < nt)
+        mbar_arrive_expect_tx(smem_u32(&bars->x_full[j % kNX]), kXBytes);
+      float (&sc)[BN] = cur;
       {
-        const uint8_t* src = smem + kXOff + (j & 1) * kXBytes + r * (BN * 4);
+        const uint8_t* src = smem + kXOff + (j % kNX) * kXBytes + r * (BN * 4);
 #pragma unroll
         for (int c = 0; c < BN / 4; ++c) {
           const uint4 w = *reinterpret_cast<const uint4*>(src + ((c ^ swz) << 4));
-          sc[4 * c] = own[4 * c] + __uint_as_float(w.x);
-          sc[4 * c + 1] = own[4 * c + 1] + __uint_as_float(w.y);
-          sc[4 * c + 2] = own[4 * c + 2] + __uint_as_float(w.z);
-          sc[4 * c + 3] = own[4 * c + 3] + __uint_as_float(w.w);
+          sc[4 * c] += __uint_as_float(w.x);
+          sc[4 * c + 1] += __uint_as_float(w.y);
+          sc[4 * c + 2] += __uint_as_float(w.z);
+          sc[4 * c + 3] += __uint_as_float(w.w);
         }
       }
-      // (b) the next tile's own partial goes to the peer now, under this
-      // tile's softmax (the peer's S_j landing here freed slot (j + 1) % 2)
-      if (j + 1 < nt && !take_and_send(j + 1, own)) {
-        ok = false;
-        break;
-      }
+      // own S_{j+1} out and to the peer, under this tile's softmax
+      if (j + 1 < nt && !(take(j + 1, nxt) && ship(j + 1, nxt))) return false;
 
-      // (c) online softmax with a lazily moved reference maximum
+      // (b) online softmax with a lazily moved reference maximum
       const int valid = min(BN, hi - (lo + j * BN));   // rows of this tile in the segment
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (valid == BN) {
@@ -392,22 +391,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       f2_split(fadd2(fadd2(sum4[0], sum4[1]), fadd2(sum4[2], sum4[3])), s_lo, s_hi);
       l_run += s_lo + s_hi;
 
-      // P buffer j % 2 is free once P_{j-2} V_{j-2} is done
-      if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->pv_done[j & 1]),
-                                                       (uint32_t)(((j - 2) >> 1) & 1)) &&
-                                                 !*abort_flag)) {
-        ok = false;
-        break;
-      }
+      // P_{j-1} V_{j-1} done: its P columns are free, and O may be rescaled
+      if (j >= 1 && !__all_sync(0xffffffffu,
+                                mbar_wait(smem_u32(&bars->pv_done), (uint32_t)((j - 1) & 1)) &&
+                                    !*abort_flag))
+        return false;
+      tc_fence_after();
       if (__any_sync(0xffffffffu, need)) {
-        // O *= alpha after P_{j-1} V_{j-1} has landed and before P_j V_j is issued
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->pv_done[(j - 1) & 1]),
-                                               (uint32_t)(((j - 1) >> 1) & 1)) &&
-                                         !*abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
 #pragma unroll 1
         for (int blk = 0; blk < 8; ++blk) {
           uint32_t v[32];
@@ -417,26 +407,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
           tmem_st32(tm + lane_off + 32 * blk, v);
         }
-        tmem_st_wait();
       }
-      // keys 8c .. 8c+7 of this tile = 16-byte chunk c of row r (128-byte swizzle)
-      uint8_t* prow = smem + kPOff + (j & 1) * kPBytes + r * 128;
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(prow + ((c ^ swz) << 4)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      fence_proxy_async_smem();                        // P visible to the tensor core
+      tmem_st32(tm + lane_off + kTmemP, pk);            // keys 2c, 2c+1 in column c
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(smem_u32(&bars->p_full[j & 1]));
-    }
+      mbar_arrive(smem_u32(&bars->p_full));
+
+      return true;
+    };
+    for (int j = 0; ok && j < nt; ++j) ok = (j & 1) ? step(j, own_b, own_a) : step(j, own_a, own_b);
 
     // epilogue: O of this CTA's 256 dims, normalised (one segment) or as a
     // partial state (o unnormalised, m in log2 units, l) for the merge
     if (ok) {
       const int jl = nt - 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->pv_done[jl & 1]),
-                                             (uint32_t)((jl >> 1) & 1)) &&
-                                       !*abort_flag)) {
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(smem_u32(&bars->pv_done), (uint32_t)(jl & 1)) && !*abort_flag)) {
         ok = false;
       } else {
         tc_fence_after();

@@ -375,7 +375,7 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 }
 
 // mbar_wait for a barrier completed from another CTA (bytes of a bulk copy
-// to this CTA): acquires at cluster scope.  Bounded like mbar_wait.
+// into this CTA): acquires at cluster scope.  Bounded like mbar_wait.
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
                                                   uint64_t limit_ns = kDefaultWaitNs) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
