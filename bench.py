@@ -463,12 +463,7 @@ def run_ours(args, world, rank, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; shapes of the five named workloads)",
-        "config": {"workload": workload_name(ops),
-                   "decode": "B32 Hq32 Hkv8 d128 Lk {32768, 2048} bf16",
-                   "prefill": "B8 H16 L512 d64 bf16", "moe": "T8192 D4096 E64 top2 bf16",
-                   "fp8": "M=N=K=4096 e4m3 (bf16 X in, bf16 Y out)",
-                   "l2": "no flush: step streams >= 4.6 GB (> 129 MB L2) between reuses",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(ops, world),
         "peaks": {k: peaks[k] for k in ("hbm_gbs", "bf16_tfs", "bf16_tfs_sustained", "source")},
         "rows": rows,
         "roofline": roofline,
@@ -506,6 +501,31 @@ def workload_name(ops):
     if [op.name for op in ops] == [op.name for op in make_ops()]:
         return "decode32k+bert_prefill+moe_gate+fp8_gemm+decode2k"
     return "+".join(op.name for op in ops)
+
+
+def workload_config(ops, world):
+    """The shapes of the calls a run times (the whole step, or the --only
+    calls) and how L2 reuse between steps is avoided."""
+    names = {op.name for op in ops}
+    cfg = {"workload": workload_name(ops)}
+    if names & {"decode_32k", "decode_2k"}:
+        cfg["decode"] = "B32 Hq32 Hkv8 d128 Lk {32768, 2048} bf16"
+    if names & {"bert_prefill", "bert_prefill_causal"}:
+        cfg["prefill"] = "B8 H16 L512 d64 bf16"
+    if "moe_gate" in names:
+        cfg["moe"] = "T8192 D4096 E64 top2 bf16"
+    if "fp8_gemm" in names:
+        cfg["fp8"] = "M=N=K=4096 e4m3 (bf16 X in, bf16 Y out)"
+    if "mla_decode" in names:
+        s = I.MLA_DECODE
+        cfg["mla"] = (f"B{s.B} Hq{s.Hq} Lk{s.Lk} d_qk{s.d_qk} d_v{s.d_v} bf16, one latent head, "
+                      f"scale 1/sqrt(192)")
+    total = sum(op.bytes for op in ops)
+    cfg["l2"] = (f"no flush: inputs of {total / 1e6:.0f} MB per step streamed "
+                 + ("(> 129 MB L2) between reuses" if total > 129e6 else
+                    "(under the 129 MB L2: later steps may hit L2)"))
+    cfg["parallelism"] = f"replicas x{world}"
+    return cfg
 
 
 def run_e2e(rf, ops, peaks, host, step, world, args):
