@@ -76,7 +76,9 @@ constexpr int kTmemCols = 512;
 constexpr int kTmemS = 256, kTmemP = 320, kTmemQ = 352;
 constexpr float kLazy = 8.f;
 constexpr uint32_t kIdescS = make_idesc(BH, BN, /*bf16*/ 1, 0, 0);
-constexpr uint32_t kIdescO = make_idesc(BH, 64, /*bf16*/ 1, 0, /*V MN-major*/ 1);
+// P . V: N = 256 value dims in one product; the four 64-dim blocks of a stage
+// are 8 KB apart, the stride between 64-element blocks of an MN-major operand
+constexpr uint32_t kIdescO = make_idesc(BH, 256, /*bf16*/ 1, 0, /*V MN-major*/ 1);
 constexpr int kMergeThreads = 128;                 // 4 dims per thread
 
 __device__ __forceinline__ float ex2(float x) {
@@ -201,18 +203,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t idle = 0;
       while (ok && npv < nt) {
         if (npv < ns && mbar_test_wait(smem_u32(&bars->p_full), (uint32_t)(npv & 1))) {
-          // O[:, 64 blk ..] (+)= P_j V_j,blk, P_j from tensor memory
+          // O (+)= P_j V_j over all 256 value dims, P_j from tensor memory
           tc_fence_after();
           const int st = npv % kStages;
           const uint32_t sb = smem_u32(smem + kStOff + st * kStageBytes);
 #pragma unroll
-          for (int blk = 0; blk < 4; ++blk) {
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-              mma_bf16_ts(tm + 64 * blk, tm + kTmemP + kk * 8,
-                          sw128_desc(sb + blk * kChBytes + kk * 16 * 128, 1024, kChBytes), kIdescO,
-                          (npv | kk) != 0);
-          }
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_bf16_ts(tm, tm + kTmemP + kk * 8, sw128_desc(sb + kk * 16 * 128, 1024, kChBytes),
+                        kIdescO, (npv | kk) != 0);
           mma_commit(smem_u32(&bars->pv_done));
           mma_commit(smem_u32(&bars->empty[st]));
           ++npv;
@@ -255,19 +253,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool row_ok = r < Hq;
     const int64_t bh = (int64_t)b * Hq + r;
 
-    // Q row r (this CTA's blocks) into tensor memory; rows past Hq are zero
+    // Q row r (this CTA's blocks) into tensor memory; rows past Hq are zero.
+    // All loads are issued before the first store, so that the row's blocks
+    // are fetched together rather than one round trip per block.
     {
       const uint4* qrow = reinterpret_cast<const uint4*>(Q + (row_ok ? bh : 0) * kDqk);
-      for (int c = 0; c < nblk; ++c) {
+      uint4 w[kMaxBlk][8];
+#pragma unroll
+      for (int c = 0; c < kMaxBlk; ++c) {
         const int db = dim_block(rank, c);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          w[c][i] = row_ok && c < nblk ? qrow[db * 8 + i] : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int c = 0; c < kMaxBlk; ++c) {
+        if (c >= nblk) break;                          // uniform over the CTA
         uint32_t v[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const uint4 w = row_ok ? qrow[db * 8 + i] : make_uint4(0u, 0u, 0u, 0u);
-          v[4 * i] = w.x;
-          v[4 * i + 1] = w.y;
-          v[4 * i + 2] = w.z;
-          v[4 * i + 3] = w.w;
+          v[4 * i] = w[c][i].x;
+          v[4 * i + 1] = w[c][i].y;
+          v[4 * i + 2] = w[c][i].z;
+          v[4 * i + 3] = w[c][i].w;
         }
         tmem_st32(tm + lane_off + kTmemQ + c * 32, v);
       }

@@ -1,7 +1,8 @@
 """Every entry point only enqueues work on the caller's stream, so a call can
 be captured into a CUDA graph and replayed: the replay must reproduce the
 eager call's bits.  (The programmatic dependent launches of the split-KV
-merge and of the FP8 GEMM become graph edges.)"""
+merge, of the FP8 GEMM and of the latent-KV merge, and the cluster launches,
+become graph nodes and edges.)"""
 import pytest
 import torch
 
@@ -64,6 +65,18 @@ def _paths(rf):
                       device="cuda")
     y = torch.empty(fs.M, fs.N, dtype=torch.bfloat16, device="cuda")
     paths.append(("fp8", [y], lambda: rf.rf_absmax_fp8_gemm(X, Wq, sw, y, workspace=wsf)))
+
+    ml = I.MLAShape(B=2, Hq=128, Lk=700, seed=87)
+    qm, cm = (t.cuda() for t in I.mla_inputs(ml))
+    om1 = torch.empty(ml.B, ml.Hq, ml.d_v, dtype=torch.bfloat16, device="cuda")
+    om3 = torch.empty_like(om1)
+    wsm = torch.empty(rf.rf_mla_decode_workspace_size(ml.B, ml.Hq, ml.Lk, 576, 512, 3),
+                      dtype=torch.uint8, device="cuda")
+
+    def mla():
+        rf.rf_mla_decode(qm, cm, om1, ml.scale, None, 1)       # one segment (cluster kernel)
+        rf.rf_mla_decode(qm, cm, om3, ml.scale, wsm, 3)        # three segments + merge
+    paths.append(("mla", [om1, om3], mla))
     return paths
 
 
