@@ -291,6 +291,7 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
+
 // Whole-cluster barrier (every thread of every CTA of the cluster).
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
@@ -403,7 +404,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
-
 
 // Packed fp32 pairs (Blackwell f32x2 instructions): lo in bits 0-31.
 __device__ __forceinline__ uint64_t f2(float lo, float hi) {
