@@ -480,15 +480,16 @@ __global__ void __launch_bounds__(kThreads, 2)
           return false;
         tc_fence_after();
         const uint64_t a2 = f2(alpha, alpha);
+        uint32_t v[2][32];                               // both halves in flight together
+        tmem_ld32(tmem_s + (t & 1) * BKV + lane_off, v[0]);
+        tmem_ld32(tmem_s + (t & 1) * BKV + lane_off + 32, v[1]);
+        tmem_ld_wait();
   #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          uint32_t v[32];
-          tmem_ld32(tmem_s + (t & 1) * BKV + lane_off + h * 32, v);
-          tmem_ld_wait();
   #pragma unroll
           for (int i = 0; i < 16; ++i)
-            o2[h * 16 + i] =
-                ffma2(o2[h * 16 + i], a2, f2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])));
+            o2[h * 16 + i] = ffma2(o2[h * 16 + i], a2,
+                                   f2(__uint_as_float(v[h][2 * i]), __uint_as_float(v[h][2 * i + 1])));
         }
         return true;
       };
@@ -514,18 +515,24 @@ __global__ void __launch_bounds__(kThreads, 2)
         // pass 1: row max of the raw scores (four independent max chains)
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
   #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t v[32];
-          tmem_ld32(sbuf + q * 32, v);
+        for (int qq = 0; qq < 2; ++qq) {
+          uint32_t v[2][32];                             // two 32-key blocks in flight together
+          tmem_ld32(sbuf + (2 * qq) * 32, v[0]);
+          tmem_ld32(sbuf + (2 * qq + 1) * 32, v[1]);
           tmem_ld_wait();
-          if (full) {
   #pragma unroll
-            for (int i = 0; i < 32; i += 2)
-              mx4[(i >> 1) & 3] = fmax3(mx4[(i >> 1) & 3], __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
-          } else {
+          for (int h = 0; h < 2; ++h) {
+            const int q = 2 * qq + h;
+            if (full) {
   #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (q * 32 + i < valid) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(v[i]));
+              for (int i = 0; i < 32; i += 2)
+                mx4[(i >> 1) & 3] =
+                    fmax3(mx4[(i >> 1) & 3], __uint_as_float(v[h][i]), __uint_as_float(v[h][i + 1]));
+            } else {
+  #pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (q * 32 + i < valid) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(v[h][i]));
+            }
           }
         }
         const float mx = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]);
