@@ -235,14 +235,14 @@ size_t rf_mla_decode_workspace_size(int B, int Hq, int Lk, int d_qk, int d_v, in
  *   s_j = scale * Q[b,h,:] . CKV[b,j,:]   (all d_qk dims)
  *   O[b,h,:] = sum_j softmax(s)_j CKV[b,j,0:d_v]
  * computed as the safe-softmax cascade in one incremental loop over tiles
- * of 32 cache rows ([E] §2.3, §4.1), on a cluster of two CTAs per (batch,
+ * of 64 cache rows ([E] §2.3, §4.1), on a cluster of two CTAs per (batch,
  * segment) that exchange partial scores; with more than one segment, the
  * partial states (m, l, o) of the segments are merged by a second kernel
  * ([S] Methodologie 3).
  *   Sizes   B, Lk >= 1; 1 <= Hq <= 128; d_qk = 576 and d_v = 512 (else
  *           RF_ERR_UNSUPPORTED); scale finite, > 0.
  *   num_splits  0 = automatic, else the requested number of segments
- *           (clamped to whole 32-row tiles: rf_mla_decode_num_splits tells
+ *           (clamped to whole 64-row tiles: rf_mla_decode_num_splits tells
  *           the count used).
  *   workspace   device buffer of at least rf_mla_decode_workspace_size(...)
  *           bytes, 16-byte aligned, owned by the caller; may be NULL when
