@@ -18,7 +18,12 @@ by the measured step time, in percent.  Peaks come from MEASURED_PEAKS.json
 when present, else the fallback figures (6.8 TB/s, 1.9 PFLOP/s bf16; FP8 =
 2x bf16).  One JSON line is printed by rank 0.
 
+--only times a subset of the step, or calls outside it (the causal and
+variable-length prefill, short prefill in both evaluation orders, other
+expert counts of the gate, the latent-KV decode), with the same metric.
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--only CALL,...]
 """
 from __future__ import annotations
 
