@@ -37,7 +37,10 @@
 // place of a peer tile and the staging place of an own tile: S_{j+1} is
 // staged in slot j % 2, whose peer tile S_j each thread has just read (its own
 // row), and each warp bulk-copies its 32 rows to the peer's slot (j + 1) % 2.
-// Ordering needs no extra messages: the peer's S_j landing here shows that
+// Each row is read and written by the warp of the same number on both sides,
+// so the slots are tracked per warp (one barrier per slot and warp, 8 KB):
+// a warp waits only for its own rows.  Ordering needs no extra messages: the
+// peer's S_j landing here shows that
 // the peer has read our S_{j-1} from its slot (j + 1) % 2; the peer ships its
 // S_{j+2} into the slot our S_{j+1} was staged in only after our S_{j+1} has
 // landed there, i.e. after the copy has read it.
@@ -94,7 +97,7 @@ struct Bars {
   uint64_t s_free;                  // S_t taken by the softmax warps
   uint64_t p_full;                  // P_j in tensor memory
   uint64_t pv_done;                 // P_j V_j accumulated into O (P_j read)
-  uint64_t x_full[kNX];             // the peer's partial S_t in slot t % 2
+  uint64_t x_full[kNX][4];          // rows 32 w .. of the peer's partial S_t in slot t % 2
   uint64_t drain;
   uint32_t tmem;
   int abort;
@@ -142,13 +145,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&bars->s_free), BH);
     mbar_init(smem_u32(&bars->p_full), BH);
     mbar_init(smem_u32(&bars->pv_done), 1);
-    for (int i = 0; i < kNX; ++i) mbar_init(smem_u32(&bars->x_full[i]), 1);
+    for (int i = 0; i < kNX; ++i)
+      for (int w = 0; w < 4; ++w) mbar_init(smem_u32(&bars->x_full[i][w]), 1);
     mbar_init(smem_u32(&bars->drain), 1);
     bars->abort = 0;
     fence_mbar_init();
     // armed for the peer's first two partial tiles; re-armed as slots are read
     for (int i = 0; i < kNX && i < nt; ++i)
-      mbar_arrive_expect_tx(smem_u32(&bars->x_full[i]), kXBytes);
+      for (int w = 0; w < 4; ++w) mbar_arrive_expect_tx(smem_u32(&bars->x_full[i][w]), kXBytes / 4);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&bars->tmem), kTmemCols);
@@ -314,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        __float_as_uint(own[4 * c + 2]), __float_as_uint(own[4 * c + 3]));
       fence_proxy_async_smem();                      // rows visible to the copy engine
       if (t >= 1 && !__all_sync(0xffffffffu,
-                                mbar_wait_cluster(smem_u32(&bars->x_full[(t - 1) % kNX]),
+                                mbar_wait_cluster(smem_u32(&bars->x_full[(t - 1) % kNX][sub]),
                                                   (uint32_t)(((t - 1) / kNX) & 1)) &&
                                     !*abort_flag))
         return false;
@@ -322,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         const uint32_t blk = (uint32_t)(sub * 32 * BN * 4);   // this warp's 32 rows
         bulk_copy_to_peer(x_peer + (t % kNX) * kXBytes + blk, smem_u32(stage) + blk, 32 * BN * 4,
-                          mapa_shared(smem_u32(&bars->x_full[t % kNX]), (uint32_t)peer));
+                          mapa_shared(smem_u32(&bars->x_full[t % kNX][sub]), (uint32_t)peer));
       }
       return true;
     };
@@ -334,14 +338,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tile j with cur = own S_j and nxt = own S_{j+1} (taken here)
     auto step = [&](int j, float (&cur)[BN], float (&nxt)[BN]) -> bool {
       // (a) s = own + the peer's partial scores of tile j
-      if (!__all_sync(0xffffffffu, mbar_wait_cluster(smem_u32(&bars->x_full[j % kNX]),
+      if (!__all_sync(0xffffffffu, mbar_wait_cluster(smem_u32(&bars->x_full[j % kNX][sub]),
                                                      (uint32_t)((j / kNX) & 1)) &&
                                        !*abort_flag))
         return false;
-      // armed for the peer's S_{j+2}, which it ships only after our S_{j+1}
-      // has reached it (the phase of S_j here is complete by then)
-      if (sub == 0 && lane == 0 && j + kNX < nt)
-        mbar_arrive_expect_tx(smem_u32(&bars->x_full[j % kNX]), kXBytes);
+      // armed for the peer's S_{j+2}, which its warp ships only after our
+      // warp's S_{j+1} rows have reached it (this phase is complete by then)
+      if (lane == 0 && j + kNX < nt)
+        mbar_arrive_expect_tx(smem_u32(&bars->x_full[j % kNX][sub]), kXBytes / 4);
       float (&sc)[BN] = cur;
       {
         const uint8_t* src = smem + kXOff + (j % kNX) * kXBytes + r * (BN * 4);
