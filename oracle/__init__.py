@@ -24,7 +24,7 @@ method's sources define the cascade.  Sources cited in this package:
     E4M3 format (bias 7, no infinities, max normal 448, NaN = S.1111.111).
 
 Modules: ``attention`` (safe-softmax cascade, its incremental and
-multi-segment forms), ``moe_gate`` (gate scores, top-k, softmax of the
+multi-segment forms, the latent-KV decode), ``moe_gate`` (gate scores, top-k, softmax of the
 selected scores), ``fp8_quant_gemm`` (row absmax, E4M3 quantisation, GEMM,
 dequantisation).  Every function is pinned by tests under ``tests/`` against
 closed forms, library routines, brute force or worked examples; none is
