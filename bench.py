@@ -16,7 +16,12 @@ Metric: the step's roofline time (sum over the kernels of
 max(algorithmic bytes / HBM peak, algorithmic FLOPs / tensor peak)) divided
 by the measured step time, in percent.  Peaks come from MEASURED_PEAKS.json
 when present, else the fallback figures (6.8 TB/s, 1.9 PFLOP/s bf16; FP8 =
-2x bf16).  One JSON line is printed by rank 0.
+2x bf16).  The tensor peak is the burst figure: every kernel is timed in a
+region far shorter than a second.  One JSON line is printed by rank 0.
+
+Before timing, the first call of every op is checked against the fp64 CPU
+oracle on the same seeded inputs (bit-exact indices, codes and scales; the
+stated tolerances for floats); the run exits non-zero if any check fails.
 
 --only times a subset of the step, or calls outside it (the causal and
 variable-length prefill, short prefill in both evaluation orders, other
@@ -44,7 +49,7 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from cascaded_reductions_loop_gb300 import inputs as I  # noqa: E402
+import workloads as I  # noqa: E402
 
 METRIC = "fused cascaded-reduction TFLOP/s or HBM GB/s, % of GB300 roofline (1 GPU)"
 UNIT = "% of roofline (step roofline time / measured step time)"
@@ -83,16 +88,19 @@ class Op:
         self.name, self.bytes, self.flops, self.tc_dtype = name, bytes_, flops, tc_dtype
         self.n_kernels = n_kernels
 
+    def tensor_peak(self, peaks):
+        """Dense tensor peak of this op's dtype (TFLOP/s): the measured bf16
+        burst figure, x2 for FP8 (the nominal ratio)."""
+        return peaks["bf16_tfs"] * (2.0 if self.tc_dtype == "fp8" else 1.0)
+
     def roofline_s(self, peaks):
         t_mem = self.bytes / (peaks["hbm_gbs"] * 1e9)
-        tc = peaks["bf16_tfs_sustained"] * (2.0 if self.tc_dtype == "fp8" else 1.0)
-        t_tc = self.flops / (tc * 1e12) if self.flops else 0.0
+        t_tc = self.flops / (self.tensor_peak(peaks) * 1e12) if self.flops else 0.0
         return max(t_mem, t_tc)
 
     def bound(self, peaks):
         t_mem = self.bytes / (peaks["hbm_gbs"] * 1e9)
-        tc = peaks["bf16_tfs_sustained"] * (2.0 if self.tc_dtype == "fp8" else 1.0)
-        t_tc = self.flops / (tc * 1e12) if self.flops else 0.0
+        t_tc = self.flops / (self.tensor_peak(peaks) * 1e12) if self.flops else 0.0
         return "hbm" if t_mem >= t_tc else "tensor"
 
 
@@ -112,7 +120,7 @@ def make_ops():
            "bf16", 1),
         Op("moe_gate", m.T * m.D * 2 + m.E * m.D * 2 + m.T * m.k * 8, 2 * m.T * m.D * m.E, "bf16", 1),
         Op("fp8_gemm", f.M * f.K * 2 + f.N * f.K + f.N * 4 + f.M * f.N * 2, 2 * f.M * f.N * f.K,
-           "fp8", 2),
+           "fp8", 1),
         decode_op("decode_2k", I.DECODE_2K),
     ]
 
@@ -141,23 +149,13 @@ def make_extra_ops():
 
 def mla_op():
     """Latent-KV decode: the cache is read once (B * Lk rows of d_qk bf16),
-    plus Q and O; FLOPs count the scores over d_qk dims and P.V over d_v."""
+    plus Q and O; FLOPs count the scores over d_qk dims and P.V over d_v.
+    Its kernel count (1, or 2 with a merge) is filled in by run_ours from the
+    library's choice of segments."""
     s = I.MLA_DECODE
     cache = s.B * s.Lk * s.d_qk * 2
     qo = s.B * s.Hq * (s.d_qk + s.d_v) * 2
-    return Op("mla_decode", cache + qo, 2 * s.B * s.Hq * s.Lk * (s.d_qk + s.d_v), "bf16",
-              1 + (mla_splits() > 1))
-
-
-def mla_splits():
-    """Segments per batch the library takes for the latent-KV workload (1
-    where the library cannot tell without a device)."""
-    try:
-        import cascaded_reductions_loop_gb300 as rf
-        s = I.MLA_DECODE
-        return max(1, rf.rf_mla_decode_num_splits(s.B, s.Hq, s.Lk, s.d_qk, s.d_v, 0))
-    except (ImportError, OSError):
-        return 1
+    return Op("mla_decode", cache + qo, 2 * s.B * s.Hq * s.Lk * (s.d_qk + s.d_v), "bf16", 1)
 
 
 def varlen_lengths():
@@ -232,6 +230,16 @@ class Step:
         self.y = torch.empty(sf.M, sf.N, dtype=torch.bfloat16, device=cuda)
         self.wsf = torch.empty(rf.rf_absmax_fp8_gemm_workspace_size(sf.M, sf.N, sf.K),
                                dtype=torch.uint8, device=cuda)
+        if "fp8_gemm" in d:
+            # the fused call takes W pre-quantised: made once here by the
+            # library's own per-row quantiser (not part of the timed step)
+            x_d, w_d = d["fp8_gemm"]
+            self.wq = torch.empty(sf.N, sf.K, dtype=torch.uint8, device=cuda)
+            self.sw = torch.empty(sf.N, dtype=torch.float32, device=cuda)
+            rf.rf_absmax_quant_fp8(w_d, self.sw, self.wq)
+            d["fp8_gemm"] = [x_d, self.wq, self.sw]
+            self.sx = torch.empty(sf.M, dtype=torch.float32, device=cuda)
+            self.xq = torch.empty(sf.M, sf.K, dtype=torch.uint8, device=cuda)
         self.calls = {
             "decode_32k": lambda: rf.rf_attn_decode_splitkv(*d["decode_32k"], self.o32, s32.scale,
                                                             self.ws32, args_splits(32768)),
@@ -240,7 +248,7 @@ class Step:
                                                           sb.scale, 1),
             "moe_gate": lambda: rf.rf_moe_gate_topk_softmax(*d["moe_gate"], sm.k, self.idx,
                                                             self.wts),
-            "fp8_gemm": lambda: rf.rf_absmax_fp8_gemm(*d["fp8_gemm"], self.y, workspace=self.wsf),
+            "fp8_gemm": lambda: rf.rf_absmax_fp8_gemm(*d["fp8_gemm"], self.y, self.wsf),
             "decode_2k": lambda: rf.rf_attn_decode_splitkv(*d["decode_2k"], self.o2, s2.scale,
                                                            self.ws2, args_splits(2048)),
         }
@@ -269,6 +277,12 @@ class Step:
             self.calls[name] = (lambda name=name, m=m, ix=ix, wt=wt:
                                 rf.rf_moe_gate_topk_softmax(*d[name], m.k, ix, wt))
             setattr(self, "out_" + name, [ix, wt])
+        # the un-timed first call of the FP8 op also writes its codes and row
+        # scales out, for the parity check; timed calls keep them in the workspace
+        self.parity_calls = {
+            "fp8_gemm": lambda: rf.rf_absmax_fp8_gemm(*d["fp8_gemm"], self.y, self.wsf,
+                                                      sx_out=self.sx, xq_out=self.xq),
+        }
         self.outputs = {"decode_32k": [self.o32], "decode_2k": [self.o2],
                         "bert_prefill": [self.ob], "bert_prefill_causal": [self.ob],
                         "moe_gate": [self.idx, self.wts],
@@ -282,6 +296,120 @@ class Step:
         for name in SHORT_EXTRA:
             if name in d:
                 self.outputs[name] = getattr(self, "out_" + name)
+
+
+# ------------------------------------------------------------------ parity
+
+# Tolerances of the parity check: the ones the GPU parity tests use.
+TOL_BF16_MAX_ABS = 2e-2        # attention outputs, elementwise
+TOL_BF16_REL_L2 = 5e-3
+TOL_FP8_Y_REL = 2e-2           # FP8 Y: |Y - Y_ref| <= 2e-2 * max(1, |Y_ref|)
+TOL_FP8_Y_REL_L2 = 5e-3
+TOL_MOE_W_ABS = 1e-6           # MoE weights (scores are exact integers)
+
+
+def oracle_fp8_weight(w):
+    """The pre-quantised FP8 weight as the oracle makes it (row_scale, then
+    quantise, per row of W [N][K])."""
+    from oracle import fp8_quant_gemm as F
+    _, sw = F.row_scale(w)
+    return F.quantise(w, sw), sw
+
+
+def oracle_view(host):
+    """The ops' inputs as the oracle takes them: the FP8 weight quantised by
+    the oracle's own quantiser."""
+    out = dict(host)
+    if "fp8_gemm" in host:
+        x, w = host["fp8_gemm"]
+        wq, sw = oracle_fp8_weight(w)
+        out["fp8_gemm"] = [x, wq, sw]
+    return out
+
+
+def _f64(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def _close(got, ref, max_abs, rel_l2, relative):
+    got, ref = _f64(got).reshape(ref.shape), np.asarray(ref, np.float64)
+    if not np.isfinite(got).all():
+        return f"FAIL: {int((~np.isfinite(got)).sum())} non-finite elements"
+    bound = max_abs * (np.maximum(1.0, np.abs(ref)) if relative else 1.0)
+    nbad = int((np.abs(got - ref) > bound).sum())
+    r = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
+    if nbad or r > rel_l2:
+        return f"FAIL: {nbad} elements outside tolerance, rel-L2 {r:.2e}"
+    return "ok"
+
+
+def check_op(name, outs, ov):
+    """Compares one op's outputs (host tensors) with the full fp64 oracle."""
+    from oracle import attention as A
+    from oracle import fp8_quant_gemm as F
+    from oracle import moe_gate as G
+
+    if name in ("decode_32k", "decode_2k"):
+        s = I.DECODE_32K if name == "decode_32k" else I.DECODE_2K
+        ref = A.decode_attention(*ov[name], s.scale)
+        return _close(outs[0], ref, TOL_BF16_MAX_ABS, TOL_BF16_REL_L2, False)
+    if name in ("bert_prefill", "bert_prefill_causal"):
+        s = I.BERT_PREFILL
+        ref = A.attention(*ov[name], s.scale, causal=name.endswith("causal"))
+        return _close(outs[0], ref, TOL_BF16_MAX_ABS, TOL_BF16_REL_L2, False)
+    if name in SHORT_EXTRA:
+        sh = SHORT_EXTRA[name][0]
+        ref = A.attention(*ov[name], sh.scale)
+        return _close(outs[0], ref, TOL_BF16_MAX_ABS, TOL_BF16_REL_L2, False)
+    if name == "prefill_varlen":
+        q, k, v, cu = ov[name]
+        ref = A.attention_varlen(q, k, v, cu, cu, I.PREFILL_VARLEN.scale)
+        return _close(outs[0], ref, TOL_BF16_MAX_ABS, TOL_BF16_REL_L2, False)
+    if name == "mla_decode":
+        s = I.MLA_DECODE
+        ref = A.mla_decode(*ov[name], s.scale, s.d_v)
+        return _close(outs[0], ref, TOL_BF16_MAX_ABS, TOL_BF16_REL_L2, False)
+    if name == "moe_gate" or name in MOE_EXTRA:
+        m = I.MOE_GATE if name == "moe_gate" else MOE_EXTRA[name]
+        ref_idx, ref_w, _ = G.moe_gate(*ov[name], m.k)
+        nbad = int((outs[0].numpy() != ref_idx).sum())
+        if nbad:
+            return f"FAIL: {nbad} expert indices differ"
+        err = float(np.abs(_f64(outs[1]) - ref_w).max())
+        return "ok" if err <= TOL_MOE_W_ABS else f"FAIL: weights differ by {err:.2e}"
+    if name == "fp8_gemm":
+        y, sx, xq = outs
+        ref_sx, ref_xq, ref_y = F.absmax_fp8_gemm(*ov[name])
+        if not np.array_equal(sx.numpy().view(np.uint32), ref_sx.view(np.uint32)):
+            return "FAIL: row scales differ"
+        nbad = int((xq.numpy() != ref_xq).sum())
+        if nbad:
+            return f"FAIL: {nbad} E4M3 codes differ"
+        return _close(y, ref_y, TOL_FP8_Y_REL, TOL_FP8_Y_REL_L2, True)
+    raise KeyError(name)
+
+
+def parity_gate(rf, step, ops, host):
+    """The first, un-timed call of every op, checked against the full oracle
+    on the same seeded inputs; returns {op: "ok" | "FAIL: ..."}."""
+    ov = oracle_view(host)
+    res = {}
+    if "fp8_gemm" in host:
+        wq_o, sw_o = ov["fp8_gemm"][1:]
+        same = (np.array_equal(step.wq.cpu().numpy(), wq_o)
+                and np.array_equal(step.sw.cpu().numpy().view(np.uint32), sw_o.view(np.uint32)))
+        res["fp8_weight"] = "ok" if same else "FAIL: weight codes or scales differ"
+    for op in ops:
+        (step.parity_calls.get(op.name) or step.calls[op.name])()
+        torch.cuda.synchronize()
+        outs = [t.cpu() for t in step.outputs[op.name]]
+        if op.name == "fp8_gemm":
+            outs += [step.sx.cpu(), step.xq.cpu()]
+        res[op.name] = check_op(op.name, outs, ov)
+    st = rf.rf_get_device_status()
+    if st != rf.RF_OK:
+        res["device_status"] = "FAIL: " + rf.rf_status_string(st)
+    return res
 
 
 # ------------------------------------------------------------------ clocks
@@ -393,6 +521,24 @@ def run_ours(args, world, rank, local):
     dev = {k: [t.cuda() for t in v] for k, v in host.items()}
     step = Step(rf, dev)
     stream = torch.cuda.current_stream()
+    for op in ops:
+        if op.name == "mla_decode":
+            s = I.MLA_DECODE
+            op.n_kernels = 1 + (rf.rf_mla_decode_num_splits(s.B, s.Hq, s.Lk, s.d_qk, s.d_v, 0) > 1)
+    # what a caller holds on the host for each call (the e2e copies): the FP8
+    # call takes the quantised weight the set-up made
+    call_host = dict(host)
+    if "fp8_gemm" in host:
+        call_host["fp8_gemm"] = [host["fp8_gemm"][0], step.wq.cpu(), step.sw.cpu()]
+
+    # parity: the first call of every op against the oracle (rank 0)
+    parity = None
+    if args.parity == "full" and rank == 0:
+        parity = parity_gate(rf, step, ops, host)
+        if any(v != "ok" for v in parity.values()):
+            print(json.dumps({"metric": METRIC, "value": None, "parity": parity,
+                              "error": "GPU outputs differ from the oracle"}), flush=True)
+            raise SystemExit(3)
 
     # warm-up
     for _ in range(args.warmup):
@@ -456,7 +602,7 @@ def run_ours(args, world, rank, local):
                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
     else:
         achieved = dom.flops / dom_t / 1e12
-        pk = peaks["bf16_tfs_sustained"] * (2.0 if dom.tc_dtype == "fp8" else 1.0)
+        pk = dom.tensor_peak(peaks)
         roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk,
                     "unit": "TFLOP/s", "frac": round(achieved / pk, 4)}
     roofline.update({"traffic": traffic_for(dom.name), "kernel": dom.name,
@@ -469,17 +615,20 @@ def run_ours(args, world, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; shapes of the five named workloads)",
         "config": workload_config(ops, world),
-        "peaks": {k: peaks[k] for k in ("hbm_gbs", "bf16_tfs", "bf16_tfs_sustained", "source")},
+        "peaks": {**{k: peaks[k] for k in ("hbm_gbs", "bf16_tfs", "bf16_tfs_sustained", "source")},
+                  "tensor_basis": "bf16_tfs (burst; x2 for FP8): each kernel runs well under 1 s"},
         "rows": rows,
         "roofline": roofline,
         "gpu_launches": args.steps * sum(op.n_kernels for op in ops),
         "clocks": clk,
+        "parity": parity if parity is not None else "not checked (--parity off or rank > 0)",
     }
 
     if not args.no_e2e:
-        result["e2e"] = run_e2e(rf, ops, peaks, host, step, world, args)
+        result["e2e"] = run_e2e(rf, ops, peaks, call_host, step, world, args)
     if not args.no_cpu_baseline and rank == 0 and world == 1:
-        result["cpu_baseline"] = cpu_baseline(ops, peaks, host, budget_s=args.cpu_budget)
+        result["cpu_baseline"] = cpu_baseline(ops, peaks, oracle_view(host),
+                                              budget_s=args.cpu_budget)
     return result
 
 
@@ -749,7 +898,7 @@ def run_reference(args, world, rank):
         return None
     peaks = load_peaks()
     ops = select_ops(args)
-    host = host_inputs([op.name for op in ops])
+    host = oracle_view(host_inputs([op.name for op in ops]))
     fits = oracle_cost_fits(host, 1.0 / 8192, 1.0 / 1024)
     names = list(fits)
     est = {k: fixed + slope for k, (fixed, slope, _) in fits.items()}
@@ -771,10 +920,14 @@ def run_reference(args, world, rank):
     sample = ("one op per step, in turn, by the fp64 numpy oracle; fraction of the op's "
               "rows/heads/tokens: " + ", ".join(f"{k} {f:.4f}" for k, f in fracs.items())
               + "; full step = sum of each op's latest estimate (fixed per-call part plus the "
-                "rest scaled to the whole op)")
+                "rest scaled to the whole op); no full step is run: steps and ms_per_step are "
+                "estimates")
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(full_s * 1e3, 1),
+        "estimated": True,
+        "ops_sampled": {"per_step": 1, "total": args.steps + args.warmup,
+                        "distinct": len(fracs)},
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded; shapes of the five named workloads)",
         "config": {"workload": workload_name(ops),
@@ -799,6 +952,9 @@ def main():
     ap.add_argument("--splits", default="",
                     help="explicit decode split counts, e.g. 32768:64,2048:8 (default: automatic)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--parity", choices=["full", "off"], default="full",
+                    help="check the first call of every op against the full fp64 oracle "
+                         "before timing (default full)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0,

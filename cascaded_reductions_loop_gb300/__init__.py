@@ -25,14 +25,15 @@ __all__ = [
     "rf_attn_decode_splitkv_workspace_size", "rf_attn_decode_splitkv_noalloc",
     "RF_DECODE_NOALLOC_SCRATCH_BYTES", "rf_mla_decode", "rf_mla_decode_num_splits",
     "rf_mla_decode_workspace_size", "rf_moe_gate_topk_softmax",
-    "rf_absmax_fp8_gemm", "rf_absmax_fp8_gemm_workspace_size", "rf_selftest_wait_timeout",
+    "rf_absmax_fp8_gemm", "rf_absmax_fp8_gemm_workspace_size", "rf_absmax_quant_fp8",
+    "rf_selftest_wait_timeout",
     "RF_OK", "RF_ERR_INVALID_ARG", "RF_ERR_UNSUPPORTED", "RF_ERR_WORKSPACE", "RF_ERR_CUDA",
-    "RF_ERR_DEVICE_TIMEOUT", "RF_ERR_DEVICE_INPUT", "RF_F32", "RF_BF16",
+    "RF_ERR_DEVICE_TIMEOUT", "RF_ERR_DEVICE_INPUT", "RF_ERR_DEVICE_LAYOUT", "RF_F32", "RF_BF16",
     "RF_ATTN_AUTO", "RF_ATTN_INCREMENTAL", "RF_ATTN_TWO_PASS",
 ]
 
 RF_OK, RF_ERR_INVALID_ARG, RF_ERR_UNSUPPORTED, RF_ERR_WORKSPACE, RF_ERR_CUDA, \
-    RF_ERR_DEVICE_TIMEOUT, RF_ERR_DEVICE_INPUT = range(7)
+    RF_ERR_DEVICE_TIMEOUT, RF_ERR_DEVICE_INPUT, RF_ERR_DEVICE_LAYOUT = range(8)
 RF_F32, RF_BF16 = 0, 1
 RF_ATTN_AUTO, RF_ATTN_INCREMENTAL, RF_ATTN_TWO_PASS = 0, 1, 2
 RF_DECODE_NOALLOC_SCRATCH_BYTES = 16 << 20   # as in rf.h
@@ -69,6 +70,7 @@ _SIGS = {
     "rf_moe_gate_topk_softmax": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "rf_absmax_fp8_gemm_workspace_size": (_Z, [_I, _I, _I]),
     "rf_absmax_fp8_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _Z, _P]),
+    "rf_absmax_quant_fp8": (_I, [_P, _I, _I, _P, _P, _P]),
     "rf_selftest_wait_timeout": (_I, [_I, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -267,12 +269,13 @@ def rf_absmax_fp8_gemm_workspace_size(M, N, K) -> int:
     return lib.rf_absmax_fp8_gemm_workspace_size(M, N, K)
 
 
-def rf_absmax_fp8_gemm(x, wq, sw, y, sx_out=None, xq_out=None, workspace=None,
-                       stream=None) -> None:
+def rf_absmax_fp8_gemm(x, wq, sw, y, workspace, sx_out=None, xq_out=None, stream=None) -> None:
     """Row absmax -> E4M3 quantisation -> FP8 GEMM -> dequantisation.
     x: [M,K] bf16; wq: [N,K] uint8 E4M3 codes; sw: [N] fp32; y: [M,N] bf16
-    out; sx_out: [M] fp32 out or None; xq_out: [M,K] uint8 out or None;
-    workspace: uint8 CUDA tensor (needed when sx_out or xq_out is None)."""
+    out; workspace: uint8 CUDA tensor of at least
+    rf_absmax_fp8_gemm_workspace_size(M, N, K) bytes (always required: it
+    holds the kernel's row counters); sx_out: [M] fp32 out or None; xq_out:
+    [M,K] uint8 out or None."""
     M, K = x.shape
     N = wq.shape[0]
     _need(x, torch.bfloat16, (M, K), "x")
@@ -287,6 +290,17 @@ def rf_absmax_fp8_gemm(x, wq, sw, y, sx_out=None, xq_out=None, workspace=None,
     _check(lib.rf_absmax_fp8_gemm(_ptr(x), _ptr(wq), _ptr(sw), _ptr(y), M, N, K, _ptr(sx_out),
                                   _ptr(xq_out), _ptr(workspace), ws_bytes, _stream(stream)),
            "rf_absmax_fp8_gemm")
+
+
+def rf_absmax_quant_fp8(x, sx_out, xq_out, stream=None) -> None:
+    """Row absmax and E4M3 quantisation alone.  x: [M,K] bf16; sx_out: [M]
+    fp32 out; xq_out: [M,K] uint8 out (same bits as rf_absmax_fp8_gemm)."""
+    M, K = x.shape
+    _need(x, torch.bfloat16, (M, K), "x")
+    _need(sx_out, torch.float32, (M,), "sx_out")
+    _need(xq_out, torch.uint8, (M, K), "xq_out")
+    _check(lib.rf_absmax_quant_fp8(_ptr(x), M, K, _ptr(sx_out), _ptr(xq_out), _stream(stream)),
+           "rf_absmax_quant_fp8")
 
 
 def rf_selftest_wait_timeout(timeout_us: int, stream=None) -> None:

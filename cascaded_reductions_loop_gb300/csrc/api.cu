@@ -20,8 +20,10 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 unsigned* g_err_ptr[kMaxDevices] = {};
+void* g_err_ctx[kMaxDevices] = {};
 int g_sm_count[kMaxDevices] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+PFN_cuCtxGetCurrent_v4000 g_ctx_get = nullptr;
 
 int current_device() {
   int dev = -1;
@@ -30,15 +32,42 @@ int current_device() {
 }
 }  // namespace
 
+void* current_cu_context() {
+  PFN_cuCtxGetCurrent_v4000 get = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_ctx_get) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return nullptr;
+      g_ctx_get = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    }
+    get = g_ctx_get;
+  }
+  CUcontext ctx = nullptr;
+  return get(&ctx) == CUDA_SUCCESS ? static_cast<void*>(ctx) : nullptr;
+}
+
+// The address is cached together with the context it belongs to: after a
+// device reset the runtime creates a new context whose copy of the word
+// lives elsewhere, and the lookup is then repeated.
 unsigned* device_error_word() {
   const int dev = current_device();
   if (dev < 0) return nullptr;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_err_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
-    g_err_ptr[dev] = static_cast<unsigned*>(p);
+  void* ctx = current_cu_context();
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_err_ptr[dev] && ctx && ctx == g_err_ctx[dev]) return g_err_ptr[dev];
   }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess || !p) return nullptr;
+  ctx = current_cu_context();        // the lookup above creates the context if needed
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_err_ptr[dev] = static_cast<unsigned*>(p);
+  g_err_ctx[dev] = ctx;
   return g_err_ptr[dev];
 }
 
@@ -149,6 +178,8 @@ const char* rf_status_string(int status) {
     case RF_ERR_DEVICE_TIMEOUT: return "RF_ERR_DEVICE_TIMEOUT: a kernel's bounded wait ran out";
     case RF_ERR_DEVICE_INPUT:
       return "RF_ERR_DEVICE_INPUT: device-side sizes (cu_seqlens) were inconsistent";
+    case RF_ERR_DEVICE_LAYOUT:
+      return "RF_ERR_DEVICE_LAYOUT: a kernel's shared memory was not aligned as its tiles need";
     default: return "unknown rf_status";
   }
 }
@@ -165,6 +196,7 @@ rf_status rf_get_device_status(rf_stream_t stream) {
     if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) return RF_ERR_CUDA;
   }
   if (v & kDevErrTimeout) return RF_ERR_DEVICE_TIMEOUT;
+  if (v & kDevErrLayout) return RF_ERR_DEVICE_LAYOUT;
   return (v & kDevErrInput) ? RF_ERR_DEVICE_INPUT : RF_OK;
 }
 
@@ -330,7 +362,7 @@ rf_status rf_moe_gate_topk_softmax(const void* X, const void* Wg, int T, int D, 
 
 size_t rf_absmax_fp8_gemm_workspace_size(int M, int N, int K) {
   if (M < 1 || N < 1 || K < 16 || K % 16 != 0) return 0;
-  return fp8_workspace_bytes(M, N, K);
+  return fp8_workspace_bytes(M, N, K, true, true);
 }
 
 rf_status rf_absmax_fp8_gemm(const void* X, const uint8_t* Wq, const float* sw, void* Y, int M,
@@ -340,20 +372,22 @@ rf_status rf_absmax_fp8_gemm(const void* X, const uint8_t* Wq, const float* sw, 
   if (M < 1 || N < 1 || K < 16 || K % 16 != 0) return RF_ERR_INVALID_ARG;
   if ((int64_t)M * K >= (1ll << 40) || (int64_t)N * K >= (1ll << 40)) return RF_ERR_INVALID_ARG;
   if ((sx_out && !aligned16(sx_out)) || (xq_out && !aligned16(xq_out))) return RF_ERR_INVALID_ARG;
-  float* sx = sx_out;
-  uint8_t* xq = xq_out;
-  if (!sx || !xq) {
-    if (!workspace || !aligned16(workspace) || workspace_bytes < fp8_workspace_bytes(M, N, K))
-      return RF_ERR_WORKSPACE;
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    const size_t xq_bytes = ((size_t)M * K + 255) & ~(size_t)255;
-    if (!xq) xq = ws;
-    if (!sx) sx = reinterpret_cast<float*>(ws + xq_bytes);
-  }
+  if (!workspace || !aligned16(workspace) ||
+      workspace_bytes < fp8_workspace_bytes(M, N, K, !xq_out, !sx_out))
+    return RF_ERR_WORKSPACE;
   unsigned* err = device_error_word();
   if (!err) return RF_ERR_CUDA;
-  return from_cuda(launch_absmax_fp8_gemm(X, Wq, sw, Y, M, N, K, sx, xq, err,
+  return from_cuda(launch_absmax_fp8_gemm(X, Wq, sw, Y, M, N, K, sx_out, xq_out, workspace, err,
                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+rf_status rf_absmax_quant_fp8(const void* X, int M, int K, float* sx_out, uint8_t* xq_out,
+                              rf_stream_t stream) {
+  if (!ptr_ok(X) || !ptr_ok(sx_out) || !ptr_ok(xq_out)) return RF_ERR_INVALID_ARG;
+  if (M < 1 || K < 16 || K % 16 != 0) return RF_ERR_INVALID_ARG;
+  if ((int64_t)M * K >= (1ll << 40)) return RF_ERR_INVALID_ARG;
+  return from_cuda(launch_absmax_quant(X, M, K, sx_out, xq_out,
+                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
 rf_status rf_selftest_wait_timeout(int timeout_us, rf_stream_t stream) {

@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   };
 
   if ((smem_u32(smem) & 1023u) != 0) {   // swizzled tiles need 1 KB alignment
-    if (threadIdx.x == 0) raise_error(err, kDevErrTimeout);
+    if (threadIdx.x == 0) raise_error(err, kDevErrLayout);
     return;
   }
 

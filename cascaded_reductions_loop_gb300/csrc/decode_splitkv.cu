@@ -468,20 +468,29 @@ static __device__ __align__(256) uint8_t g_decode_scratch[kNoAllocScratchBytes];
 constexpr int kMaxScratchDevices = 64;
 std::mutex g_scratch_mu;
 void* g_scratch_ptr[kMaxScratchDevices] = {};
+void* g_scratch_ctx[kMaxScratchDevices] = {};
 
 // Device address of g_decode_scratch on the current device.  In host code the
 // array's name is only a host-side handle, so the address is looked up once
-// per device (with that device current) and cached.  Returns nullptr on error.
+// per device (with that device current) and cached together with the CUDA
+// context it belongs to; if the context changes (a device reset makes the
+// runtime create a new one, with its own copy of the array), it is looked up
+// again.  Returns nullptr on error.
 void* decode_scratch_address() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxScratchDevices) return nullptr;
-  std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return nullptr;
-    g_scratch_ptr[dev] = p;
+  void* ctx = current_cu_context();
+  {
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (g_scratch_ptr[dev] && ctx && ctx == g_scratch_ctx[dev]) return g_scratch_ptr[dev];
   }
-  return g_scratch_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return nullptr;
+  ctx = current_cu_context();        // the lookup above creates the context if needed
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  g_scratch_ptr[dev] = p;
+  g_scratch_ctx[dev] = ctx;
+  return p;
 }
 
 }  // namespace

@@ -4,22 +4,27 @@
 // The cascade has a hard dependency: no element can be rounded before the
 // max of its whole row is known, and the rounding is not linear, so the max
 // cannot be folded into the GEMM loop incrementally the way the softmax max
-// can.  It therefore runs as two cooperating kernels ([E] §3.3 multi-kernel
-// level):
-//   1. absmax_quant_regs_kernel (rows up to 4096 elements; longer rows use
-//      absmax_quant_long_kernel, which reads each row twice): one warp per
-//      row of X reads the row once into registers, reduces |x| to the row
-//      max, sets sx = max / 448 (IEEE fp32 division) and writes the E4M3
-//      codes of the correctly rounded x / sx (cvt.rn.satfinite) plus sx.
-//      X is read from HBM once.
-//   2. fp8_gemm_kernel: a tcgen05 GEMM (kind::f8f6f4, E4M3 x E4M3 -> fp32 in
-//      tensor memory) over TMA-staged 128-byte-swizzled tiles, warp
-//      specialised (TMA producer warp, single-thread MMA issuer, four
-//      epilogue warps), whose epilogue applies sx[m] * sw[n] and rounds to
-//      bf16.  It is launched as a programmatic dependent of kernel 1.  The
-//      codes travel through memory as 1 byte per element, half the size of
-//      the bf16 input, so the pair moves as many bytes as a fused kernel
-//      that re-reads X would.
+// can ([S] Methodologie 1: the round has no invertible dependent factor).
+// The two stages therefore cooperate inside one persistent kernel
+// (fp8_gemm_kernel), at the granularity of 128-row blocks of X ([E] §3.3,
+// the inter-block level):
+//   * quantiser warps (four per CTA) take rows of X from a global counter in
+//     increasing order; one warp holds a whole row in registers, reduces |x|
+//     to the row max, sets sx = max / 448 (IEEE fp32 division), writes the
+//     E4M3 codes of the correctly rounded x / sx (cvt.rn.satfinite) and then
+//     counts the row into its 128-row block's readiness counter (release);
+//   * the GEMM part runs on CTA pairs (2-CTA clusters, tcgen05 cta_group::2):
+//     a pair computes a 256 x 256 output tile, each CTA loading with TMA its
+//     own 128 rows of the codes and its own 128 rows of Wq into its own
+//     shared memory; one thread of rank 0 issues the M = 256 MMAs
+//     (kind::f8f6f4, E4M3 x E4M3 -> fp32 in tensor memory), so each SM reads
+//     only its half of the B tile from its shared memory.  A CTA's TMA
+//     producer waits (acquire) for its row block to be complete before it
+//     loads codes from it, so the first tiles start while later rows are
+//     still being quantised.  Four epilogue warps per CTA apply sx[m]*sw[n]
+//     and round to bf16.
+// The standalone absmax_quant_regs_kernel / absmax_quant_long_kernel compute
+// the first two steps alone (rf_absmax_quant_fp8).
 #include <math.h>
 
 #include "rf_device.cuh"
@@ -28,10 +33,11 @@
 namespace rf {
 namespace {
 
-// ------------------------------------------------------------------ kernel 1
+// ------------------------------------------------------------------ quantisation
 
 constexpr int kQuantWarps = 4;
 constexpr int kVecPerLaneMax = 16;   // rows up to 32 * 16 * 8 = 4096 elements stay in registers
+constexpr int kRegRowMax = 32 * kVecPerLaneMax * 8;
 
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
   uint16_t r;
@@ -113,67 +119,53 @@ __device__ __forceinline__ RowScale row_scale(uint32_t amax_bits) {
   return rs;
 }
 
-// Rows of up to 4096 elements: one warp per row, the row held in registers
-// (16 x 16-byte loads per lane).  Memory parallelism comes from occupancy:
-// four 4-warp CTAs per SM, each warp with its whole row in flight.
-__global__ void __launch_bounds__(kQuantWarps * 32, 4)
-    absmax_quant_regs_kernel(const uint4* __restrict__ X, uint8_t* __restrict__ Xq,
-                             float* __restrict__ sx, int M, int K) {
-  // the GEMM (a programmatic dependent) may be scheduled onto SMs this grid
-  // leaves; it waits for this grid to finish before reading Xq or sx
-  asm volatile("griddepcontrol.launch_dependents;");
-  const int lane = threadIdx.x & 31;
-  const int nw = gridDim.x * kQuantWarps;
-  const int nvec = K >> 3;
-  int row = blockIdx.x * kQuantWarps + (threadIdx.x >> 5);
+template <bool kStream>
+__device__ __forceinline__ void store_codes(uint2* p, uint2 v) {
+  if constexpr (kStream) __stcs(p, v);
+  else *p = v;
+}
+
+// One warp quantises one row of nvec 16-byte vectors (nvec <= 32 *
+// kVecPerLaneMax) held in registers: X is read from memory once.  kStream
+// marks the codes as streamed (evict-first) when nothing reads them soon.
+template <bool kStream>
+__device__ __forceinline__ void quant_row_regs(const uint4* __restrict__ xr, uint2* __restrict__ qr,
+                                               float* __restrict__ sxp, int nvec, int lane) {
   uint4 cur[kVecPerLaneMax];
-  auto load = [&](uint4 (&v)[kVecPerLaneMax], int rr) {
-    const uint4* xr = X + (size_t)rr * nvec;
 #pragma unroll
-    for (int i = 0; i < kVecPerLaneMax; ++i) {
-      const int j = lane + 32 * i;
-      v[i] = j < nvec ? __ldcs(xr + j) : make_uint4(0, 0, 0, 0);
-    }
-  };
-  for (; row < M; row += nw) {
-    load(cur, row);
-    uint32_t amax = 0;
+  for (int i = 0; i < kVecPerLaneMax; ++i) {
+    const int j = lane + 32 * i;
+    cur[i] = j < nvec ? __ldcs(xr + j) : make_uint4(0, 0, 0, 0);
+  }
+  uint32_t amax = 0;
 #pragma unroll
-    for (int i = 0; i < kVecPerLaneMax; ++i) amax = max(amax, absmax_bits(cur[i]));
-    const RowScale rs = row_scale(amax);
-    if (lane == 0) sx[row] = rs.s;
-    uint2* qr = reinterpret_cast<uint2*>(Xq + (size_t)row * K);
-    if (rs.s == 0.f) {                                // all-zero row: codes 0x00
+  for (int i = 0; i < kVecPerLaneMax; ++i) amax = max(amax, absmax_bits(cur[i]));
+  const RowScale rs = row_scale(amax);
+  if (lane == 0) *sxp = rs.s;
+  if (rs.s == 0.f) {                                // all-zero row: codes 0x00
 #pragma unroll
-      for (int i = 0; i < kVecPerLaneMax; ++i)
-        if (lane + 32 * i < nvec) qr[lane + 32 * i] = make_uint2(0, 0);
-    } else if (rs.recip) {
+    for (int i = 0; i < kVecPerLaneMax; ++i)
+      if (lane + 32 * i < nvec) store_codes<kStream>(qr + lane + 32 * i, make_uint2(0, 0));
+  } else if (rs.recip) {
 #pragma unroll
-      for (int i = 0; i < kVecPerLaneMax; ++i)
-        if (lane + 32 * i < nvec) __stcs(qr + lane + 32 * i, quant8<true>(cur[i], rs.s, rs.r));
-    } else {
+    for (int i = 0; i < kVecPerLaneMax; ++i)
+      if (lane + 32 * i < nvec)
+        store_codes<kStream>(qr + lane + 32 * i, quant8<true>(cur[i], rs.s, rs.r));
+  } else {
 #pragma unroll
-      for (int i = 0; i < kVecPerLaneMax; ++i)
-        if (lane + 32 * i < nvec) __stcs(qr + lane + 32 * i, quant8<false>(cur[i], rs.s, rs.r));
-    }
+    for (int i = 0; i < kVecPerLaneMax; ++i)
+      if (lane + 32 * i < nvec)
+        store_codes<kStream>(qr + lane + 32 * i, quant8<false>(cur[i], rs.s, rs.r));
   }
 }
 
-// Longer rows: two passes over the row (the second one hits L2).
-__global__ void __launch_bounds__(kQuantWarps * 32)
-    absmax_quant_long_kernel(const uint4* __restrict__ X, uint8_t* __restrict__ Xq,
-                             float* __restrict__ sx, int M, int K) {
-  asm volatile("griddepcontrol.launch_dependents;");
-  const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kQuantWarps + (threadIdx.x >> 5);
-  if (row >= M) return;
-  const int nvec = K >> 3;
-  const uint4* xr = X + (size_t)row * nvec;
-  uint2* qr = reinterpret_cast<uint2*>(Xq + (size_t)row * K);
+// Longer rows: two passes over the row (the second one mostly hits L2).
+__device__ __forceinline__ void quant_row_long(const uint4* __restrict__ xr, uint2* __restrict__ qr,
+                                               float* __restrict__ sxp, int nvec, int lane) {
   uint32_t amax = 0;
   for (int j = lane; j < nvec; j += 32) amax = max(amax, absmax_bits(__ldg(xr + j)));
   const RowScale rs = row_scale(amax);
-  if (lane == 0) sx[row] = rs.s;
+  if (lane == 0) *sxp = rs.s;
   for (int j = lane; j < nvec; j += 32) {
     if (rs.s == 0.f)
       qr[j] = make_uint2(0, 0);
@@ -183,52 +175,104 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
   }
 }
 
-// ------------------------------------------------------------------ kernel 2
+// Standalone quantisation, rows up to kRegRowMax elements: one warp per row.
+// Memory parallelism comes from occupancy: four 4-warp CTAs per SM, each
+// warp with its whole row in flight.
+__global__ void __launch_bounds__(kQuantWarps * 32, 4)
+    absmax_quant_regs_kernel(const uint4* __restrict__ X, uint8_t* __restrict__ Xq,
+                             float* __restrict__ sx, int M, int K) {
+  const int lane = threadIdx.x & 31;
+  const int nw = gridDim.x * kQuantWarps;
+  const int nvec = K >> 3;
+  for (int row = blockIdx.x * kQuantWarps + (threadIdx.x >> 5); row < M; row += nw)
+    quant_row_regs<true>(X + (size_t)row * nvec, reinterpret_cast<uint2*>(Xq + (size_t)row * K),
+                         sx + row, nvec, lane);
+}
 
-constexpr int BM = 128, BN = 256, BK = 128;      // BK bytes = one 128-byte swizzle row
-constexpr int kStages = 4;
-constexpr int kABytes = BM * BK, kBBytes = BN * BK, kStageBytes = kABytes + kBBytes;
-constexpr int kBHalfBytes = kBBytes / 2;         // the part of B one CTA of a pair loads
-constexpr int kGemmThreads = 192;                // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
-constexpr int kEpiThreads = 128;
+__global__ void __launch_bounds__(kQuantWarps * 32)
+    absmax_quant_long_kernel(const uint4* __restrict__ X, uint8_t* __restrict__ Xq,
+                             float* __restrict__ sx, int M, int K) {
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kQuantWarps + (threadIdx.x >> 5);
+  if (row >= M) return;
+  const int nvec = K >> 3;
+  quant_row_long(X + (size_t)row * nvec, reinterpret_cast<uint2*>(Xq + (size_t)row * K), sx + row,
+                 nvec, lane);
+}
+
+// ------------------------------------------------------------------ fused kernel
+
+constexpr int BM = 128;                          // rows of A per CTA (256 per pair)
+constexpr int BN = 256;                          // output columns per pair tile
+constexpr int BK = 128;                          // bytes of K per stage = one 128-byte swizzle row
+constexpr int kStages = 6;
+constexpr int kABytes = BM * BK;                 // this CTA's 128 rows of codes
+constexpr int kBBytes = (BN / 2) * BK;           // this CTA's half of the B tile
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kPairStageBytes = 2 * kStageBytes; // what lands on rank 0's barrier per stage
+constexpr int kEpiWarps = 4;
+constexpr int kFusedQuantWarps = 4;
+constexpr int kFirstEpiWarp = 2, kFirstQuantWarp = kFirstEpiWarp + kEpiWarps;
+constexpr int kGemmThreads = 32 * (kFirstQuantWarp + kFusedQuantWarps);   // 320
 constexpr int kAccCols = BN;                     // one fp32 accumulator tile in TMEM
 constexpr int kTmemCols = 2 * kAccCols;          // two: epilogue of tile i overlaps tile i+1
 constexpr int kGemmSmem = kStages * kStageBytes + 1024 /*align*/ + 256 /*bars*/;
-constexpr uint32_t kIdescF8 = make_idesc(BM, BN, /*e4m3*/ 0, 0, 0);
-constexpr uint16_t kPairMask = 0x3;
+constexpr uint32_t kIdescPair = make_idesc(2 * BM, BN, /*e4m3*/ 0, 0, 0);
+static_assert(kStages * kStageBytes + 256 + 1024 <= 227 * 1024, "shared memory");
 
 struct GemmBars {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
-  uint64_t acc_full[2];
-  uint64_t acc_empty[2];
-  uint64_t drain;
+  uint64_t full[kStages];    // rank 0: both CTAs' tiles of a stage have landed
+  uint64_t empty[kStages];   // each CTA: the pair's MMAs have read its slot
+  uint64_t acc_full[2];      // each CTA: its accumulator rows of a tile are complete
+  uint64_t acc_empty[2];     // rank 0: both CTAs' epilogues have drained a buffer
+  uint64_t drain;            // rank 0: every MMA has completed
   uint32_t tmem;
   int abort;
 };
 
-// Persistent, clusters of two CTAs.  The pair shares each 256-column B tile:
-// CTA r loads B rows n0 + 128 r .. + 127 and multicasts them to both CTAs, so
-// each SM pulls 32 KB (A 16 KB + half of B) per k-block from L2 instead of
-// 48 KB.  Pair p of the tile grid covers output rows 256 mp .. + 255 (CTA r
-// takes rows 256 mp + 128 r) and columns 256 nb; cluster c handles pairs
-// c, c + nclusters, ...  The MMA thread accumulates tile i into TMEM buffer
-// i % 2 while the epilogue warps drain buffer (i - 1) % 2.  A stage is
-// refilled only after the MMAs of both CTAs have read it (each MMA thread
-// commits to the "empty" barrier of both CTAs).
+// Readiness of one 128-row block of codes: bounded wait (acquire) until all
+// its rows below M have been counted in.
+__device__ __forceinline__ bool wait_rows_ready(const unsigned* ready, int m0, int M) {
+  if (m0 >= M) return true;                       // rows past M: TMA fills zeros
+  const unsigned need = (unsigned)min(BM, M - m0);
+  const unsigned* c = ready + m0 / BM;
+  if (ld_acquire_u32(c) < need) {
+    const uint64_t t0 = globaltimer_ns();
+    while (ld_acquire_u32(c) < need) {
+      if (globaltimer_ns() - t0 > kDefaultWaitNs) return false;
+      __nanosleep(128);
+    }
+  }
+  fence_proxy_async_global();                     // the codes are then read by TMA
+  return true;
+}
+
+// Persistent: 2-CTA clusters, one CTA per SM, 320 threads.
+//   warp 0     TMA producer (both CTAs)
+//   warp 1     TMEM allocation (both CTAs); MMA issuer (rank 0, one thread)
+//   warps 2-5  epilogue (TMEM lane quarter = warp % 4)
+//   warps 6-9  quantisers
+// Pair tile p covers output rows 256 (p / tiles_n) .. + 255 (CTA r: + 128 r)
+// and columns 256 (p % tiles_n) .. + 255 (CTA r loads B rows + 128 r); cluster
+// c takes tiles c, c + nclusters, ...  Rank 0's MMA thread accumulates tile i
+// into TMEM buffer i % 2 of both CTAs while the epilogues drain buffer
+// (i - 1) % 2.  Counters (zeroed by the host before the launch): ctr[0] is
+// the next row to quantise, ctr[1 + b] the rows of block b done.
 __global__ void __launch_bounds__(kGemmThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const float* __restrict__ sx, const float* __restrict__ sw,
-                    __nv_bfloat16* __restrict__ Y, int M, int N, int K, int tiles_n, int num_pairs,
-                    unsigned* err) {
+                    const uint4* __restrict__ X, uint8_t* __restrict__ Xq, float* __restrict__ sx,
+                    const float* __restrict__ sw, __nv_bfloat16* __restrict__ Y, int M, int N,
+                    int K, int tiles_n, int num_pairs, unsigned* __restrict__ ctr, unsigned* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   GemmBars* bars = reinterpret_cast<GemmBars*>(smem + kStages * kStageBytes);
   volatile int* abort_flag = &bars->abort;
+  const unsigned* ready = ctr + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int crank = (int)cluster_ctarank();
+  const bool leader = crank == 0;
   const int cid = (int)blockIdx.x >> 1, ncl = (int)gridDim.x >> 1;
   const int nk = (K + BK - 1) / BK;
   const int my_tiles = num_pairs > cid ? (num_pairs - cid + ncl - 1) / ncl : 0;
@@ -238,65 +282,76 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     prefetch_tmap(&tmB);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(smem_u32(&bars->full[i]), 1);
-      mbar_init(smem_u32(&bars->empty[i]), 2);      // both CTAs' MMAs release a stage
+      mbar_init(smem_u32(&bars->empty[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars->acc_full[i]), 1);
-      mbar_init(smem_u32(&bars->acc_empty[i]), kEpiThreads);
+      mbar_init(smem_u32(&bars->acc_empty[i]), 2 * kEpiWarps);
     }
     mbar_init(smem_u32(&bars->drain), 1);
     bars->abort = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&bars->tmem), kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(&bars->tmem), kTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  cluster_sync();            // both CTAs' barriers exist before any multicast
+  cluster_sync();            // both CTAs' barriers and TMEM exist before any cross-CTA use
   tc_fence_after();
   const uint32_t tmem = bars->tmem;
-  // launched as a programmatic dependent of the quantisation kernel: the
-  // prologue above overlapped its tail; Xq and sx are read only after this
-  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer
+      // ---------------- TMA producer: this CTA's A rows and B half, counted
+      // on rank 0's full barrier
       int it = 0;
-      for (int i = 0; i < my_tiles && !*abort_flag; ++i) {
+      bool ok = true;
+      for (int i = 0; ok && i < my_tiles && !*abort_flag; ++i) {
         const int p = cid + i * ncl;
-        const int m0 = (p / tiles_n) * (2 * BM) + crank * BM, n0 = (p % tiles_n) * BN;
+        const int m0 = (p / tiles_n) * (2 * BM) + crank * BM;
+        const int nb0 = (p % tiles_n) * BN + crank * (BN / 2);
+        if (!wait_rows_ready(ready, m0, M)) {
+          ok = false;
+          break;
+        }
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int slot = it % kStages;
           if (it >= kStages &&
-              !mbar_wait(smem_u32(&bars->empty[slot]), (uint32_t)(((it / kStages) + 1) & 1))) {
-            raise_error(err, kDevErrTimeout);
-            *abort_flag = 1;
+              !mbar_wait_cluster(smem_u32(&bars->empty[slot]), (uint32_t)(((it / kStages) + 1) & 1))) {
+            ok = false;
             break;
           }
-          if (*abort_flag) break;
+          if (*abort_flag) {
+            ok = false;
+            break;
+          }
           uint8_t* a = smem + slot * kStageBytes;
-          const uint32_t bar = smem_u32(&bars->full[slot]);
-          mbar_arrive_expect_tx(bar, kStageBytes);   // A + both halves of B
-          tma_load_2d(smem_u32(a), &tmA, bar, kb * BK, m0);
-          tma_load_2d_mc(smem_u32(a + kABytes + crank * kBHalfBytes), &tmB, bar, kb * BK,
-                         n0 + crank * (BN / 2), kPairMask);
+          const uint32_t full0 = mapa_shared(smem_u32(&bars->full[slot]), 0);
+          if (leader) mbar_arrive_expect_tx(smem_u32(&bars->full[slot]), kPairStageBytes);
+          tma_load_2d_pair(smem_u32(a), &tmA, full0, kb * BK, m0);
+          tma_load_2d_pair(smem_u32(a + kABytes), &tmB, full0, kb * BK, nb0);
         }
       }
-      if (*abort_flag)   // let the copies this CTA waits for land before smem is released
-        for (int j = it - kStages < 0 ? 0 : it - kStages; j < it; ++j)
-          (void)mbar_wait(smem_u32(&bars->full[j % kStages]), (uint32_t)((j / kStages) & 1),
-                          1000000ull);
+      if (!ok) {
+        raise_error(err, kDevErrTimeout);
+        *abort_flag = 1;
+      }
+      // the last stages' release arrives from the peer's MMA thread: take
+      // them before this CTA may exit (bounded)
+      for (int j = it - kStages < 0 ? 0 : it - kStages; j < it; ++j)
+        ok = mbar_wait_cluster(smem_u32(&bars->empty[j % kStages]), (uint32_t)((j / kStages) & 1),
+                               ok ? kDefaultWaitNs : 1000000ull) && ok;
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer (one thread)
+    if (leader && lane == 0) {
+      // ---------------- MMA issuer (one thread of rank 0)
       int it = 0;
       bool ok = true;
       for (int i = 0; ok && i < my_tiles; ++i) {
         const int a = i & 1;
-        if (i >= 2 && !mbar_wait(smem_u32(&bars->acc_empty[a]), (uint32_t)(((i >> 1) + 1) & 1))) {
+        if (i >= 2 &&
+            !mbar_wait_cluster(smem_u32(&bars->acc_empty[a]), (uint32_t)(((i >> 1) + 1) & 1))) {
           ok = false;
           break;
         }
@@ -304,7 +359,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t d = tmem + a * kAccCols;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int slot = it % kStages;
-          if (!mbar_wait(smem_u32(&bars->full[slot]), (uint32_t)((it / kStages) & 1)) ||
+          if (!mbar_wait_cluster(smem_u32(&bars->full[slot]), (uint32_t)((it / kStages) & 1)) ||
               *abort_flag) {
             ok = false;
             break;
@@ -314,21 +369,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t sb = sa + kABytes;
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k)
-            mma_f8_ss(d, sw128_desc(sa + k * 32, 1024, 16), sw128_desc(sb + k * 32, 1024, 16),
-                      kIdescF8, (kb | k) != 0);
-          mma_commit_mc(smem_u32(&bars->empty[slot]), kPairMask);
+            mma_f8_pair(d, sw128_desc(sa + k * 32, 1024, 16), sw128_desc(sb + k * 32, 1024, 16),
+                        kIdescPair, (kb | k) != 0);
+          mma_commit_pair(smem_u32(&bars->empty[slot]));
+          mma_commit_pair(mapa_shared(smem_u32(&bars->empty[slot]), 1));
         }
-        if (ok) mma_commit(smem_u32(&bars->acc_full[a]));
+        if (ok) {
+          mma_commit_pair(smem_u32(&bars->acc_full[a]));
+          mma_commit_pair(mapa_shared(smem_u32(&bars->acc_full[a]), 1));
+        }
       }
       if (!ok) {
         raise_error(err, kDevErrTimeout);
         *abort_flag = 1;
       }
       // nothing may still run on the tensor core when TMEM is released
-      mma_commit(smem_u32(&bars->drain));
+      mma_commit_pair(smem_u32(&bars->drain));
       (void)mbar_wait(smem_u32(&bars->drain), 0, 1000000000ull);
     }
-  } else {
+  } else if (warp < kFirstQuantWarp) {
     // ---------------- epilogue: TMEM -> registers -> scale -> bf16 -> global
     const int sub = warp & 3;                    // TMEM lane quarter of this warp
     const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
@@ -338,7 +397,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int p = cid + i * ncl;
       const int m0 = (p / tiles_n) * (2 * BM) + crank * BM, n0 = (p % tiles_n) * BN;
       const int row = m0 + sub * 32 + lane;
-      const bool got = mbar_wait(smem_u32(&bars->acc_full[a]), (uint32_t)((i >> 1) & 1));
+      const bool got = mbar_wait_cluster(smem_u32(&bars->acc_full[a]), (uint32_t)((i >> 1) & 1)) &&
+                       wait_rows_ready(ready, m0, M);
       if (!__all_sync(0xffffffffu, got && !*abort_flag)) {
         raise_error(err, kDevErrTimeout);
         *abort_flag = 1;
@@ -391,76 +451,139 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(smem_u32(&bars->acc_empty[a]));   // buffer a may be overwritten
+      __syncwarp();
+      if (lane == 0) {                             // buffer a may be overwritten
+        if (leader) mbar_arrive(smem_u32(&bars->acc_empty[a]));
+        else mbar_arrive_remote(mapa_shared(smem_u32(&bars->acc_empty[a]), 0));
+      }
+    }
+  } else {
+    // ---------------- quantisers: rows in increasing order from ctr[0]
+    const int nvec = K >> 3;
+    while (true) {
+      int row = 0;
+      if (lane == 0) row = (int)atomicAdd(ctr, 1u);
+      row = __shfl_sync(0xffffffffu, row, 0);
+      if (row >= M) break;
+      const uint4* xr = X + (size_t)row * nvec;
+      uint2* qr = reinterpret_cast<uint2*>(Xq + (size_t)row * K);
+      if (K <= kRegRowMax) quant_row_regs<false>(xr, qr, sx + row, nvec, lane);
+      else quant_row_long(xr, qr, sx + row, nvec, lane);
+      fence_proxy_async_global();                  // codes are read by TMA
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence();
+        red_release_add(ctr + 1 + row / BM, 1u);
+      }
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  // rank 0 has drained its MMAs and each CTA has taken its last barrier
+  // arrivals from the peer; neither CTA's shared or tensor memory is used by
+  // the other after this
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc_pair(tmem, kTmemCols);
   }
-  // the peer may still multicast into this CTA or arrive on its barriers
-  // until both are done
-  cluster_sync();
+}
+
+// Pairs of CTAs of fp8_gemm_kernel that can be resident at once (cached per
+// device): at most one per two SMs.
+int gemm_clusters(int sms, cudaLaunchConfig_t cfg) {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!cached[dev]) {
+    cfg.gridDim = dim3(sms & ~1, 1, 1);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_kernel, &cfg) != cudaSuccess || n < 1) return 0;
+    cached[dev] = n < sms / 2 ? n : sms / 2;
+  }
+  return cached[dev];
 }
 
 }  // namespace
 
-size_t fp8_workspace_bytes(int M, int N, int K) {
-  (void)N;
-  const size_t xq = ((size_t)M * K + 255) & ~(size_t)255;
-  return xq + (size_t)M * sizeof(float);
+size_t fp8_counter_bytes(int M) {
+  return ((size_t)(1 + (M + BM - 1) / BM) * sizeof(unsigned) + 255) & ~(size_t)255;
 }
 
-cudaError_t launch_absmax_fp8_gemm(const void* X, const uint8_t* Wq, const float* sw, void* Y,
-                                   int M, int N, int K, float* sx, uint8_t* xq, unsigned* err,
-                                   cudaStream_t s) {
-  // kernel 1: absmax + quantisation
+size_t fp8_workspace_bytes(int M, int N, int K, bool need_xq, bool need_sx) {
+  (void)N;
+  size_t b = fp8_counter_bytes(M);
+  if (need_xq) b += ((size_t)M * K + 255) & ~(size_t)255;
+  if (need_sx) b += (size_t)M * sizeof(float);
+  return b;
+}
+
+cudaError_t launch_absmax_quant(const void* X, int M, int K, float* sx, uint8_t* xq,
+                                cudaStream_t s) {
   const int qblocks = (M + kQuantWarps - 1) / kQuantWarps;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidValue;
-  if (K <= 32 * kVecPerLaneMax * 8) {
+  if (K <= kRegRowMax) {
     const int resident = 4 * sms;                      // four 4-warp CTAs per SM
     absmax_quant_regs_kernel<<<qblocks < resident ? qblocks : resident, kQuantWarps * 32, 0, s>>>(
         static_cast<const uint4*>(X), xq, sx, M, K);
   } else {
-    absmax_quant_long_kernel<<<qblocks, kQuantWarps * 32, 0, s>>>(
-        static_cast<const uint4*>(X), xq, sx, M, K);
+    absmax_quant_long_kernel<<<qblocks, kQuantWarps * 32, 0, s>>>(static_cast<const uint4*>(X), xq,
+                                                                   sx, M, K);
   }
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
 
-  // kernel 2: FP8 GEMM with dequantising epilogue
+cudaError_t launch_absmax_fp8_gemm(const void* X, const uint8_t* Wq, const float* sw, void* Y,
+                                   int M, int N, int K, float* sx, uint8_t* xq, void* workspace,
+                                   unsigned* err, cudaStream_t s) {
+  const int sms = sm_count();
+  if (sms < 2) return cudaErrorInvalidValue;
+  // workspace: counters first, then (when the caller keeps no copy) the codes
+  // and the row scales
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  unsigned* ctr = reinterpret_cast<unsigned*>(ws);
+  size_t off = fp8_counter_bytes(M);
+  if (!xq) {
+    xq = ws + off;
+    off += ((size_t)M * K + 255) & ~(size_t)255;
+  }
+  if (!sx) sx = reinterpret_cast<float*>(ws + off);
+
   CUtensorMap tmA, tmB;
   if (!encode_tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, (uint64_t)K, (uint64_t)M,
                       (uint64_t)K, BK, BM, true) ||
       !encode_tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, (uint64_t)K, (uint64_t)N,
                       (uint64_t)K, BK, BN / 2, true))
     return cudaErrorInvalidValue;
+  cudaError_t e = cudaMemsetAsync(ctr, 0, (size_t)(1 + (M + BM - 1) / BM) * sizeof(unsigned), s);
+  if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(fp8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
   if (e != cudaSuccess) return e;
   const int tiles_n = (N + BN - 1) / BN;
   const int64_t pairs = (int64_t)tiles_n * ((M + 2 * BM - 1) / (2 * BM));
   if (pairs >= (1ll << 30)) return cudaErrorInvalidValue;
-  const int clusters = (int)(pairs < sms / 2 ? pairs : sms / 2);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * (clusters > 0 ? clusters : 1), 1, 1);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = kGemmSmem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, fp8_gemm_kernel, tmA, tmB, static_cast<const float*>(sx), sw,
-                            static_cast<__nv_bfloat16*>(Y), M, N, K, tiles_n, (int)pairs, err);
+  cfg.numAttrs = 1;
+  // every CTA also quantises, so the grid fills the GPU even when there are
+  // fewer tiles than pairs of SMs; it is sized to the clusters that can be
+  // resident together
+  const int clusters = gemm_clusters(sms, cfg);
+  if (clusters < 1) return cudaErrorInvalidConfiguration;
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  return cudaLaunchKernelEx(&cfg, fp8_gemm_kernel, tmA, tmB, static_cast<const uint4*>(X), xq, sx,
+                            sw, static_cast<__nv_bfloat16*>(Y), M, N, K, tiles_n, (int)pairs, ctr,
+                            err);
 }
 
 }  // namespace rf

@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lo = t0 * BN, hi = min(Lk, (t0 + nt) * BN);
   const int nblk = rank == 0 ? 5 : 4;
   if ((smem_u32(smem) & 1023u) != 0 || nt < 1) {   // both CTAs of the cluster agree
-    if (threadIdx.x == 0) raise_error(err, kDevErrInput);
+    if (threadIdx.x == 0) raise_error(err, nt < 1 ? kDevErrInput : kDevErrLayout);
     nt = 0;
   }
 

@@ -1,6 +1,8 @@
 // rf_device.cuh -- device-side building blocks for sm_103a: mbarriers with
-// bounded waits, TMA (tensor and bulk copies, no multicast), tcgen05 tensor
-// memory / MMA / loads, and small warp utilities.  Inline PTX only.
+// bounded waits, TMA tensor and bulk copies (each copy lands in the shared
+// memory of the CTA that issues it), tcgen05 tensor memory / MMA / loads for
+// one CTA and for a CTA pair, global acquire/release counters, and small warp
+// utilities.  Inline PTX only.
 #pragma once
 
 #include <cuda.h>
@@ -14,6 +16,7 @@ namespace rf {
 // Bits of the device-side error word (one per device, owned by the library).
 constexpr unsigned kDevErrTimeout = 1u;
 constexpr unsigned kDevErrInput = 2u;     // inconsistent device-side sizes (clamped, skipped)
+constexpr unsigned kDevErrLayout = 4u;    // shared memory not aligned as the tiles need (no work done)
 
 // Default wait limit of a bounded wait, in nanoseconds of %globaltimer.
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;   // 2 s
@@ -149,18 +152,6 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* m, int32_t x,
                : "memory");
 }
 
-// 2-D tiled load multicast to every CTA of the cluster in `cta_mask`: the
-// tile lands at the same shared-memory offset in each, and each destination
-// CTA's barrier at `bar`'s offset receives the byte count.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* m, uint32_t bar,
-                                               int32_t x, int32_t y, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask)
-      : "memory");
-}
-
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -275,13 +266,67 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       : "memory");
 }
 
-// Like mma_commit, but arrives on the barrier at the same shared-memory offset
-// in every CTA of the cluster named in `cta_mask`.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
+// ----------------------------------------------------------------- CTA pairs
+// A pair is the two CTAs of a 2-CTA cluster (ranks 0 and 1).  With
+// cta_group::2 one thread of rank 0 issues an MMA whose M = 256 rows are split
+// over the pair: each CTA supplies 128 rows of A and N/2 rows of B at the same
+// shared-memory offsets, and each CTA's tensor memory receives its 128 rows of
+// D.  Every tcgen05 instruction of a kernel that uses the pair form must use
+// it too (allocation, MMA, commit).
+
+// TMEM allocation of the same columns in both CTAs: one warp of each CTA
+// executes it; each writes the base address to its own shared memory.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// D[tmem, both CTAs] (+)= A * B^T over the pair (E4M3 x E4M3 -> fp32).
+__device__ __forceinline__ void mma_f8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar), "h"(cta_mask)
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// Arrives once on the barrier at cluster address `bar` (this CTA's or the
+// peer's, from mapa_shared) when every pair MMA issued so far by this thread
+// has completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// 2-D tiled load into this CTA's shared memory whose bytes complete the
+// transaction count of `bar`, a cluster address of a barrier in this CTA or
+// in its pair peer (used to gather both CTAs' operand tiles on rank 0's
+// barrier).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                                 int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+// Arrive (release at cluster scope) on a barrier of another CTA of the
+// cluster, given its cluster address.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
 }
 
 // ----------------------------------------------------------------- clusters
@@ -382,6 +427,26 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
       if (mbar_try_wait_cluster(bar, parity)) return true;
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
+}
+
+// ----------------------------------------------------------------- global counters
+
+// Load with acquire semantics at GPU scope (pairs with red_release_add).
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Atomic add with release semantics at GPU scope.
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Orders this thread's generic-proxy global accesses with its async-proxy
+// (TMA) accesses of global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // ----------------------------------------------------------------- misc

@@ -11,8 +11,11 @@
 
 namespace rf {
 
-// Device address of the per-device error word (set up once per device).
-// Returns nullptr if the address could not be obtained.
+// The current CUDA context (driver handle), or nullptr if there is none yet.
+void* current_cu_context();
+
+// Device address of the per-device error word (looked up once per device and
+// context).  Returns nullptr if the address could not be obtained.
 unsigned* device_error_word();
 
 // SM count of the current device (cached per device).
@@ -70,10 +73,15 @@ cudaError_t launch_mla_decode(const void* Q, const void* CKV, void* O, int B, in
 cudaError_t launch_moe_gate(const void* X, const void* Wg, int T, int D, int E, int k,
                             int32_t* idx, float* w, unsigned* err, cudaStream_t s);
 
-size_t fp8_workspace_bytes(int M, int N, int K);
+// FP8: the workspace holds the kernel's row counters, then (when the caller
+// keeps no copy) the codes and the row scales.
+size_t fp8_counter_bytes(int M);
+size_t fp8_workspace_bytes(int M, int N, int K, bool need_xq, bool need_sx);
+cudaError_t launch_absmax_quant(const void* X, int M, int K, float* sx, uint8_t* xq,
+                                cudaStream_t s);
 cudaError_t launch_absmax_fp8_gemm(const void* X, const uint8_t* Wq, const float* sw, void* Y,
-                                   int M, int N, int K, float* sx, uint8_t* xq, unsigned* err,
-                                   cudaStream_t s);
+                                   int M, int N, int K, float* sx, uint8_t* xq, void* workspace,
+                                   unsigned* err, cudaStream_t s);
 
 cudaError_t launch_selftest_wait_timeout(int timeout_us, unsigned* err, cudaStream_t s);
 

@@ -51,7 +51,8 @@ typedef enum {
   RF_ERR_WORKSPACE = 3,       /* workspace missing or too small             */
   RF_ERR_CUDA = 4,            /* a CUDA runtime call or launch failed       */
   RF_ERR_DEVICE_TIMEOUT = 5,  /* a kernel's bounded wait ran out            */
-  RF_ERR_DEVICE_INPUT = 6     /* device-resident sizes were inconsistent    */
+  RF_ERR_DEVICE_INPUT = 6,    /* device-resident sizes were inconsistent    */
+  RF_ERR_DEVICE_LAYOUT = 7    /* a kernel's shared memory was misaligned    */
 } rf_status;
 
 typedef enum { RF_F32 = 0, RF_BF16 = 1 } rf_dtype;
@@ -68,8 +69,11 @@ int rf_version(void);
  * up on a bounded wait and returned early; its outputs are incomplete),
  * RF_ERR_DEVICE_INPUT (a kernel found device-resident sizes, such as the
  * cumulative sequence lengths of rf_attn_fwd_varlen, inconsistent with the
- * host-side sizes; it skipped that work and wrote nothing out of bounds) or
- * RF_ERR_CUDA (the synchronisation itself failed).
+ * host-side sizes; it skipped that work and wrote nothing out of bounds),
+ * RF_ERR_DEVICE_LAYOUT (a kernel found its dynamic shared memory not aligned
+ * as its swizzled tiles need; it did no work) or RF_ERR_CUDA (the
+ * synchronisation itself failed).  When several kinds occurred, the first
+ * of TIMEOUT, LAYOUT, INPUT in that order is returned.
  */
 rf_status rf_get_device_status(rf_stream_t stream);
 
@@ -200,8 +204,11 @@ rf_status rf_attn_decode_splitkv(const void* Q, const void* K, const void* V, vo
  *     RF_DECODE_NOALLOC_SCRATCH_BYTES (lower num_splits, or use
  *     rf_attn_decode_splitkv with a caller workspace).
  *   - The first call on a device looks up the scratch's device address (one
- *     cudaGetSymbolAddress with that device current) and caches it; make
- *     that first call before any stream capture on the device.
+ *     cudaGetSymbolAddress with that device current) and caches it with the
+ *     device's current CUDA context; make that first call before any stream
+ *     capture on the device.  After a device reset the runtime creates a new
+ *     context, and the next call looks the address up again (so, again,
+ *     before any capture).
  *   - All calls on a device share the one scratch, which keeps the last
  *     call's contents (nothing in it needs to start at zero).  Calls that
  *     may overlap on the GPU -- on different streams without ordering, or
@@ -275,34 +282,60 @@ rf_status rf_mla_decode(const void* Q, const void* CKV, void* O, int B, int Hq, 
 rf_status rf_moe_gate_topk_softmax(const void* X, const void* Wg, int T, int D, int E, int k,
                                    int32_t* idx, float* w, rf_stream_t stream);
 
-/* Workspace bytes rf_absmax_fp8_gemm needs (0 for an invalid shape). */
+/*
+ * Workspace bytes rf_absmax_fp8_gemm needs when neither sx_out nor xq_out is
+ * given (0 for an invalid shape).  With both outputs given it needs only the
+ * row counters at the start of this size: 4 * (1 + ceil(M / 128)) bytes,
+ * rounded up to 256.
+ */
 size_t rf_absmax_fp8_gemm_workspace_size(int M, int N, int K);
 
 /*
  * Dynamic FP8 quantised GEMM ([E] §4.3), read per row of X:
  *   sx[m]    = fp32(max_k |X[m,k]| / 448)                     (row absmax)
  *   Xq[m,k]  = E4M3(fp32(X[m,k] / sx[m])), round-to-nearest-even,
- *              saturating to +-448; rows with sx = 0 give code 0x00
+ *              saturating to +-448; rows with sx = 0 give code 0x00, and a
+ *              negative value that rounds to zero gives 0x80
  *   Y[m,n]   = bf16( (sum_k Xq[m,k] * Wq[n,k]) * sx[m] * sw[n] )
  * The division is an IEEE fp32 division; the sum is accumulated in fp32 on
  * the tensor cores (tcgen05 kind::f8f6f4); Y is rounded to nearest even.
- * Kernel 1 reads each row of X once (absmax and quantisation from
- * registers); kernel 2 is the FP8 GEMM with the dequantising epilogue.
+ * One persistent kernel does both stages: quantiser warps read each row of X
+ * once (absmax and quantisation from registers), and the GEMM of a 128-row
+ * block of X starts as soon as that block's codes are written.
  *   X       [M][K] bf16.
  *   Wq      [N][K] uint8 E4M3 codes (pre-quantised weight; K contiguous).
  *   sw      [N] fp32 per-output-column weight scales.
  *   Y       [M][N] bf16 out.
  *   sx_out  [M] fp32 out, or NULL (then kept in the workspace).
  *   xq_out  [M][K] uint8 out, or NULL (then kept in the workspace).
- *   workspace  device buffer of rf_absmax_fp8_gemm_workspace_size(M,N,K)
- *              bytes, 16-byte aligned; may be NULL with 0 bytes when both
- *              sx_out and xq_out are given.
+ *   workspace  device buffer, 16-byte aligned, always required: the
+ *              kernel's row counters (reset by the call itself, with a
+ *              memset on `stream`), plus the codes and scales the caller
+ *              does not keep.  rf_absmax_fp8_gemm_workspace_size(M,N,K)
+ *              bytes always suffice.  Calls that overlap on the GPU must
+ *              not share a workspace.
  *   Sizes   M, N >= 1; K >= 16 with K % 16 == 0.
- * Errors: RF_ERR_INVALID_ARG, RF_ERR_WORKSPACE, RF_ERR_CUDA.
+ * Errors: RF_ERR_INVALID_ARG, RF_ERR_WORKSPACE (missing, misaligned or too
+ * small), RF_ERR_CUDA.
  */
 rf_status rf_absmax_fp8_gemm(const void* X, const uint8_t* Wq, const float* sw, void* Y,
                              int M, int N, int K, float* sx_out, uint8_t* xq_out,
                              void* workspace, size_t workspace_bytes, rf_stream_t stream);
+
+/*
+ * The first two steps of the FP8 cascade alone ([E] §4.3): row absmax and
+ * E4M3 quantisation, with the same arithmetic and bits as
+ * rf_absmax_fp8_gemm (sx[m] = fp32(max_k |X[m,k]| / 448), Xq = E4M3(fp32(X /
+ * sx)) round-to-nearest-even, satfinite, signed zero kept).  Used, for
+ * example, to quantise a weight per output column (rows of Wq [N][K]).
+ *   X       [M][K] bf16.
+ *   sx_out  [M] fp32 out.
+ *   xq_out  [M][K] uint8 E4M3 codes out.
+ *   Sizes   M >= 1; K >= 16 with K % 16 == 0.
+ * Errors: RF_ERR_INVALID_ARG, RF_ERR_CUDA.
+ */
+rf_status rf_absmax_quant_fp8(const void* X, int M, int K, float* sx_out, uint8_t* xq_out,
+                              rf_stream_t stream);
 
 /*
  * Failure-detection self-test (no counterpart in the paper).  Launches one

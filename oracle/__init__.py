@@ -4,7 +4,7 @@ TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` may import this package.  The CUDA library
 never calls it, and it shares no code with the CUDA path: the only module
 both sides use is the seeded input generator
-(``cascaded_reductions_loop_gb300.inputs``), which holds none of the method's
+(``workloads``, at the repository root), which holds none of the method's
 arithmetic.
 
 Each cascade is computed the plain, unfused way: every reduction is a

@@ -75,3 +75,56 @@ def assert_fp8_y_close(got, ref, what=""):
     bad = np.abs(got - ref) > bound
     assert not bad.any(), f"{what}: {bad.sum()} elements outside tolerance"
     assert rel_l2(got, ref) <= FP8_Y_REL_L2, f"{what}: rel-L2 {rel_l2(got, ref):.3e}"
+
+
+# ------------------------------------------------------------------ FP8 weight
+
+def fp8_weight_gpu(rf, w):
+    """The pre-quantised weight as the CUDA path makes it: the library's own
+    per-row absmax quantiser (rf_absmax_quant_fp8) applied to W [N, K].
+    Returns device tensors (wq uint8 [N, K], sw fp32 [N])."""
+    w = w.cuda()
+    N, K = w.shape
+    sw = torch.empty(N, dtype=torch.float32, device="cuda")
+    wq = torch.empty(N, K, dtype=torch.uint8, device="cuda")
+    rf.rf_absmax_quant_fp8(w, sw, wq)
+    return wq, sw
+
+
+def fp8_weight_oracle(w):
+    """The same weight as the oracle makes it (row_scale, then quantise):
+    (wq uint8 [N, K], sw fp32 [N]) numpy arrays."""
+    from oracle import fp8_quant_gemm as F
+    _, sw = F.row_scale(w)
+    return F.quantise(w, sw), sw
+
+
+# ------------------------------------------------------------------ guard bytes
+
+GUARD_FRONT = 256      # keeps the tensor 256-byte aligned
+GUARD_BACK = 4096
+GUARD_BYTE = 0xA5
+
+
+class Guarded:
+    """A device output tensor with guard bytes of a known pattern in front of
+    and behind it.  ``check()`` asserts that the kernel wrote nothing outside
+    the tensor (the out-of-bounds-write detector of the ragged parity cases)."""
+
+    def __init__(self, shape, dtype, fill=None):
+        n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        self.n = n
+        self.raw = torch.full((GUARD_FRONT + n + GUARD_BACK,), GUARD_BYTE, dtype=torch.uint8,
+                              device="cuda")
+        self.t = self.raw[GUARD_FRONT:GUARD_FRONT + n].view(dtype).view(shape)
+        if fill is None:
+            fill = float("nan") if dtype.is_floating_point else 0x7F
+        self.t.fill_(fill)
+
+    def check(self, what=""):
+        front = self.raw[:GUARD_FRONT]
+        back = self.raw[GUARD_FRONT + self.n:]
+        bad_f = int((front != GUARD_BYTE).sum().item())
+        bad_b = int((back != GUARD_BYTE).sum().item())
+        assert bad_f == 0 and bad_b == 0, \
+            f"{what}: {bad_f} guard bytes before and {bad_b} after the output were overwritten"

@@ -42,8 +42,9 @@ def test_library_exports_every_declared_symbol(rf):
 
 def test_status_strings(rf):
     assert rf.rf_status_string(0) == "RF_OK"
-    for s in range(1, 6):
+    for s in range(1, 8):
         assert rf.rf_status_string(s).startswith("RF_ERR_")
+    assert "aligned" in rf.rf_status_string(rf.RF_ERR_DEVICE_LAYOUT)
     assert "unknown" in rf.rf_status_string(99)
     assert rf.rf_version() >= 10000
 
@@ -119,7 +120,16 @@ def test_validation_rejects_bad_arguments_without_a_gpu(rf):
     # FP8: K not a multiple of 16, missing workspace
     assert L.rf_absmax_fp8_gemm(p, p, p, p, 16, 16, 40, p, p, null, 0, None) == rf.RF_ERR_INVALID_ARG
     assert L.rf_absmax_fp8_gemm(p, p, p, p, 16, 16, 64, null, null, null, 0, None) == rf.RF_ERR_WORKSPACE
-    assert rf.rf_absmax_fp8_gemm_workspace_size(16, 16, 64) == 16 * 64 + 16 * 4
+    # the workspace is always needed (row counters), even with both outputs given
+    assert L.rf_absmax_fp8_gemm(p, p, p, p, 16, 16, 64, p, p, null, 0, None) == rf.RF_ERR_WORKSPACE
+    assert L.rf_absmax_fp8_gemm(p, p, p, p, 16, 16, 64, p, p, p, 255, None) == rf.RF_ERR_WORKSPACE
+    # counters (1 + ceil(16 / 128) words, padded to 256) + codes (padded to 256) + scales
+    assert rf.rf_absmax_fp8_gemm_workspace_size(16, 16, 64) == 256 + 1024 + 16 * 4
+    assert rf.rf_absmax_fp8_gemm_workspace_size(300, 16, 64) == 256 + 19200 + 300 * 4
+    # standalone quantiser: K not a multiple of 16, null outputs
+    assert L.rf_absmax_quant_fp8(p, 16, 40, p, p, None) == rf.RF_ERR_INVALID_ARG
+    assert L.rf_absmax_quant_fp8(p, 16, 64, null, p, None) == rf.RF_ERR_INVALID_ARG
+    assert L.rf_absmax_quant_fp8(p, 0, 64, p, p, None) == rf.RF_ERR_INVALID_ARG
     assert rf.rf_absmax_fp8_gemm_workspace_size(16, 16, 40) == 0
     # self-test: out-of-range limit
     assert L.rf_selftest_wait_timeout(0, None) == rf.RF_ERR_INVALID_ARG

@@ -6,9 +6,9 @@ import numpy as np
 import pytest
 import torch
 
-from cascaded_reductions_loop_gb300 import inputs as I
+import workloads as I
 from oracle import attention as A
-from tests.helpers import assert_bf16_close, assert_f32_close, to64
+from tests.helpers import Guarded, assert_bf16_close, assert_f32_close, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -21,11 +21,13 @@ def rf():
 
 
 def _run(rf, q, k, v, scale, causal=0):
+    """One call with guard bytes around the (NaN-filled) output."""
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
-    o = torch.full_like(qd, float("nan"))
-    rf.rf_attn_fwd(qd, kd, vd, o, scale, causal)
+    o = Guarded(tuple(qd.shape), qd.dtype)
+    rf.rf_attn_fwd(qd, kd, vd, o.t, scale, causal)
     assert rf.rf_get_device_status() == rf.RF_OK
-    return o.cpu()
+    o.check("attention output")
+    return o.t.cpu()
 
 
 def test_tiny_fp32_workload(rf):
@@ -140,10 +142,11 @@ def test_bf16_two_pass(rf, shape, causal):
     sh = I.AttnShape(B, H, H, Lq, Lk, d, "bf16", seed=500 + Lq + Lk + causal)
     q, k, v = I.attention_inputs(sh)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
-    o = torch.full_like(qd, float("nan"))
-    rf.rf_attn_fwd_ex(qd, kd, vd, o, sh.scale, causal, rf.RF_ATTN_TWO_PASS)
+    o = Guarded(tuple(qd.shape), qd.dtype)
+    rf.rf_attn_fwd_ex(qd, kd, vd, o.t, sh.scale, causal, rf.RF_ATTN_TWO_PASS)
     assert rf.rf_get_device_status() == rf.RF_OK
-    assert_bf16_close(o.cpu(), A.attention(q, k, v, sh.scale, causal=bool(causal)),
+    o.check("two-pass output")
+    assert_bf16_close(o.t.cpu(), A.attention(q, k, v, sh.scale, causal=bool(causal)),
                       f"two-pass {shape} causal={causal}")
 
 
@@ -151,12 +154,11 @@ def test_two_pass_short_workloads_and_mode_errors(rf):
     for sh in (I.SHORT_PREFILL_256, I.SHORT_PREFILL_128):
         q, k, v = I.attention_inputs(sh)
         for mode in (rf.RF_ATTN_INCREMENTAL, rf.RF_ATTN_TWO_PASS):
-            o = torch.full_like(q, float("nan"), device="cuda")
-            rf.rf_attn_fwd_ex(q.cuda(), k.cuda(), v.cuda(), o, sh.scale, 0, mode)
+            o = Guarded(tuple(q.shape), q.dtype)
+            rf.rf_attn_fwd_ex(q.cuda(), k.cuda(), v.cuda(), o.t, sh.scale, 0, mode)
             assert rf.rf_get_device_status() == rf.RF_OK
-            rows = [(b, h, i) for b in (0, sh.B - 1) for h in (0, sh.Hq - 1) for i in range(sh.Lq)]
-            got = torch.stack([o[b, h, i].cpu() for b, h, i in rows])
-            assert_bf16_close(got, A.attention(q, k, v, sh.scale, rows=rows), f"mode {mode}")
+            o.check(f"mode {mode} output")
+            assert_bf16_close(o.t.cpu(), A.attention(q, k, v, sh.scale), f"mode {mode}")
     x = torch.zeros(1, 1, 64, 64, device="cuda", dtype=torch.bfloat16)
     kk = torch.zeros(1, 1, 300, 64, device="cuda", dtype=torch.bfloat16)
     with pytest.raises(rf.RFError):                     # two-pass needs Lk <= 256

@@ -1,12 +1,11 @@
 """GPU parity: multi-segment split-KV decode attention (partial + merge
 kernels) against the fp64 three-pass oracle, through the C ABI."""
-import numpy as np
 import pytest
 import torch
 
-from cascaded_reductions_loop_gb300 import inputs as I
+import workloads as I
 from oracle import attention as A
-from tests.helpers import assert_bf16_close
+from tests.helpers import Guarded, assert_bf16_close
 
 pytestmark = pytest.mark.gpu
 
@@ -19,22 +18,26 @@ def rf():
 
 
 def _run(rf, q, k, v, scale, num_splits=0):
+    """One call with guard bytes around the output and the workspace."""
     B, Hq, d = q.shape
     Hkv, Lk = k.shape[1], k.shape[2]
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
-    o = torch.full_like(qd, float("nan"))
+    o = Guarded((B, Hq, d), torch.bfloat16)
     nbytes = rf.rf_attn_decode_splitkv_workspace_size(B, Hq, Hkv, Lk, d, num_splits)
     assert nbytes > 0
-    ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device="cuda")   # NaN-filled partials
-    rf.rf_attn_decode_splitkv(qd, kd, vd, o, scale, ws, num_splits)
+    ws = Guarded((nbytes,), torch.uint8, fill=0xFF)                    # NaN-filled partials
+    rf.rf_attn_decode_splitkv(qd, kd, vd, o.t, scale, ws.t, num_splits)
     assert rf.rf_get_device_status() == rf.RF_OK
-    return o.cpu()
+    o.check("decode output")
+    ws.check("decode workspace")
+    return o.t.cpu()
 
 
 @pytest.mark.parametrize("B,Hq,Hkv,Lk,splits", [
     (2, 8, 2, 300, 0), (2, 8, 2, 300, 1), (2, 8, 2, 300, 3), (2, 8, 2, 300, 7),
     (1, 4, 4, 77, 5), (1, 8, 4, 1000, 0), (3, 8, 1, 513, 2), (1, 32, 8, 1, 0),
-    (1, 32, 8, 31, 1), (2, 16, 4, 4096, 16), (1, 4, 1, 300, 300)])
+    (1, 32, 8, 31, 1), (2, 16, 4, 4096, 16), (1, 4, 1, 300, 300), (5, 24, 3, 2049, 0),
+    (1, 16, 2, 129, 4)])
 def test_decode_small(rf, B, Hq, Hkv, Lk, splits):
     sh = I.AttnShape(B, Hq, Hkv, 1, Lk, 128, "bf16", seed=1000 + Lk + splits)
     q, k, v = I.decode_inputs(sh)
@@ -49,17 +52,12 @@ def test_decode_2k_full(rf):
     assert_bf16_close(o, A.decode_attention(q, k, v, s.scale), "decode 2k")
 
 
-def test_decode_32k_sampled(rf):
+def test_decode_32k_full(rf):
+    """The 32768-key workload: every one of the 1024 (batch, head) rows."""
     s = I.DECODE_32K
     q, k, v = I.decode_inputs(s)
     o = _run(rf, q, k, v, s.scale)
-    rng = np.random.default_rng(0)
-    rows = [(int(b), int(h)) for b, h in zip(rng.integers(0, s.B, 48), rng.integers(0, s.Hq, 48))]
-    rows += [(0, 0), (s.B - 1, s.Hq - 1)]
-    ref = A.decode_attention(q, k, v, s.scale, rows=rows)
-    got = torch.stack([o[b, h] for b, h in rows])
-    assert_bf16_close(got, ref, "decode 32k sampled")
-    assert torch.isfinite(o.float()).all()
+    assert_bf16_close(o, A.decode_attention(q, k, v, s.scale), "decode 32k")
 
 
 def test_segment_count_does_not_change_the_result_much(rf):

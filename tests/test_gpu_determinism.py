@@ -8,7 +8,8 @@ a call whose bits differ."""
 import pytest
 import torch
 
-from cascaded_reductions_loop_gb300 import inputs as I
+import workloads as I
+from tests.helpers import fp8_weight_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -58,13 +59,14 @@ def _calls(rf):
     calls.append(("moe", moe))
 
     f = I.FP8Shape(M=1024, N=2048, K=4096, seed=74)
-    X, Wq, sw = (t.cuda() for t in I.fp8_inputs(f))
+    X, W = (t.cuda() for t in I.fp8_inputs(f))
+    Wq, sw = fp8_weight_gpu(rf, W)
     wsf = torch.empty(rf.rf_absmax_fp8_gemm_workspace_size(f.M, f.N, f.K), dtype=torch.uint8,
                       device="cuda")
 
     def fp8():
         y = torch.empty(f.M, f.N, dtype=torch.bfloat16, device="cuda")
-        rf.rf_absmax_fp8_gemm(X, Wq, sw, y, workspace=wsf)
+        rf.rf_absmax_fp8_gemm(X, Wq, sw, y, wsf)
         return [y]
     calls.append(("fp8", fp8))
     return calls

@@ -6,7 +6,8 @@ become graph nodes and edges.)"""
 import pytest
 import torch
 
-from cascaded_reductions_loop_gb300 import inputs as I
+import workloads as I
+from tests.helpers import fp8_weight_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -60,11 +61,12 @@ def _paths(rf):
     paths.append(("moe", [idx, wt], lambda: rf.rf_moe_gate_topk_softmax(x, w, m.k, idx, wt)))
 
     fs = I.FP8Shape(M=512, N=1024, K=2048, seed=86)
-    X, Wq, sw = (t.cuda() for t in I.fp8_inputs(fs))
+    X, W = (t.cuda() for t in I.fp8_inputs(fs))
+    Wq, sw = fp8_weight_gpu(rf, W)
     wsf = torch.empty(rf.rf_absmax_fp8_gemm_workspace_size(fs.M, fs.N, fs.K), dtype=torch.uint8,
                       device="cuda")
     y = torch.empty(fs.M, fs.N, dtype=torch.bfloat16, device="cuda")
-    paths.append(("fp8", [y], lambda: rf.rf_absmax_fp8_gemm(X, Wq, sw, y, workspace=wsf)))
+    paths.append(("fp8", [y], lambda: rf.rf_absmax_fp8_gemm(X, Wq, sw, y, wsf)))
 
     ml = I.MLAShape(B=2, Hq=128, Lk=700, seed=87)
     qm, cm = (t.cuda() for t in I.mla_inputs(ml))

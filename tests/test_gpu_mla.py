@@ -1,13 +1,12 @@
 """GPU parity: latent-KV (multi-latent attention) decode -- the two-CTA
 kernel that exchanges partial scores, and the segment merge -- against the
 fp64 oracle, through the C ABI."""
-import numpy as np
 import pytest
 import torch
 
-from cascaded_reductions_loop_gb300 import inputs as I
+import workloads as I
 from oracle import attention as A
-from tests.helpers import assert_bf16_close, assert_bf16_close_scaled
+from tests.helpers import Guarded, assert_bf16_close, assert_bf16_close_scaled
 
 pytestmark = pytest.mark.gpu
 
@@ -20,15 +19,19 @@ def rf():
 
 
 def _run(rf, q, ckv, scale, num_splits=0):
+    """One call with guard bytes around the output and the workspace."""
     B, Hq, _ = q.shape
     Lk = ckv.shape[1]
     qd, cd = q.cuda(), ckv.cuda()
-    o = torch.full((B, Hq, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    o = Guarded((B, Hq, 512), torch.bfloat16)
     nbytes = rf.rf_mla_decode_workspace_size(B, Hq, Lk, 576, 512, num_splits)
-    ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device="cuda") if nbytes else None
-    rf.rf_mla_decode(qd, cd, o, scale, ws, num_splits)
+    ws = Guarded((nbytes,), torch.uint8, fill=0xFF) if nbytes else None
+    rf.rf_mla_decode(qd, cd, o.t, scale, None if ws is None else ws.t, num_splits)
     assert rf.rf_get_device_status() == rf.RF_OK
-    return o.cpu()
+    o.check("mla output")
+    if ws is not None:
+        ws.check("mla workspace")
+    return o.t.cpu()
 
 
 @pytest.mark.parametrize("B,Hq,Lk,splits", [
@@ -72,35 +75,23 @@ def test_mla_one_dominant_row_late(rf):
     assert_bf16_close(o, A.mla_decode(q, c, sh.scale, 512), "dominant row")
 
 
-def test_mla_decode_full_sampled(rf):
+def test_mla_decode_full(rf):
     """The full workload in the launch configuration the benchmark times
-    (automatic segment count), on sampled (batch, head) rows; every output
-    element is written."""
+    (automatic segment count): every (batch, head) row."""
     s = I.MLA_DECODE
     q, c = I.mla_inputs(s)
     o = _run(rf, q, c, s.scale)
-    assert not torch.isnan(o.float()).any()
-    rng = np.random.default_rng(0)
-    rows = [(int(b), int(h)) for b, h in zip(rng.integers(0, s.B, 48), rng.integers(0, s.Hq, 48))]
-    rows += [(0, 0), (0, s.Hq - 1), (s.B - 1, 0), (s.B - 1, s.Hq - 1)]
-    ref = A.mla_decode(q, c, s.scale, 512, rows=rows)
-    got = torch.stack([o[b, h] for b, h in rows])
-    assert_bf16_close(got, ref, "mla full")
+    assert_bf16_close(o, A.mla_decode(q, c, s.scale, 512), "mla full")
 
 
-def test_mla_long_context_split_sampled(rf):
+def test_mla_long_context_split(rf):
     """Few batches over a long cache: the automatic choice cuts every batch
-    into several segments, merged by the second kernel."""
+    into several segments, merged by the second kernel; every row checked."""
     s = I.MLAShape(B=8, Hq=128, Lk=32768, seed=33)
     assert rf.rf_mla_decode_num_splits(s.B, s.Hq, s.Lk, 576, 512, 0) > 1
     q, c = I.mla_inputs(s)
     o = _run(rf, q, c, s.scale)
-    assert not torch.isnan(o.float()).any()
-    rng = np.random.default_rng(1)
-    rows = [(int(b), int(h)) for b, h in zip(rng.integers(0, s.B, 24), rng.integers(0, s.Hq, 24))]
-    ref = A.mla_decode(q, c, s.scale, 512, rows=rows)
-    got = torch.stack([o[b, h] for b, h in rows])
-    assert_bf16_close(got, ref, "mla long")
+    assert_bf16_close(o, A.mla_decode(q, c, s.scale, 512), "mla long")
 
 
 def test_mla_repeatable(rf):

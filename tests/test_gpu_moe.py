@@ -4,9 +4,9 @@ import numpy as np
 import pytest
 import torch
 
-from cascaded_reductions_loop_gb300 import inputs as I
+import workloads as I
 from oracle import moe_gate as G
-from tests.helpers import MOE_W_ABS
+from tests.helpers import Guarded, MOE_W_ABS
 
 pytestmark = pytest.mark.gpu
 
@@ -20,11 +20,13 @@ def rf():
 
 def _run(rf, x, w, k):
     T = x.shape[0]
-    idx = torch.full((T, k), -1, dtype=torch.int32, device="cuda")
-    wts = torch.full((T, k), float("nan"), dtype=torch.float32, device="cuda")
-    rf.rf_moe_gate_topk_softmax(x.cuda(), w.cuda(), k, idx, wts)
+    idx = Guarded((T, k), torch.int32, fill=-1)
+    wts = Guarded((T, k), torch.float32)
+    rf.rf_moe_gate_topk_softmax(x.cuda(), w.cuda(), k, idx.t, wts.t)
     assert rf.rf_get_device_status() == rf.RF_OK
-    return idx.cpu().numpy(), wts.cpu().numpy()
+    idx.check("expert indices")
+    wts.check("expert weights")
+    return idx.t.cpu().numpy(), wts.t.cpu().numpy()
 
 
 def _check(x, w, k, idx, wts, what):

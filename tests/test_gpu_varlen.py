@@ -5,9 +5,9 @@ import numpy as np
 import pytest
 import torch
 
-from cascaded_reductions_loop_gb300 import inputs as I
+import workloads as I
 from oracle import attention as A
-from tests.helpers import assert_bf16_close, assert_f32_close
+from tests.helpers import Guarded, assert_bf16_close, assert_f32_close
 
 pytestmark = pytest.mark.gpu
 
@@ -35,11 +35,12 @@ def _inputs(lens_q, lens_k, H, d, dtype, seed):
 
 
 def _run(rf, q, k, v, cu_q, cu_k, max_q, scale, causal):
-    o = torch.full(q.shape, float("nan"), dtype=q.dtype, device="cuda")
-    rf.rf_attn_fwd_varlen(q.cuda(), k.cuda(), v.cuda(), o, cu_q.cuda(), cu_k.cuda(), max_q, scale,
+    o = Guarded(tuple(q.shape), q.dtype)
+    rf.rf_attn_fwd_varlen(q.cuda(), k.cuda(), v.cuda(), o.t, cu_q.cuda(), cu_k.cuda(), max_q, scale,
                           causal)
     assert rf.rf_get_device_status() == rf.RF_OK
-    return o.cpu()
+    o.check("varlen output")
+    return o.t.cpu()
 
 
 @pytest.mark.parametrize("causal", [0, 1])

@@ -1,9 +1,8 @@
 """The seeded input generators: shapes, dtypes, determinism and the value
-sets the workloads promise (integers in {-2..2}, ~1% outliers, E4M3 codes
-without NaN)."""
+sets the workloads promise (integers in {-2..2}, ~1% outliers)."""
 import torch
 
-from cascaded_reductions_loop_gb300 import inputs as I
+import workloads as I
 
 
 def test_attention_shapes_and_determinism():
@@ -25,9 +24,11 @@ def test_moe_values_are_small_integers():
 
 
 def test_fp8_inputs():
-    x, wq, sw = I.fp8_inputs(I.FP8Shape(M=256, N=64, K=512, seed=2))
-    assert x.dtype == torch.bfloat16 and wq.dtype == torch.uint8 and sw.dtype == torch.float32
+    x, w = I.fp8_inputs(I.FP8Shape(M=256, N=64, K=512, seed=2))
+    assert x.dtype == torch.bfloat16 and w.dtype == torch.bfloat16
+    assert x.shape == (256, 512) and w.shape == (64, 512)
     frac = (x.float().abs() > 6).float().mean().item()      # outliers (|N(0,1)| > 6 is ~2e-9)
     assert 0.004 < frac < 0.012
-    assert not ((wq & 0x7F) == 0x7F).any()                  # no NaN codes
-    assert (((wq & 0x7F) == 0x7E).sum(dim=1) >= 1).all()    # every column reaches +-448
+    assert (w.float().abs() < 7).all()                      # the weight has no outliers
+    x2, w2 = I.fp8_inputs(I.FP8Shape(M=256, N=64, K=512, seed=2))
+    assert torch.equal(x, x2) and torch.equal(w, w2)

@@ -1,17 +1,20 @@
 """rf_attn_decode_splitkv_noalloc: the split-KV decode for callers that cannot
 give the library device memory (its partial states live in a scratch array
-built into the library).  Through the C ABI, its output must match the
-workspace-taking rf_attn_decode_splitkv on consecutive calls, whatever the
-previous call left in the shared scratch; requests whose partial states do
-not fit the scratch are refused with RF_ERR_WORKSPACE.
+built into the library).  Through the C ABI, on consecutive calls (whatever
+the previous call left in the shared scratch), its output must equal the
+workspace-taking rf_attn_decode_splitkv bit for bit (same kernels, same
+segments, only the scratch memory differs) and match the fp64 oracle within
+the decode tolerance; requests whose partial states do not fit the scratch
+are refused with RF_ERR_WORKSPACE.
 
 This file is collected last on purpose, and it sets up everything it needs
 itself, so it passes both alone in a fresh process and after the others."""
 import pytest
 import torch
 
-from cascaded_reductions_loop_gb300 import inputs as I
-from tests.helpers import assert_bf16_close
+import workloads as I
+from oracle import attention as A
+from tests.helpers import Guarded, assert_bf16_close
 
 pytestmark = pytest.mark.gpu
 
@@ -31,14 +34,19 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
 
     cases = [(I.AttnShape(4, 32, 8, 1, 3000, 128, "bf16", seed=501), 0),
              (I.AttnShape(2, 16, 2, 1, 777, 128, "bf16", seed=502), 5),
+             (I.AttnShape(3, 8, 8, 1, 1, 128, "bf16", seed=504), 0),
              (I.AttnShape(4, 32, 8, 1, 3000, 128, "bf16", seed=503), 0)]
     for sh, splits in cases:          # consecutive calls share (and overwrite) the scratch
-        q, k, v = (t.cuda() for t in I.decode_inputs(sh))
-        o = torch.full_like(q, float("nan"))
-        rf.rf_attn_decode_splitkv_noalloc(q, k, v, o, sh.scale, splits)
+        q_h, k_h, v_h = I.decode_inputs(sh)
+        q, k, v = q_h.cuda(), k_h.cuda(), v_h.cuda()
+        o = Guarded(tuple(q.shape), torch.bfloat16)
+        rf.rf_attn_decode_splitkv_noalloc(q, k, v, o.t, sh.scale, splits)
         ref = _reference(rf, q, k, v, sh.scale, splits)
         assert rf.rf_get_device_status() == rf.RF_OK
-        assert_bf16_close(o.cpu(), ref.cpu(), f"noalloc vs workspace {sh.B}x{sh.Hq}x{sh.Lk}")
+        o.check("noalloc output")
+        what = f"noalloc {sh.B}x{sh.Hq}x{sh.Lk} splits={splits}"
+        assert torch.equal(o.t, ref), f"{what}: differs from the workspace entry point"
+        assert_bf16_close(o.t.cpu(), A.decode_attention(q_h, k_h, v_h, sh.scale), what)
 
 
 def test_noalloc_refuses_requests_beyond_its_scratch():

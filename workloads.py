@@ -1,9 +1,10 @@
 """Seeded synthetic inputs for the fused cascaded-reduction kernels.
 
-This module is shared by the CUDA path (bench, GPU tests) and the CPU oracle.
-It holds random draws, dtype casts and the workload shapes only: no step of
-the cascades themselves (no max, no exp, no softmax, no top-k, no absmax of X,
-no GEMM).  Every tensor is a CPU tensor; callers move it where they need it.
+This module is shared by the CUDA path (bench, GPU tests) and the CPU oracle;
+it imports neither.  It holds random draws, dtype casts and the workload
+shapes only: no step of the cascades themselves (no max, no exp, no softmax,
+no top-k, no absmax, no quantisation, no GEMM).  Every tensor is a CPU
+tensor; callers move it where they need it.
 
 Recipes (one per workload; shapes are those of the five workloads the kernels
 are built for):
@@ -18,11 +19,12 @@ are built for):
   to bf16 (exact).  W_gate is stored expert-major, [E][D] (the layout of a
   linear layer's weight), so that both GEMM operands are contiguous along D.
 * FP8 GEMM: X ~ N(0, 1) with an i.i.d. Bernoulli(0.01) outlier mask whose
-  entries are multiplied by 20, cast to bf16.  W ~ N(0, 1) stored [N][K]
-  (each output column's K weights contiguous); the pre-quantised weight is
-  made here with the library's float8_e4m3fn cast of W / sw, where
-  sw[n] = max_k |W[n, k]| / 448 in fp32.  This preparation of the weight
-  input is not part of the fused path: the path receives Wq and sw as given.
+  entries are multiplied by 20, cast to bf16.  W ~ N(0, 1) cast to bf16,
+  stored [N][K] (each output column's K weights contiguous).  The fused path
+  takes W pre-quantised (E4M3 codes with one fp32 scale per output column);
+  each side makes that from W with its own per-row absmax quantiser (the
+  library's rf_absmax_quant_fp8, the oracle's row_scale and quantise), and
+  the tests check that the two agree bit for bit.
 """
 from __future__ import annotations
 
@@ -30,9 +32,6 @@ import math
 from dataclasses import dataclass
 
 import torch
-
-E4M3_MAX = 448.0
-
 
 def _gen(seed: int) -> torch.Generator:
     g = torch.Generator(device="cpu")
@@ -201,12 +200,11 @@ def moe_inputs(shape: MoEShape):
 
 
 def fp8_inputs(shape: FP8Shape):
-    """X [M,K] bf16 with outliers; Wq [N,K] e4m3 codes as uint8; sw [N] fp32."""
+    """X [M,K] bf16 with outliers; W [N,K] bf16 ~ N(0, 1) (to be quantised
+    per row of this layout, i.e. per output column)."""
     g = _gen(shape.seed)
     x = _normal(g, (shape.M, shape.K))
     mask = torch.rand(shape.M, shape.K, generator=g) < shape.outlier_p
     x = torch.where(mask, x * shape.outlier_mult, x).to(torch.bfloat16).contiguous()
-    w = _normal(g, (shape.N, shape.K))
-    sw = (w.abs().amax(dim=1) / E4M3_MAX).to(torch.float32)
-    wq = (w / sw[:, None]).to(torch.float8_e4m3fn).view(torch.uint8).contiguous()
-    return x, wq, sw.contiguous()
+    w = _normal(g, (shape.N, shape.K)).to(torch.bfloat16).contiguous()
+    return x, w
