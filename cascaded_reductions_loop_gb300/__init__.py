@@ -19,7 +19,7 @@ import torch
 from . import _build
 
 __all__ = [
-    "RFError", "lib", "rf_status_string", "rf_version", "rf_get_device_status",
+    "RFError", "lib", "rf_status_string", "rf_version", "rf_get_device_status", "rf_last_cuda_error",
     "rf_attn_fwd", "rf_attn_fwd_ex", "rf_attn_fwd_varlen", "rf_attn_decode_splitkv",
     "rf_attn_decode_splitkv_num_splits",
     "rf_attn_decode_splitkv_workspace_size", "rf_attn_decode_splitkv_noalloc",
@@ -55,6 +55,7 @@ lib = _c.CDLL(LIB_PATH)
 
 _SIGS = {
     "rf_status_string": (_c.c_char_p, [_I]),
+    "rf_last_cuda_error": (_c.c_char_p, []),
     "rf_version": (_I, []),
     "rf_get_device_status": (_I, [_P]),
     "rf_attn_fwd": (_I, [_I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
@@ -82,7 +83,10 @@ for _name, (_res, _args) in _SIGS.items():
 class RFError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {rf_status_string(status)}")
+        msg = f"{where}: {rf_status_string(status)}"
+        if status == RF_ERR_CUDA:
+            msg += f" ({lib.rf_last_cuda_error().decode()})"
+        super().__init__(msg)
 
 
 def _check(status: int, where: str) -> None:
@@ -120,6 +124,10 @@ def rf_status_string(status: int) -> str:
 
 def rf_version() -> int:
     return lib.rf_version()
+
+
+def rf_last_cuda_error() -> str:
+    return lib.rf_last_cuda_error().decode()
 
 
 def rf_get_device_status(stream=None) -> int:

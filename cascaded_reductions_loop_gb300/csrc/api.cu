@@ -2,6 +2,7 @@
 // device-side error word, tensor-map encoding and the wait-timeout self-test.
 #include <cudaTypedefs.h>
 #include <math.h>
+#include <stdio.h>
 
 #include <mutex>
 
@@ -162,7 +163,14 @@ namespace {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool ptr_ok(const void* p) { return p != nullptr && aligned16(p); }
 
-rf_status from_cuda(cudaError_t e) { return e == cudaSuccess ? RF_OK : RF_ERR_CUDA; }
+thread_local char g_last_cuda_error[160] = "none";
+
+rf_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return RF_OK;
+  snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s", cudaGetErrorName(e),
+           cudaGetErrorString(e));
+  return RF_ERR_CUDA;
+}
 
 }  // namespace
 
@@ -185,6 +193,8 @@ const char* rf_status_string(int status) {
 }
 
 int rf_version(void) { return RF_VERSION_NUM; }
+
+const char* rf_last_cuda_error(void) { return g_last_cuda_error; }
 
 rf_status rf_get_device_status(rf_stream_t stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

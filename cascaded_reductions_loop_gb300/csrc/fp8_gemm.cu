@@ -8,15 +8,19 @@
 // The two stages therefore cooperate inside one persistent kernel
 // (fp8_gemm_kernel), at the granularity of 128-row blocks of X ([E] §3.3,
 // the inter-block level):
-//   * quantiser warps (four per CTA) take rows of X from a global counter in
-//     increasing order; one warp holds a whole row in registers, reduces |x|
+//   * quantiser warps (eight per CTA) take rows of X in increasing order, a
+//     batch of eight per CTA at a time from a global counter (the next batch
+//     is claimed while the current one is processed); one warp holds a whole
+//     row in registers, reduces |x|
 //     to the row max, sets sx = max / 448 (IEEE fp32 division), writes the
 //     E4M3 codes of the correctly rounded x / sx (cvt.rn.satfinite) and then
 //     counts the row into its 128-row block's readiness counter (release);
 //   * the GEMM part runs on CTA pairs (2-CTA clusters, tcgen05 cta_group::2):
-//     a pair computes a 256 x 256 output tile, each CTA loading with TMA its
-//     own 128 rows of the codes and its own 128 rows of Wq into its own
-//     shared memory; one thread of rank 0 issues the M = 256 MMAs
+//     a pair computes a 256 x 256 output tile (or, in the last round, a
+//     256 x 128 half tile, so that the leftover tiles spread over every
+//     pair), each CTA loading with TMA its own 128 rows of the codes and its
+//     own half of the tile's Wq rows into its own shared memory; one thread
+//     of rank 0 issues the M = 256 MMAs
 //     (kind::f8f6f4, E4M3 x E4M3 -> fp32 in tensor memory), so each SM reads
 //     only its half of the B tile from its shared memory.  A CTA's TMA
 //     producer waits (acquire) for its row block to be complete before it
@@ -207,17 +211,42 @@ constexpr int BN = 256;                          // output columns per pair tile
 constexpr int BK = 128;                          // bytes of K per stage = one 128-byte swizzle row
 constexpr int kStages = 6;
 constexpr int kABytes = BM * BK;                 // this CTA's 128 rows of codes
-constexpr int kBBytes = (BN / 2) * BK;           // this CTA's half of the B tile
+constexpr int kBBytes = (BN / 2) * BK;           // this CTA's half of the B tile (full tiles)
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kPairStageBytes = 2 * kStageBytes; // what lands on rank 0's barrier per stage
 constexpr int kEpiWarps = 4;
-constexpr int kFusedQuantWarps = 4;
+constexpr int kFusedQuantWarps = 8;
 constexpr int kFirstEpiWarp = 2, kFirstQuantWarp = kFirstEpiWarp + kEpiWarps;
-constexpr int kGemmThreads = 32 * (kFirstQuantWarp + kFusedQuantWarps);   // 320
+constexpr int kGemmThreads = 32 * (kFirstQuantWarp + kFusedQuantWarps);   // 448
 constexpr int kAccCols = BN;                     // one fp32 accumulator tile in TMEM
 constexpr int kTmemCols = 2 * kAccCols;          // two: epilogue of tile i overlaps tile i+1
 constexpr int kGemmSmem = kStages * kStageBytes + 1024 /*align*/ + 256 /*bars*/;
 constexpr uint32_t kIdescPair = make_idesc(2 * BM, BN, /*e4m3*/ 0, 0, 0);
+constexpr uint32_t kIdescPairHalf = make_idesc(2 * BM, BN / 2, /*e4m3*/ 0, 0, 0);
+
+// Output tile t of the schedule.  Tiles t < n_full are 256 x 256 tiles in
+// row-major order of the tile grid; the next n_half are 256 x 128 halves of
+// the remaining tiles (full tile n_full + h / 2, column half h % 2).
+struct Tile {
+  int m0;      // first output row of the pair
+  int n0;      // first output column
+  int ncols;   // 256 or 128
+};
+
+__device__ __forceinline__ Tile tile_of(int t, int tiles_n, int n_full) {
+  Tile w;
+  if (t < n_full) {
+    w.m0 = (t / tiles_n) * (2 * BM);
+    w.n0 = (t % tiles_n) * BN;
+    w.ncols = BN;
+  } else {
+    const int h = t - n_full, f = n_full + (h >> 1);
+    w.m0 = (f / tiles_n) * (2 * BM);
+    w.n0 = (f % tiles_n) * BN + (h & 1) * (BN / 2);
+    w.ncols = BN / 2;
+  }
+  return w;
+}
 static_assert(kStages * kStageBytes + 256 + 1024 <= 227 * 1024, "shared memory");
 
 struct GemmBars {
@@ -228,6 +257,7 @@ struct GemmBars {
   uint64_t drain;            // rank 0: every MMA has completed
   uint32_t tmem;
   int abort;
+  int qbase[2];              // first row of the quantisers' current / next batch
 };
 
 // Readiness of one 128-row block of codes: bounded wait (acquire) until all
@@ -252,17 +282,19 @@ __device__ __forceinline__ bool wait_rows_ready(const unsigned* ready, int m0, i
 //   warp 1     TMEM allocation (both CTAs); MMA issuer (rank 0, one thread)
 //   warps 2-5  epilogue (TMEM lane quarter = warp % 4)
 //   warps 6-9  quantisers
-// Pair tile p covers output rows 256 (p / tiles_n) .. + 255 (CTA r: + 128 r)
-// and columns 256 (p % tiles_n) .. + 255 (CTA r loads B rows + 128 r); cluster
-// c takes tiles c, c + nclusters, ...  Rank 0's MMA thread accumulates tile i
-// into TMEM buffer i % 2 of both CTAs while the epilogues drain buffer
-// (i - 1) % 2.  Counters (zeroed by the host before the launch): ctr[0] is
-// the next row to quantise, ctr[1 + b] the rows of block b done.
+// Tile t (tile_of) covers output rows m0 .. m0 + 255 (CTA r: + 128 r) and
+// columns n0 .. n0 + ncols - 1 (CTA r loads B rows n0 + r ncols / 2 ..,
+// through tmB for full tiles and tmBh, with boxes of 64 rows, for halves);
+// cluster c takes tiles c, c + nclusters, ...  Rank 0's MMA thread
+// accumulates tile i into TMEM buffer i % 2 of both CTAs while the epilogues
+// drain buffer (i - 1) % 2.  Counters (zeroed by the host before the launch):
+// ctr[0] is the next row to quantise, ctr[1 + b] the rows of block b done.
 __global__ void __launch_bounds__(kGemmThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const uint4* __restrict__ X, uint8_t* __restrict__ Xq, float* __restrict__ sx,
-                    const float* __restrict__ sw, __nv_bfloat16* __restrict__ Y, int M, int N,
-                    int K, int tiles_n, int num_pairs, unsigned* __restrict__ ctr, unsigned* err) {
+                    const __grid_constant__ CUtensorMap tmBh, const uint4* __restrict__ X,
+                    uint8_t* __restrict__ Xq, float* __restrict__ sx, const float* __restrict__ sw,
+                    __nv_bfloat16* __restrict__ Y, int M, int N, int K, int tiles_n, int n_full,
+                    int n_tiles, unsigned* __restrict__ ctr, unsigned* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -275,11 +307,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const bool leader = crank == 0;
   const int cid = (int)blockIdx.x >> 1, ncl = (int)gridDim.x >> 1;
   const int nk = (K + BK - 1) / BK;
-  const int my_tiles = num_pairs > cid ? (num_pairs - cid + ncl - 1) / ncl : 0;
+  const int my_tiles = n_tiles > cid ? (n_tiles - cid + ncl - 1) / ncl : 0;
 
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    prefetch_tmap(&tmBh);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(smem_u32(&bars->full[i]), 1);
       mbar_init(smem_u32(&bars->empty[i]), 1);
@@ -308,9 +341,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int it = 0;
       bool ok = true;
       for (int i = 0; ok && i < my_tiles && !*abort_flag; ++i) {
-        const int p = cid + i * ncl;
-        const int m0 = (p / tiles_n) * (2 * BM) + crank * BM;
-        const int nb0 = (p % tiles_n) * BN + crank * (BN / 2);
+        const Tile w = tile_of(cid + i * ncl, tiles_n, n_full);
+        const int m0 = w.m0 + crank * BM;
+        const int nb0 = w.n0 + crank * (w.ncols / 2);
+        const bool half = w.ncols != BN;
         if (!wait_rows_ready(ready, m0, M)) {
           ok = false;
           break;
@@ -328,9 +362,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           uint8_t* a = smem + slot * kStageBytes;
           const uint32_t full0 = mapa_shared(smem_u32(&bars->full[slot]), 0);
-          if (leader) mbar_arrive_expect_tx(smem_u32(&bars->full[slot]), kPairStageBytes);
+          if (leader)
+            mbar_arrive_expect_tx(smem_u32(&bars->full[slot]),
+                                  half ? 2 * (kABytes + kBBytes / 2) : kPairStageBytes);
           tma_load_2d_pair(smem_u32(a), &tmA, full0, kb * BK, m0);
-          tma_load_2d_pair(smem_u32(a + kABytes), &tmB, full0, kb * BK, nb0);
+          tma_load_2d_pair(smem_u32(a + kABytes), half ? &tmBh : &tmB, full0, kb * BK, nb0);
         }
       }
       if (!ok) {
@@ -357,6 +393,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         tc_fence_after();
         const uint32_t d = tmem + a * kAccCols;
+        const uint32_t idesc =
+            tile_of(cid + i * ncl, tiles_n, n_full).ncols == BN ? kIdescPair : kIdescPairHalf;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int slot = it % kStages;
           if (!mbar_wait_cluster(smem_u32(&bars->full[slot]), (uint32_t)((it / kStages) & 1)) ||
@@ -370,7 +408,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k)
             mma_f8_pair(d, sw128_desc(sa + k * 32, 1024, 16), sw128_desc(sb + k * 32, 1024, 16),
-                        kIdescPair, (kb | k) != 0);
+                        idesc, (kb | k) != 0);
           mma_commit_pair(smem_u32(&bars->empty[slot]));
           mma_commit_pair(mapa_shared(smem_u32(&bars->empty[slot]), 1));
         }
@@ -394,8 +432,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const bool vec_ok = (N % 8) == 0;
     for (int i = 0; i < my_tiles; ++i) {
       const int a = i & 1;
-      const int p = cid + i * ncl;
-      const int m0 = (p / tiles_n) * (2 * BM) + crank * BM, n0 = (p % tiles_n) * BN;
+      const Tile w = tile_of(cid + i * ncl, tiles_n, n_full);
+      const int m0 = w.m0 + crank * BM, n0 = w.n0;
       const int row = m0 + sub * 32 + lane;
       const bool got = mbar_wait_cluster(smem_u32(&bars->acc_full[a]), (uint32_t)((i >> 1) & 1)) &&
                        wait_rows_ready(ready, m0, M);
@@ -407,7 +445,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const float srow = (row < M) ? sx[row] : 0.f;
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
+      for (int c0 = 0; c0 < w.ncols; c0 += 32) {
         if (n0 + c0 >= N) break;
         uint32_t r[32];
         tmem_ld32(tmem + a * kAccCols + lane_off + c0, r);
@@ -458,23 +496,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   } else {
-    // ---------------- quantisers: rows in increasing order from ctr[0]
+    // ---------------- quantisers: batches of rows in increasing order from ctr[0]
+    const int qw = warp - kFirstQuantWarp;
     const int nvec = K >> 3;
-    while (true) {
-      int row = 0;
-      if (lane == 0) row = (int)atomicAdd(ctr, 1u);
-      row = __shfl_sync(0xffffffffu, row, 0);
-      if (row >= M) break;
-      const uint4* xr = X + (size_t)row * nvec;
-      uint2* qr = reinterpret_cast<uint2*>(Xq + (size_t)row * K);
-      if (K <= kRegRowMax) quant_row_regs<false>(xr, qr, sx + row, nvec, lane);
-      else quant_row_long(xr, qr, sx + row, nvec, lane);
-      fence_proxy_async_global();                  // codes are read by TMA
-      __syncwarp();
-      if (lane == 0) {
-        __threadfence();
-        red_release_add(ctr + 1 + row / BM, 1u);
+    if (qw == 0 && lane == 0) bars->qbase[0] = (int)atomicAdd(ctr, (unsigned)kFusedQuantWarps);
+    named_bar_sync(1, 32 * kFusedQuantWarps);
+    for (int k = 0;; ++k) {
+      const int base = *reinterpret_cast<volatile int*>(&bars->qbase[k & 1]);
+      if (base >= M) break;                        // the same for every quantiser warp
+      if (qw == 0 && lane == 0)                    // claim the next batch early
+        bars->qbase[(k + 1) & 1] = (int)atomicAdd(ctr, (unsigned)kFusedQuantWarps);
+      const int row = base + qw;
+      if (row < M) {
+        const uint4* xr = X + (size_t)row * nvec;
+        uint2* qr = reinterpret_cast<uint2*>(Xq + (size_t)row * K);
+        if (K <= kRegRowMax) quant_row_regs<false>(xr, qr, sx + row, nvec, lane);
+        else quant_row_long(xr, qr, sx + row, nvec, lane);
+        fence_proxy_async_global();                // codes are read by TMA
+        __syncwarp();                              // the row's stores before the release below
+        if (lane == 0) red_release_add(ctr + 1 + row / BM, 1u);
       }
+      // the next batch's base is visible, and every warp has read this one
+      // before it is overwritten two batches on
+      named_bar_sync(1, 32 * kFusedQuantWarps);
     }
   }
 
@@ -551,11 +595,13 @@ cudaError_t launch_absmax_fp8_gemm(const void* X, const uint8_t* Wq, const float
   }
   if (!sx) sx = reinterpret_cast<float*>(ws + off);
 
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA, tmB, tmBh;
   if (!encode_tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, (uint64_t)K, (uint64_t)M,
                       (uint64_t)K, BK, BM, true) ||
       !encode_tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, (uint64_t)K, (uint64_t)N,
-                      (uint64_t)K, BK, BN / 2, true))
+                      (uint64_t)K, BK, BN / 2, true) ||
+      !encode_tmap_2d(&tmBh, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, (uint64_t)K, (uint64_t)N,
+                      (uint64_t)K, BK, BN / 4, true))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaMemsetAsync(ctr, 0, (size_t)(1 + (M + BM - 1) / BM) * sizeof(unsigned), s);
   if (e != cudaSuccess) return e;
@@ -563,7 +609,7 @@ cudaError_t launch_absmax_fp8_gemm(const void* X, const uint8_t* Wq, const float
   if (e != cudaSuccess) return e;
   const int tiles_n = (N + BN - 1) / BN;
   const int64_t pairs = (int64_t)tiles_n * ((M + 2 * BM - 1) / (2 * BM));
-  if (pairs >= (1ll << 30)) return cudaErrorInvalidValue;
+  if (pairs >= (1ll << 29)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = kGemmSmem;
@@ -581,9 +627,15 @@ cudaError_t launch_absmax_fp8_gemm(const void* X, const uint8_t* Wq, const float
   const int clusters = gemm_clusters(sms, cfg);
   if (clusters < 1) return cudaErrorInvalidConfiguration;
   cfg.gridDim = dim3(2 * clusters, 1, 1);
-  return cudaLaunchKernelEx(&cfg, fp8_gemm_kernel, tmA, tmB, static_cast<const uint4*>(X), xq, sx,
-                            sw, static_cast<__nv_bfloat16*>(Y), M, N, K, tiles_n, (int)pairs, ctr,
-                            err);
+  // whole rounds of full tiles; the tiles left over for a last, partial round
+  // are split in column halves when that lets them spread over the pairs
+  const int full_rounds = (int)(pairs / clusters);
+  const int left = (int)(pairs - (int64_t)full_rounds * clusters);
+  const int n_full = (left > 0 && 2 * left <= clusters) ? full_rounds * clusters : (int)pairs;
+  const int n_tiles = n_full + 2 * ((int)pairs - n_full);
+  return cudaLaunchKernelEx(&cfg, fp8_gemm_kernel, tmA, tmB, tmBh, static_cast<const uint4*>(X), xq,
+                            sx, sw, static_cast<__nv_bfloat16*>(Y), M, N, K, tiles_n, n_full, n_tiles,
+                            ctr, err);
 }
 
 }  // namespace rf

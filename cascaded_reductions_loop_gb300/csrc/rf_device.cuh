@@ -337,6 +337,12 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   return r;
 }
 
+// Barrier among `threads` threads (a multiple of 32) of this CTA, on named
+// barrier `id` (1..15; 0 is the one __syncthreads uses).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // Whole-cluster barrier (every thread of every CTA of the cluster).
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::

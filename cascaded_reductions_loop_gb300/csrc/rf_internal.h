@@ -47,6 +47,12 @@ cudaError_t launch_attn_fwd_bf16_tc(const void* Q, const void* K, const void* V,
                                     int H, int Lq, int Lk, int d, float scale, int causal,
                                     int two_pass, unsigned* err, cudaStream_t s);
 
+// Fixed-length, unmasked, incremental: two query tiles per CTA in ping-pong,
+// P and O in tensor memory (the BERT-style prefill path).
+cudaError_t launch_attn_prefill_tc(const void* Q, const void* K, const void* V, void* O, int B,
+                                   int H, int Lq, int Lk, float scale, unsigned* err,
+                                   cudaStream_t s);
+
 // Packed variable-length layout: Q/O [total_q][H][d], K/V [total_k][H][d],
 // sequence b = tokens cu_q[b] .. cu_q[b+1]-1 (device arrays of B + 1 int32).
 cudaError_t launch_attn_fwd_f32_varlen(const float* Q, const float* K, const float* V, float* O,

@@ -64,6 +64,14 @@ const char* rf_status_string(int status);
 int rf_version(void);
 
 /*
+ * Name and description of the last CUDA error that made an entry point
+ * return RF_ERR_CUDA in the calling host thread ("none" if there was none).
+ * The string is owned by the library and stays valid until the thread's next
+ * call.  (An interface aid; the paper has no counterpart.)
+ */
+const char* rf_last_cuda_error(void);
+
+/*
  * Synchronises `stream`, then reads and clears the device-side error word of
  * the current device.  Returns RF_OK, RF_ERR_DEVICE_TIMEOUT (some kernel gave
  * up on a bounded wait and returned early; its outputs are incomplete),

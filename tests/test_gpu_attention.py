@@ -120,13 +120,17 @@ def test_bf16_causal_ragged(rf, shape):
 
 
 def test_bf16_causal_last_row_equals_unmasked(rf):
-    """The last query row reads every key, so it must equal the unmasked
-    kernel's last row bit for bit (same tiles, same arithmetic order)."""
+    """The last query row reads every key: the causal kernel's last row
+    matches the unmasked oracle, and the unmasked kernel (a different kernel,
+    whose running maximum moves lazily) to within bf16 rounding."""
     sh = I.AttnShape(1, 4, 4, 384, 384, 64, "bf16", seed=77)
     q, k, v = I.attention_inputs(sh)
     oc = _run(rf, q, k, v, sh.scale, causal=1)
     on = _run(rf, q, k, v, sh.scale, causal=0)
-    np.testing.assert_array_equal(to64(oc[:, :, -1]), to64(on[:, :, -1]))
+    ref = A.attention(q, k, v, sh.scale)
+    assert_bf16_close(oc[:, :, -1], ref[:, :, -1], "causal last row")
+    assert_bf16_close(on[:, :, -1], ref[:, :, -1], "unmasked last row")
+    assert np.abs(to64(oc[:, :, -1]) - to64(on[:, :, -1])).max() <= 4e-3
 
 
 # ----------------------------------------- non-incremental (two-pass) mode

@@ -71,7 +71,10 @@ def test_fp8_full_size(rf):
 
 @pytest.mark.parametrize("M,N,K", [(200, 300, 272), (1, 16, 16), (130, 264, 4096),
                                    (257, 512, 384), (64, 1000, 5008), (700, 520, 1040),
-                                   (4096, 256, 128), (300, 4096, 256)])
+                                   (4096, 256, 128), (300, 4096, 256),
+                                   # 100 pair tiles: whole rounds of full tiles, then halves;
+                                   # 64 pair tiles: all full (too many left for halves)
+                                   (2560, 2560, 256), (1024, 4096, 384)])
 def test_fp8_ragged(rf, M, N, K):
     x, w = I.fp8_inputs(I.FP8Shape(M=M, N=N, K=K, seed=M + N + K))
     wq_d, sw_d, wq_o, sw_o = _weights(rf, w)
