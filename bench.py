@@ -25,7 +25,8 @@ stated tolerances for floats); the run exits non-zero if any check fails.
 
 --only times a subset of the step, or calls outside it (the causal and
 variable-length prefill, short prefill in both evaluation orders, other
-expert counts of the gate, the latent-KV decode), with the same metric.
+expert counts of the gate, the latent-KV decode), with the same metric, in
+the order given.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--only CALL,...]
@@ -107,7 +108,7 @@ class Op:
 def decode_op(name, s):
     kv = 2 * s.B * s.Hkv * s.Lk * s.d * 2
     qo = 2 * s.B * s.Hq * s.d * 2
-    return Op(name, kv + qo, 4 * s.B * s.Hq * s.Lk * s.d, "bf16", 2)
+    return Op(name, kv + qo, 4 * s.B * s.Hq * s.Lk * s.d, "bf16", 1)
 
 
 def make_ops():
@@ -647,7 +648,8 @@ def select_ops(args):
         unknown = set(names) - {op.name for op in known}
         if unknown:
             raise SystemExit(f"unknown op(s) {sorted(unknown)}")
-        ops = [op for op in known if op.name in names]
+        by_name = {op.name: op for op in known}
+        ops = [by_name[n] for n in dict.fromkeys(names)]     # in the order given
     return ops
 
 

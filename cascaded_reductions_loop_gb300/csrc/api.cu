@@ -297,9 +297,8 @@ int rf_attn_decode_splitkv_num_splits(int B, int Hq, int Hkv, int Lk, int d, int
 
 size_t rf_attn_decode_splitkv_workspace_size(int B, int Hq, int Hkv, int Lk, int d,
                                              int num_splits) {
-  const int S = rf_attn_decode_splitkv_num_splits(B, Hq, Hkv, Lk, d, num_splits);
-  if (S <= 0) return 0;
-  return decode_workspace_bytes(B, Hq, d, S);
+  if (decode_shape_check(B, Hq, Hkv, Lk, d, num_splits) != RF_OK) return 0;
+  return decode_workspace_bytes(B, Hq, Hkv, Lk, d, num_splits);
 }
 
 rf_status rf_attn_decode_splitkv(const void* Q, const void* K, const void* V, void* O, int B,
@@ -309,15 +308,13 @@ rf_status rf_attn_decode_splitkv(const void* Q, const void* K, const void* V, vo
   if (!(scale > 0.f) || !(scale < INFINITY)) return RF_ERR_INVALID_ARG;
   rf_status st = decode_shape_check(B, Hq, Hkv, Lk, d, num_splits);
   if (st != RF_OK) return st;
-  const int S = decode_num_splits(B, Hq, Hkv, Lk, d, num_splits);
-  if (S <= 0) return RF_ERR_CUDA;   // auto choice needs the device's SM count
-  if (!workspace || !aligned16(workspace) ||
-      workspace_bytes < decode_workspace_bytes(B, Hq, d, S))
-    return RF_ERR_WORKSPACE;
+  const size_t need = decode_workspace_bytes(B, Hq, Hkv, Lk, d, num_splits);
+  if (need == 0) return RF_ERR_CUDA;   // the automatic partition needs the device's SM count
+  if (!workspace || !aligned16(workspace) || workspace_bytes < need) return RF_ERR_WORKSPACE;
   unsigned* err = device_error_word();
   if (!err) return RF_ERR_CUDA;
-  return from_cuda(launch_decode_splitkv(Q, K, V, O, B, Hq, Hkv, Lk, d, scale, S, workspace, err,
-                                         reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_decode_splitkv(Q, K, V, O, B, Hq, Hkv, Lk, d, scale, num_splits,
+                                         workspace, err, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 static rf_status mla_shape_check(int B, int Hq, int Lk, int d_qk, int d_v, int num_splits) {

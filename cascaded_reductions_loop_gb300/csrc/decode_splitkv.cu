@@ -1,26 +1,49 @@
-// decode_splitkv.cu -- multi-segment (split-KV) fused decode attention.
+// decode_splitkv.cu -- multi-segment (split-KV) fused decode attention with
+// the merge of the segments' partial states done inside the same kernel.
 //
-// Multi-segment strategy ([S] Methodologie 3; [E] §3.3 inter-block merge and
-// multi-kernel cooperation): the keys of every (batch, kv head) are cut into
-// S segments.  Kernel 1 (decode_partial_kernel, a persistent grid of one CTA
-// per SM) takes the segments as work items; the four warps of the CTA that
-// takes an item each run the incremental safe-softmax loop ([E] §2.3, §4.1)
-// over every fourth chunk of the segment and write their partial state
-// (m, l, o) -- o unnormalised, m in log2 units -- for each of the G query heads
-// that share the kv head.  Kernel 2 (decode_merge_kernel, launched as a
-// programmatic dependent of kernel 1) combines the 4 S partial states of
-// every (batch, query head): M = max m_j,
-// L = sum l_j 2^(m_j - M), O = sum o_j 2^(m_j - M) / L.  (Merging inside
-// kernel 1, by the last warp to finish a group, was measured slower: each
-// warp must make its states visible with a fence before taking a ticket, and
-// the merging warp falls behind the others.)
+// Multi-segment strategy ([S] Methodologie 3; [E] §3.3 inter-block merge):
+// the keys of every (batch, kv head) sequence are cut into segments, each
+// reduced by one CTA with the incremental safe-softmax loop ([E] §2.3, §4.1)
+// into a partial state (m, l, o) -- o unnormalised, m in log2 units -- for
+// each of the G query heads that share the kv head; the states of a sequence
+// are then merged: M = max m_j, L = sum l_j 2^(m_j - M),
+// O = sum o_j 2^(m_j - M) / L.
+//
+// Partition.  Automatic (num_splits = 0): the 32-key chunks of all B * Hkv
+// sequences, laid end to end, are cut into one contiguous range per CTA of a
+// persistent grid of one CTA per SM, so every CTA streams the same number of
+// chunks (within one).  A range covers whole sequences and the ends of one or
+// two others; a sequence is cut into as many segments as ranges touch it.
+// Explicit (num_splits = S): each sequence is cut into S equal key segments,
+// and CTA c takes segments c, c + grid, ... in turn.  Either way a CTA works
+// through a list of "pieces" (a sequence and a key range of it).
+//
+// Inside a CTA: four consumer warps take every fourth chunk of the current
+// piece, each with a private 2-stage TMA ring that is refilled across piece
+// boundaries (the next piece's keys are in flight while the current one
+// ends); the G (<= 8) query rows form the M = 16 side (zero-padded) of
+// mma.sync m16n8k16 bf16 tiles with fp32 accumulation: S = Q K^T, online
+// softmax in registers (quad shuffles), O += P V with P rounded to bf16.  At
+// the end of a piece each consumer warp drops its state into a hand-off
+// buffer in shared memory (two buffers, taken in turn) and goes on with the
+// next piece at once; a fifth warp, the merge warp, combines the four states
+// (inter-warp level of the merge) and then
+//   - for a piece that is a whole sequence, writes O = o / l in bf16;
+//   - otherwise writes the piece's partial state to the workspace, and takes
+//     a ticket on the sequence's counter (a fence before the atomic makes the
+//     state visible first); the CTA that draws the last ticket reads the
+//     other pieces' states back from L2 and merges them (inter-block level),
+//     always in the pieces' key order, so the result has the same bits
+//     whichever CTA finishes last.
+// The ticket counters are zeroed by a small memset on the same stream just
+// before the kernel, so the workspace never needs initialising.  (Zeroing
+// them inside the kernel needs a grid-wide barrier before the first ticket,
+// i.e. a cooperative launch; measured, that barrier cost ~1 us more than the
+// memset.)
 //
 // Data movement: K and V stream from HBM exactly once, by TMA into 128-byte
 // swizzled shared-memory tiles (chunks of 32 keys x 128 dims, two 64-dim
-// boxes each), one private ring of stages per warp.  The G (<= 8) query rows
-// of a kv head form the M = 16 side of mma.sync m16n8k16 bf16 tiles with fp32
-// accumulation: S = Q K^T, then O += P V with P rounded to bf16; the row max,
-// exp2 and sums stay in registers (quad shuffles).
+// boxes each).  The partial states are a few hundred KB, read back from L2.
 #include <math.h>
 
 #include <mutex>
@@ -33,11 +56,123 @@ namespace {
 
 constexpr int kD = 128;          // head dim
 constexpr int kCK = 32;          // keys per chunk
-constexpr int kStages = 2;       // ring depth per warp
+constexpr int kStages = 2;       // ring depth per consumer warp
 constexpr int kWarps = 4;        // consumer warps per CTA
+constexpr int kThreads = (kWarps + 1) * 32;      // + the merge warp
 constexpr int kBoxBytes = kCK * 128;             // one 64-dim box of kCK rows
 constexpr int kStageBytes = 4 * kBoxBytes;       // K box0, K box1, V box0, V box1
-constexpr int kSmemBytes = kWarps * kStages * kStageBytes + 1024 + 256;
+constexpr int kRingBytes = kWarps * kStages * kStageBytes;
+// Hand-off buffer: o of each consumer warp and head, rows padded to 136
+// floats (so the eight head rows a warp writes at once fall in different
+// banks), then (m, l) of each warp and head.
+constexpr int kRowF = 136;
+constexpr int kHandOBytes = kWarps * 8 * kRowF * 4;
+constexpr int kHandBytes = kHandOBytes + kWarps * 8 * 8;
+constexpr int kSmemBytes = kRingBytes + 2 * kHandBytes + 256 + 1024;
+
+// The partition of the keys into pieces, the same on the host and the device.
+// Every count here is below 2^31 (B * Hkv * Lk < 2^31), so the automatic
+// partition needs 32-bit arithmetic only.
+struct DecodePlan {
+  uint32_t T;      // automatic: chunks of all sequences (P * nck)
+  uint32_t q;      // T / grid: every CTA owns q or q + 1 chunks
+  uint32_t rem;    // T % grid: CTAs c < rem own q + 1
+  uint32_t nck;    // chunks per sequence, ceil(Lk / kCK)
+  int Lk;
+  int S;           // explicit segments per sequence, 0 = automatic
+  int P;           // sequences, B * Hkv
+  int grid;        // CTAs
+};
+
+struct DecodePiece {
+  int p;           // sequence (b * Hkv + kv head)
+  int lo, hi;      // keys [lo, hi) of the sequence
+  int slot;        // workspace slot of its partial state (when npieces > 1)
+  int npieces;     // pieces the sequence is cut into
+};
+
+// grid = min(SMs, units) so that no CTA is left without work.
+__host__ __device__ inline void plan_init(DecodePlan* pl, int P, int Lk, int S, int sms) {
+  pl->P = P;
+  pl->Lk = Lk;
+  pl->S = S;
+  pl->nck = (uint32_t)((Lk + kCK - 1) / kCK);
+  pl->T = (uint32_t)P * pl->nck;
+  const int64_t units = S > 0 ? (int64_t)P * S : (int64_t)pl->T;
+  pl->grid = (int)(units < sms ? units : sms);
+  pl->q = pl->T / (uint32_t)pl->grid;
+  pl->rem = pl->T % (uint32_t)pl->grid;
+}
+
+// Automatic partition: CTA c owns chunks [start(c), start(c + 1)).
+__host__ __device__ __forceinline__ uint32_t plan_start(const DecodePlan& pl, int c) {
+  const uint32_t uc = (uint32_t)c;
+  return uc * pl.q + (uc < pl.rem ? uc : pl.rem);
+}
+// The CTA whose range holds chunk x.
+__host__ __device__ __forceinline__ int plan_owner(const DecodePlan& pl, uint32_t x) {
+  const uint32_t big = pl.rem * (pl.q + 1);          // chunks of the CTAs with q + 1
+  return (int)(x < big ? x / (pl.q + 1) : pl.rem + (x - big) / pl.q);
+}
+
+__host__ __device__ __forceinline__ int plan_num_pieces(const DecodePlan& pl, int c) {
+  if (pl.S > 0) {
+    const uint32_t items = (uint32_t)pl.P * (uint32_t)pl.S;
+    return items > (uint32_t)c ? (int)((items - c + pl.grid - 1) / pl.grid) : 0;
+  }
+  const uint32_t r0 = plan_start(pl, c), r1 = plan_start(pl, c + 1);
+  return r1 > r0 ? (int)((r1 - 1) / pl.nck - r0 / pl.nck + 1) : 0;
+}
+
+// Piece k (0 ..) of CTA c.  In the automatic partition the slot of a piece
+// is 2c for the CTA's first piece and 2c + 1 for its last; only those two
+// can be parts of a longer sequence.
+__host__ __device__ __forceinline__ DecodePiece plan_piece(const DecodePlan& pl, int c, int k) {
+  DecodePiece pc;
+  if (pl.S > 0) {
+    const uint32_t item = (uint32_t)c + (uint32_t)k * (uint32_t)pl.grid;
+    const int seg = (int)(item % (uint32_t)pl.S);
+    pc.p = (int)(item / (uint32_t)pl.S);
+    pc.lo = (int)((int64_t)seg * pl.Lk / pl.S);
+    pc.hi = (int)((int64_t)(seg + 1) * pl.Lk / pl.S);
+    pc.slot = (int)item;
+    pc.npieces = pl.S;
+    return pc;
+  }
+  const uint32_t r0 = plan_start(pl, c), r1 = plan_start(pl, c + 1);
+  const uint32_t p = r0 / pl.nck + (uint32_t)k;
+  const uint32_t s0 = p * pl.nck, s1 = s0 + pl.nck;
+  const uint32_t a = (r0 > s0 ? r0 : s0) - s0, b = (r1 < s1 ? r1 : s1) - s0;
+  const int hi = (int)(b * kCK);
+  pc.p = (int)p;
+  pc.lo = (int)(a * kCK);
+  pc.hi = hi < pl.Lk ? hi : pl.Lk;
+  pc.slot = 2 * c + (k == 0 ? 0 : 1);
+  // a piece strictly inside the range is a whole sequence
+  pc.npieces = (s0 >= r0 && s1 <= r1) ? 1 : plan_owner(pl, s1 - 1) - plan_owner(pl, s0) + 1;
+  return pc;
+}
+
+// Workspace slot of the j-th piece (in key order) of sequence p.
+__host__ __device__ __forceinline__ int plan_slot(const DecodePlan& pl, int p, int j) {
+  if (pl.S > 0) return p * pl.S + j;
+  const int c = plan_owner(pl, (uint32_t)p * pl.nck) + j;
+  return 2 * c + (plan_start(pl, c) / pl.nck == (uint32_t)p ? 0 : 1);
+}
+
+__host__ __device__ __forceinline__ int64_t plan_slots(const DecodePlan& pl) {
+  return pl.S > 0 ? (int64_t)pl.P * pl.S : 2 * (int64_t)pl.grid;
+}
+
+// The order in which a CTA works through its np pieces: in the automatic
+// partition its two partial pieces (first and last) come before the whole
+// sequences between them, so the neighbours' matching pieces are done early
+// and the merges across CTAs happen while the keys still stream, not at the
+// end of the kernel.
+__host__ __device__ __forceinline__ int plan_order(const DecodePlan& pl, int np, int k) {
+  if (pl.S > 0 || np < 3) return k;
+  return k == 0 ? 0 : (k == 1 ? np - 1 : k - 1);
+}
 
 __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
@@ -68,74 +203,98 @@ __device__ __forceinline__ uint32_t sw_off(int r, int c) {
   return (uint32_t)((c >> 3) * kBoxBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-// A work item is one key segment of one (batch, kv head): item = (b * Hkv +
-// kvh) * S + seg.  The grid is persistent: CTA c takes items c, c + gridDim.x,
-// ...  Within a CTA, warp w takes chunks w, w + kWarps, ... of each item in
-// turn; its private ring is refilled across item boundaries, so the next
-// item's keys are already in flight while the current item's partial state
-// is merged and written.
-struct DecodeItem {
-  int b, kvh, seg;
-  int64_t lo, hi, row_base;
-  int nchunks;
-};
-
-__device__ __forceinline__ DecodeItem decode_item(int item, int Hkv, int Lk, int S) {
-  DecodeItem it;
-  it.seg = item % S;
-  const int pair = item / S;
-  it.kvh = pair % Hkv;
-  it.b = pair / Hkv;
-  it.lo = (int64_t)it.seg * Lk / S;
-  it.hi = (int64_t)(it.seg + 1) * Lk / S;
-  it.row_base = (int64_t)pair * Lk;
-  it.nchunks = (int)((it.hi - it.lo + kCK - 1) / kCK);
-  return it;
+__device__ __forceinline__ int piece_chunks(const DecodePiece& pc) {
+  return (pc.hi - pc.lo + kCK - 1) / kCK;
 }
 
+// Adds state (m, l, o) into the running merge (M, L, O) whose reference is
+// the final maximum Mx (so every weight is 2^(m - Mx) <= 1).
+__device__ __forceinline__ void merge_into(float Mx, float m, float l, float4 o, float& L,
+                                           float4& O) {
+  const float w = exp2f(m - Mx);     // 0 for an empty state (m = -inf)
+  L = fmaf(l, w, L);
+  O.x = fmaf(o.x, w, O.x);
+  O.y = fmaf(o.y, w, O.y);
+  O.z = fmaf(o.z, w, O.z);
+  O.w = fmaf(o.w, w, O.w);
+}
+
+__device__ __forceinline__ void store_out(__nv_bfloat16* O, int64_t row, int lane, float L,
+                                          float4 o) {
+  const float inv = 1.f / L;
+  uint2 out;
+  out.x = pack_bf16x2(o.x * inv, o.y * inv);
+  out.y = pack_bf16x2(o.z * inv, o.w * inv);
+  reinterpret_cast<uint2*>(O + row * kD)[lane] = out;
+}
+
+// Bounded wait that sleeps between polls: for the merge warp, which idles
+// for most of a piece and would otherwise take issue slots from the consumer
+// warp it shares a scheduler with.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_test_wait(bar, parity)) {
+    __nanosleep(256);
+    if (globaltimer_ns() - t0 > kDefaultWaitNs) return false;
+  }
+  return true;
+}
+
+struct Bars {
+  uint64_t full[kWarps][kStages];   // TMA ring of each consumer warp
+  uint64_t hand_full[2];            // the four consumer states of a piece are in buffer i
+  uint64_t hand_free[2];            // the merge warp has read buffer i
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
+
 template <int G>
-__global__ void __launch_bounds__(kWarps * 32)
-    decode_partial_kernel(const __grid_constant__ CUtensorMap tmK,
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_splitkv_kernel(const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV,
-                          const __nv_bfloat16* __restrict__ Q, float* __restrict__ part_o,
-                          float* __restrict__ part_ml, int Hq, int Hkv, int Lk, int S, int items,
+                          const __nv_bfloat16* __restrict__ Q, __nv_bfloat16* __restrict__ O,
+                          float* __restrict__ ws_o, float2* __restrict__ ws_ml,
+                          unsigned* __restrict__ tickets, const DecodePlan pl,
                           float qk_scale_log2, unsigned* err) {
   static_assert(G >= 1 && G <= 8, "query heads per kv head");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * kStages * kStageBytes);
+  uint8_t* hand = smem + kRingBytes;
+  Bars* bars = reinterpret_cast<Bars*>(hand + 2 * kHandBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int my_items =
-      items > (int)blockIdx.x ? (items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
-  uint8_t* my_stage = smem + warp * kStages * kStageBytes;
-  uint64_t* my_full = bars + warp * kStages;
+  const int cta = (int)blockIdx.x;
+  const int np = plan_num_pieces(pl, cta);
+  const bool consumer = warp < kWarps;
 
-  if (lane == 0) {
-    prefetch_tmap(&tmK);
-    prefetch_tmap(&tmV);
-#pragma unroll
-    for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&my_full[i]), 1);
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < kWarps; ++w)
+      for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&bars->full[w][i]), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bars->hand_full[i]), kWarps);
+      mbar_init(smem_u32(&bars->hand_free[i]), 1);
+    }
     fence_mbar_init();
   }
-  __syncwarp();
+  __syncthreads();
 
-  // producer cursor over this warp's chunk stream (lane 0 only)
+  // producer cursor over this warp's chunk stream (lane 0 of a consumer warp)
+  uint8_t* my_stage = smem + (consumer ? warp : 0) * kStages * kStageBytes;
+  uint64_t* my_full = bars->full[consumer ? warp : 0];
   int pk = 0, pci = warp, issued = 0;
-  DecodeItem pit = decode_item(my_items > 0 ? (int)blockIdx.x : 0, Hkv, Lk, S);
+  DecodePiece pp = plan_piece(pl, cta, plan_order(pl, np, 0));
   auto skip_empty = [&]() {
-    while (pk < my_items && pci >= pit.nchunks) {
+    while (pk < np && pci >= piece_chunks(pp)) {
       ++pk;
       pci = warp;
-      if (pk < my_items) pit = decode_item((int)blockIdx.x + pk * (int)gridDim.x, Hkv, Lk, S);
+      if (pk < np) pp = plan_piece(pl, cta, plan_order(pl, np, pk));
     }
   };
   auto issue_next = [&]() {
     skip_empty();
-    if (pk >= my_items) return;
+    if (pk >= np) return;
     const int slot = issued % kStages;
-    const int32_t row = (int32_t)(pit.row_base + pit.lo + (int64_t)pci * kCK);
+    const int32_t row = (int32_t)((int64_t)pp.p * pl.Lk + pp.lo + (int64_t)pci * kCK);
     const uint32_t dst = smem_u32(my_stage + slot * kStageBytes);
     const uint32_t bar = smem_u32(&my_full[slot]);
     mbar_arrive_expect_tx(bar, kStageBytes);
@@ -146,11 +305,130 @@ __global__ void __launch_bounds__(kWarps * 32)
     ++issued;
     pci += kWarps;
   };
-  if (lane == 0)
+  if (consumer && lane == 0) {
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
     for (int i = 0; i < kStages; ++i) issue_next();
-  // the merge kernel may be scheduled now; it waits for this grid to finish
-  asm volatile("griddepcontrol.launch_dependents;");
+  }
 
+  if (!consumer) {
+    // ------------------------------------------------------------ merge warp
+    for (int k = 0; k < np; ++k) {
+      const DecodePiece pc = plan_piece(pl, cta, plan_order(pl, np, k));
+      const int buf = k & 1;
+      bool ok = mbar_wait_sleep(smem_u32(&bars->hand_full[buf]), (uint32_t)((k >> 1) & 1));
+      if (!__all_sync(0xffffffffu, ok)) {
+        raise_error(err, kDevErrTimeout);
+        return;
+      }
+      const float* ho = reinterpret_cast<const float*>(hand + buf * kHandBytes);
+      const float2* hml = reinterpret_cast<const float2*>(hand + buf * kHandBytes + kHandOBytes);
+      float Mh[G], Lh[G];
+      float4 Oh[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float m[kWarps], l[kWarps];
+        float Mx = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          const float2 v = hml[w * 8 + h];
+          m[w] = v.x;
+          l[w] = v.y;
+          Mx = fmaxf(Mx, v.x);
+        }
+        float L = 0.f;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (Mx != -INFINITY) {       // else no key of the piece reached this CTA's warps
+#pragma unroll
+          for (int w = 0; w < kWarps; ++w)
+            merge_into(Mx, m[w], l[w],
+                       *reinterpret_cast<const float4*>(ho + (w * 8 + h) * kRowF + 4 * lane), L,
+                       o);
+        }
+        Mh[h] = Mx;
+        Lh[h] = L;
+        Oh[h] = o;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->hand_free[buf]));   // release: reads done
+
+      if (pc.npieces == 1) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) store_out(O, (int64_t)pc.p * G + h, lane, Lh[h], Oh[h]);
+        continue;
+      }
+      // partial state of the piece -> workspace; ticket on the sequence
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        reinterpret_cast<float4*>(ws_o + ((int64_t)pc.slot * G + h) * kD)[lane] = Oh[h];
+        if (lane == 0) ws_ml[(int64_t)pc.slot * G + h] = make_float2(Mh[h], Lh[h]);
+      }
+      __threadfence();
+      __syncwarp();
+      unsigned t = 0;
+      if (lane == 0) t = atomicAdd(&tickets[pc.p], 1u);
+      t = __shfl_sync(0xffffffffu, t, 0);
+      if (t != (unsigned)(pc.npieces - 1)) continue;
+      __threadfence();               // the other pieces' states are visible now
+      // Last piece to finish: merge all pieces of the sequence, one after
+      // another in key order (this CTA's own piece from registers: the same
+      // values it stored), so the bits do not depend on which CTA is last.
+      // The loads of a batch of kBatch pieces are issued together.
+      constexpr int kBatch = G <= 2 ? 4 : (G == 4 ? 2 : 1);
+      float Mt[G], Lt[G];
+      float4 Ot[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        Mt[h] = -INFINITY;
+        Lt[h] = 0.f;
+        Ot[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      for (int j0 = 0; j0 < pc.npieces; j0 += kBatch) {
+        float2 ml[kBatch][G];
+        float4 oj[kBatch][G];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int j = j0 + u;
+          const int sj = j < pc.npieces ? plan_slot(pl, pc.p, j) : -1;
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            if (sj == pc.slot) {
+              ml[u][h] = make_float2(Mh[h], Lh[h]);
+              oj[u][h] = Oh[h];
+            } else if (sj >= 0) {
+              ml[u][h] = __ldcg(&ws_ml[(int64_t)sj * G + h]);
+              oj[u][h] =
+                  __ldcg(reinterpret_cast<const float4*>(ws_o + ((int64_t)sj * G + h) * kD) + lane);
+            } else {
+              ml[u][h] = make_float2(-INFINITY, 0.f);
+              oj[u][h] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float m = ml[u][h].x;
+            if (m == -INFINITY) continue;          // a piece without keys adds nothing
+            const float Mn = fmaxf(Mt[h], m);
+            const float a = exp2f(Mt[h] - Mn);     // 0 while nothing has been added
+            const float w = exp2f(m - Mn);
+            Lt[h] = fmaf(ml[u][h].y, w, Lt[h] * a);
+            Ot[h].x = fmaf(oj[u][h].x, w, Ot[h].x * a);
+            Ot[h].y = fmaf(oj[u][h].y, w, Ot[h].y * a);
+            Ot[h].z = fmaf(oj[u][h].z, w, Ot[h].z * a);
+            Ot[h].w = fmaf(oj[u][h].w, w, Ot[h].w * a);
+            Mt[h] = Mn;
+          }
+      }
+#pragma unroll
+      for (int h = 0; h < G; ++h) store_out(O, (int64_t)pc.p * G + h, lane, Lt[h], Ot[h]);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ consumer warps
   const int hrow = lane >> 2;           // head of this lane's accumulator rows
   const int kq = (lane & 3) * 2;        // first of this lane's two columns
   const int mi = lane >> 3, mr = lane & 7;   // ldmatrix: matrix, row within it
@@ -158,12 +436,12 @@ __global__ void __launch_bounds__(kWarps * 32)
   bool failed = false;
 
   // Q of the G query heads as the A operand (rows zero-padded to 16); the
-  // next item's Q is loaded while the current item runs.
+  // next piece's Q is loaded while the current piece runs.
   auto load_q = [&](int k, uint32_t (&q)[8][2]) {
-    if (k >= my_items) return;
-    const DecodeItem it = decode_item((int)blockIdx.x + k * (int)gridDim.x, Hkv, Lk, S);
+    if (k >= np) return;
+    const DecodePiece pc = plan_piece(pl, cta, plan_order(pl, np, k));
     const uint32_t* qp = reinterpret_cast<const uint32_t*>(
-        Q + ((int64_t)it.b * Hq + (int64_t)it.kvh * G + (hrow < G ? hrow : 0)) * kD);
+        Q + ((int64_t)pc.p * G + (hrow < G ? hrow : 0)) * kD);
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
       q[ks][0] = hrow < G ? __ldg(qp + ((ks * 16 + kq) >> 1)) : 0u;
@@ -173,8 +451,9 @@ __global__ void __launch_bounds__(kWarps * 32)
   uint32_t qa[8][2], qn[8][2];
   load_q(0, qn);
 
-  for (int k = 0; k < my_items && !failed; ++k) {
-    const DecodeItem it = decode_item((int)blockIdx.x + k * (int)gridDim.x, Hkv, Lk, S);
+  for (int k = 0; k < np && !failed; ++k) {
+    const DecodePiece pc = plan_piece(pl, cta, plan_order(pl, np, k));
+    const int nchunks = piece_chunks(pc);
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
       qa[ks][0] = qn[ks][0];
@@ -186,7 +465,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     for (int j = 0; j < 16; ++j) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.f;
     float m_run = -INFINITY, l_run = 0.f;
 
-    for (int ci = warp; ci < it.nchunks; ci += kWarps) {
+    for (int ci = warp; ci < nchunks; ci += kWarps) {
       const int slot = consumed % kStages;
       bool ok = mbar_wait(smem_u32(&my_full[slot]), (uint32_t)((consumed / kStages) & 1));
       ok = __all_sync(0xffffffffu, ok);
@@ -196,7 +475,7 @@ __global__ void __launch_bounds__(kWarps * 32)
       }
       const uint32_t kbase = smem_u32(my_stage + slot * kStageBytes);
       const uint32_t vbase = kbase + 2 * kBoxBytes;
-      const int64_t key0 = it.lo + (int64_t)ci * kCK;   // first key of the chunk
+      const int key0 = pc.lo + ci * kCK;   // first key of the chunk
 
       // ---- S = Q K^T for 32 keys: two 16-key sub-blocks x two 8-key n-blocks
       float sc[2][2][4];
@@ -223,8 +502,8 @@ __global__ void __launch_bounds__(kWarps * 32)
         for (int nb = 0; nb < 2; ++nb)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int64_t key = key0 + sb * 16 + nb * 8 + kq + e;
-            const float v = key < it.hi ? sc[sb][nb][e] * qk_scale_log2 : -INFINITY;
+            const int key = key0 + sb * 16 + nb * 8 + kq + e;
+            const float v = key < pc.hi ? sc[sb][nb][e] * qk_scale_log2 : -INFINITY;
             sc[sb][nb][e] = v;
             mx = fmaxf(mx, v);
           }
@@ -271,18 +550,29 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
     if (failed) break;
 
-    // ---- this warp's partial state of the item (o unnormalised, m in log2
-    // units); a warp without keys in the item writes (-inf, 0, 0)
+    // ---- this warp's state of the piece -> hand-off buffer k % 2 (a warp
+    // without keys in the piece hands over (-inf, 0, 0))
+    const int buf = k & 1;
+    if (k >= 2) {
+      bool ok = mbar_wait(smem_u32(&bars->hand_free[buf]), (uint32_t)(((k >> 1) - 1) & 1));
+      if (!__all_sync(0xffffffffu, ok)) {
+        failed = true;
+        break;
+      }
+    }
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
     if (hrow < G) {
-      const int64_t pidx =
-          (((int64_t)it.b * Hq + (int64_t)it.kvh * G + hrow) * S + it.seg) * kWarps + warp;
-      float2* po = reinterpret_cast<float2*>(part_o + pidx * kD);
+      float* ho = reinterpret_cast<float*>(hand + buf * kHandBytes) + (warp * 8 + hrow) * kRowF;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) po[(j * 8 + kq) >> 1] = make_float2(oacc[j][0], oacc[j][1]);
-      if ((lane & 3) == 0) reinterpret_cast<float2*>(part_ml)[pidx] = make_float2(m_run, l_run);
+      for (int j = 0; j < 16; ++j)
+        *reinterpret_cast<float2*>(ho + j * 8 + kq) = make_float2(oacc[j][0], oacc[j][1]);
+      if ((lane & 3) == 0)
+        reinterpret_cast<float2*>(hand + buf * kHandBytes + kHandOBytes)[warp * 8 + hrow] =
+            make_float2(m_run, l_run);
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&bars->hand_full[buf]));
   }
 
   if (failed) {
@@ -294,97 +584,42 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
 }
 
-// Merge kernel: one warp per (batch, query head), lane = 4 consecutive dims.
-// Lane j holds the (m, l) of state j of each block of 32 states and hands its
-// weight 2^(m_j - M) to the other lanes by shuffle; o is read 16 states at a
-// time so that those loads are in flight together.  It is launched as a
-// programmatic dependent of the partial kernel: its CTAs may start while the
-// partial kernel drains and wait (griddepcontrol.wait) until that grid has
-// finished and its writes are visible.
-constexpr int kMergeWarps = 4;
-
-__device__ __forceinline__ float4 o_block16(const float4* po, int j0, int n, float w,
-                                            float4 acc) {
-  float4 o[16];
-  if (n >= 16) {                     // common case: no per-load condition
-#pragma unroll
-    for (int u = 0; u < 16; ++u) o[u] = po[(int64_t)(j0 + u) * (kD / 4)];
-  } else {
-#pragma unroll
-    for (int u = 0; u < 16; ++u)
-      o[u] = u < n ? po[(int64_t)(j0 + u) * (kD / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-#pragma unroll
-  for (int u = 0; u < 16; ++u) {
-    const float wu = __shfl_sync(0xffffffffu, w, (j0 + u) & 31);
-    acc.x = fmaf(o[u].x, wu, acc.x);
-    acc.y = fmaf(o[u].y, wu, acc.y);
-    acc.z = fmaf(o[u].z, wu, acc.z);
-    acc.w = fmaf(o[u].w, wu, acc.w);
-  }
-  return acc;
-}
-
-__global__ void __launch_bounds__(kMergeWarps * 32)
-    decode_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
-                        __nv_bfloat16* __restrict__ O, int n_heads, int P) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int lane = threadIdx.x & 31;
-  const int64_t bh = (int64_t)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
-  if (bh >= n_heads) return;
-  const float2* ml = reinterpret_cast<const float2*>(part_ml) + bh * P;
-  const float4* po = reinterpret_cast<const float4*>(part_o + bh * P * kD) + lane;
-  float M = -INFINITY;
-  for (int j = lane; j < P; j += 32) M = fmaxf(M, ml[j].x);
-  M = warp_max(M);                                 // finite: some segment has keys
-  float L = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j0 = 0; j0 < P; j0 += 32) {
-    const float2 v = j0 + lane < P ? ml[j0 + lane] : make_float2(-INFINITY, 0.f);
-    const float w = exp2f(v.x - M);                // 0 for empty states
-    L += v.y * w;
-    acc = o_block16(po, j0, P - j0, w, acc);
-    if (P - j0 > 16) acc = o_block16(po, j0 + 16, P - j0 - 16, w, acc);
-  }
-  const float inv = 1.f / warp_sum(L);
-  uint2 out;
-  out.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-  out.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-  reinterpret_cast<uint2*>(O + bh * kD)[lane] = out;
-}
-
 template <int G>
 cudaError_t launch_g(const CUtensorMap& tmK, const CUtensorMap& tmV, const void* Q, void* O,
-                     int B, int Hq, int Hkv, int Lk, float scale, int S, float* part_o,
-                     float* part_ml, unsigned* err, cudaStream_t s) {
-  auto kern = decode_partial_kernel<G>;
+                     const DecodePlan& pl, float scale, float* ws_o, float2* ws_ml,
+                     unsigned* tickets, unsigned* err, cudaStream_t s) {
+  auto kern = decode_splitkv_kernel<G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int64_t items = (int64_t)B * Hkv * S;
-  if (items >= (1ll << 31)) return cudaErrorInvalidValue;
-  const int sms = sm_count();
-  if (sms <= 0) return cudaErrorInvalidValue;
-  const int grid = (int)(items < sms ? items : sms);        // one CTA per SM, persistent
   const float qk_scale_log2 = scale * 1.4426950408889634f;
-  kern<<<grid, kWarps * 32, kSmemBytes, s>>>(tmK, tmV, static_cast<const __nv_bfloat16*>(Q),
-                                             part_o, part_ml, Hq, Hkv, Lk, S, (int)items,
-                                             qk_scale_log2, err);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const int n_heads = B * Hq;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((n_heads + kMergeWarps - 1) / kMergeWarps, 1, 1);
-  cfg.blockDim = dim3(kMergeWarps * 32, 1, 1);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_merge_kernel, (const float*)part_o,
-                            (const float*)part_ml, static_cast<__nv_bfloat16*>(O), n_heads,
-                            S * kWarps);
+  // the ticket counters start at zero (one small memset; a sequence of one
+  // piece takes no ticket, so with S = 1 none is needed)
+  if (pl.S != 1) {
+    e = cudaMemsetAsync(tickets, 0, (size_t)pl.P * sizeof(unsigned), s);
+    if (e != cudaSuccess) return e;
+  }
+  kern<<<pl.grid, kThreads, kSmemBytes, s>>>(tmK, tmV, static_cast<const __nv_bfloat16*>(Q),
+                                             static_cast<__nv_bfloat16*>(O), ws_o, ws_ml,
+                                             tickets, pl, qk_scale_log2, err);
+  return cudaGetLastError();
+}
+
+// The partition for a shape; false if the device's SM count cannot be read.
+bool make_plan(int B, int Hkv, int Lk, int requested, DecodePlan* pl) {
+  const int sms = sm_count();
+  if (sms <= 0) return false;
+  plan_init(pl, B * Hkv, Lk, requested, sms);
+  return true;
+}
+
+// Workspace layout: ticket counters [P] (padded to 256 bytes), partial o
+// [slots][G][128] fp32 (padded to 256 bytes), partial (m, l) [slots][G].
+size_t ws_tickets_bytes(const DecodePlan& pl) {
+  return ((size_t)pl.P * sizeof(unsigned) + 255) & ~(size_t)255;
+}
+size_t ws_o_bytes(const DecodePlan& pl, int G) {
+  return ((size_t)plan_slots(pl) * G * kD * sizeof(float) + 255) & ~(size_t)255;
 }
 
 }  // namespace
@@ -393,56 +628,52 @@ int decode_num_splits(int B, int Hq, int Hkv, int Lk, int d, int requested) {
   (void)Hq;
   (void)d;
   if (requested > 0) return requested;
-  const int sms = sm_count();
-  if (sms <= 0) return 0;
-  // The persistent grid has one CTA per SM.  Take the smallest S whose items
-  // (B * Hkv * S) keep the SMs at least 95 % busy (items / (rounds * SMs)),
-  // with segments of at least 128 keys (one chunk per warp); else the best S.
-  const int64_t pairs = (int64_t)B * Hkv;
-  const int64_t max_s = (Lk + 127) / 128 < 1 ? 1 : (Lk + 127) / 128;
-  int best_s = 1;
-  double best_eff = -1.0;
-  for (int64_t S = 1; S <= max_s && S <= 4096; ++S) {
-    const int64_t items = pairs * S;
-    const int64_t rounds = (items + sms - 1) / sms;
-    const double eff = (double)items / (double)(rounds * sms);
-    if (eff >= 0.95) return (int)S;
-    if (eff > best_eff) {
-      best_eff = eff;
-      best_s = (int)S;
-    }
-  }
-  return best_s;
+  DecodePlan pl;
+  if (!make_plan(B, Hkv, Lk, 0, &pl)) return 0;
+  // The automatic partition cuts a sequence of nck chunks into at most
+  // ceil((nck - 1) / q) + 1 segments, q = the fewest chunks of any range.
+  const int64_t most = ((int64_t)pl.nck - 1 + pl.q - 1) / pl.q + 1;
+  return (int)(most < pl.grid ? most : pl.grid);
 }
 
-size_t decode_workspace_bytes(int B, int Hq, int d, int S) {
-  const size_t n = (size_t)B * Hq * S * kWarps;       // one partial state per warp
-  const size_t o_bytes = (n * d * sizeof(float) + 255) & ~(size_t)255;
-  return o_bytes + n * 2 * sizeof(float);
+size_t decode_workspace_bytes(int B, int Hq, int Hkv, int Lk, int d, int requested) {
+  (void)d;
+  DecodePlan pl;
+  if (!make_plan(B, Hkv, Lk, requested, &pl)) {
+    if (requested <= 0) return 0;
+    plan_init(&pl, B * Hkv, Lk, requested, 1);    // explicit S: independent of the device
+  }
+  const int G = Hq / Hkv;
+  return ws_tickets_bytes(pl) + ws_o_bytes(pl, G) + (size_t)plan_slots(pl) * G * sizeof(float2);
 }
 
 cudaError_t launch_decode_splitkv(const void* Q, const void* K, const void* V, void* O, int B,
-                                  int Hq, int Hkv, int Lk, int d, float scale, int S,
+                                  int Hq, int Hkv, int Lk, int d, float scale, int requested,
                                   void* workspace, unsigned* err, cudaStream_t s) {
+  (void)d;
+  DecodePlan pl;
+  if (!make_plan(B, Hkv, Lk, requested, &pl)) return cudaErrorInvalidValue;
   const uint64_t rows = (uint64_t)B * Hkv * Lk;
   CUtensorMap tmK, tmV;
   if (!encode_tmap_2d(&tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, kD, rows, kD * 2, 64, kCK, true) ||
       !encode_tmap_2d(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, kD, rows, kD * 2, 64, kCK, true))
     return cudaErrorInvalidValue;
-  const size_t n = (size_t)B * Hq * S * kWarps;
-  float* part_o = static_cast<float*>(workspace);
-  float* part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                            ((n * d * sizeof(float) + 255) & ~(size_t)255));
-  switch (Hq / Hkv) {
-    case 1: return launch_g<1>(tmK, tmV, Q, O, B, Hq, Hkv, Lk, scale, S, part_o, part_ml, err, s);
-    case 2: return launch_g<2>(tmK, tmV, Q, O, B, Hq, Hkv, Lk, scale, S, part_o, part_ml, err, s);
-    case 4: return launch_g<4>(tmK, tmV, Q, O, B, Hq, Hkv, Lk, scale, S, part_o, part_ml, err, s);
-    case 8: return launch_g<8>(tmK, tmV, Q, O, B, Hq, Hkv, Lk, scale, S, part_o, part_ml, err, s);
+  const int G = Hq / Hkv;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  unsigned* tickets = reinterpret_cast<unsigned*>(ws);
+  float* ws_o = reinterpret_cast<float*>(ws + ws_tickets_bytes(pl));
+  float2* ws_ml = reinterpret_cast<float2*>(ws + ws_tickets_bytes(pl) + ws_o_bytes(pl, G));
+  switch (G) {
+    case 1: return launch_g<1>(tmK, tmV, Q, O, pl, scale, ws_o, ws_ml, tickets, err, s);
+    case 2: return launch_g<2>(tmK, tmV, Q, O, pl, scale, ws_o, ws_ml, tickets, err, s);
+    case 4: return launch_g<4>(tmK, tmV, Q, O, pl, scale, ws_o, ws_ml, tickets, err, s);
+    case 8: return launch_g<8>(tmK, tmV, Q, O, pl, scale, ws_o, ws_ml, tickets, err, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace rf
+
 
 // ====================================================================
 // Allocation-free variant of rf_attn_decode_splitkv.
@@ -500,8 +731,8 @@ extern "C" rf_status rf_attn_decode_splitkv_noalloc(const void* Q, const void* K
                                                     void* O, int B, int Hq, int Hkv, int Lk,
                                                     int d, float scale, int num_splits,
                                                     rf_stream_t stream) {
-  // Nothing in the scratch has to start at zero: the partial kernel writes
-  // every (batch, head, segment) state that the merge kernel reads.
+  // Nothing in the scratch has to start at zero: the launcher zeroes the
+  // ticket counters, and every partial state is written before it is read.
   void* scratch = rf::decode_scratch_address();
   if (!scratch) return RF_ERR_CUDA;
   return rf_attn_decode_splitkv(Q, K, V, O, B, Hq, Hkv, Lk, d, scale, num_splits, scratch,

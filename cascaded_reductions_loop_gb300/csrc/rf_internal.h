@@ -65,9 +65,9 @@ cudaError_t launch_attn_fwd_bf16_tc_varlen(const void* Q, const void* K, const v
                                            int causal, unsigned* err, cudaStream_t s);
 
 int decode_num_splits(int B, int Hq, int Hkv, int Lk, int d, int requested);
-size_t decode_workspace_bytes(int B, int Hq, int d, int S);
+size_t decode_workspace_bytes(int B, int Hq, int Hkv, int Lk, int d, int requested);
 cudaError_t launch_decode_splitkv(const void* Q, const void* K, const void* V, void* O, int B,
-                                  int Hq, int Hkv, int Lk, int d, float scale, int S,
+                                  int Hq, int Hkv, int Lk, int d, float scale, int requested,
                                   void* workspace, unsigned* err, cudaStream_t s);
 
 // Latent-KV decode: Q [B][Hq][576], CKV [B][Lk][576], O [B][Hq][512] (bf16).

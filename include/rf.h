@@ -158,14 +158,16 @@ rf_status rf_attn_fwd_varlen(int dtype, const void* Q, const void* K, const void
                              float scale, int causal, rf_stream_t stream);
 
 /*
- * Number of key segments rf_attn_decode_splitkv uses for this shape when its
- * num_splits argument is `num_splits` (0 = automatic choice, which sizes the
- * grid of the partial kernel to the device's SM count).  Returns 0 for an
- * invalid shape.
+ * Number of key segments rf_attn_decode_splitkv cuts a (b, kv head) sequence
+ * into for this shape when its num_splits argument is `num_splits`: that
+ * number itself when it is > 0; for 0 (the automatic partition, sized to the
+ * device's SM count) the most segments any one sequence can be cut into.
+ * Returns 0 for an invalid shape, or for 0 when no device can be queried.
  */
 int rf_attn_decode_splitkv_num_splits(int B, int Hq, int Hkv, int Lk, int d, int num_splits);
 
-/* Workspace bytes rf_attn_decode_splitkv needs for the same arguments. */
+/* Workspace bytes rf_attn_decode_splitkv needs for the same arguments (for
+ * num_splits = 0 it depends on the current device's SM count). */
 size_t rf_attn_decode_splitkv_workspace_size(int B, int Hq, int Hkv, int Lk, int d,
                                              int num_splits);
 
@@ -175,18 +177,24 @@ size_t rf_attn_decode_splitkv_workspace_size(int B, int Hq, int Hkv, int Lk, int
  * (b, query head):
  *   Q   [B][Hq][d] bf16;  K, V  [B][Hkv][Lk][d] bf16;  O  [B][Hq][d] bf16.
  * Grouped-query attention: query head hq reads K/V head hq / (Hq / Hkv).
- * Kernel 1 (persistent) splits each (b, kv head) sequence into S key
- * segments and writes, per (b, hq, segment, warp), the partial state
- * (m, l, o) with o unnormalised (m in log2 units); kernel 2 merges the
- * states of each (b, hq): M = max m_j, L = sum l_j 2^(m_j - M),
- * O = sum o_j 2^(m_j - M) / L.
+ * One kernel (a persistent grid of at most one CTA per SM) cuts the
+ * (b, kv head) sequences into key segments, reduces each segment to a
+ * partial state (m, l, o) per query head (o unnormalised, m in log2 units)
+ * and merges the segments of a sequence: M = max m_j,
+ * L = sum l_j 2^(m_j - M), O = sum o_j 2^(m_j - M) / L.  The merge is done
+ * by the CTA that finishes a sequence's last segment, always in key order,
+ * so the result does not depend on which CTA that is.
  *   Sizes   B, Lk >= 1; d = 128; Hq / Hkv in {1, 2, 4, 8}; scale finite, > 0.
- *   num_splits  0 = automatic, else 1..Lk segments.
+ *   num_splits  0 = automatic: the 32-key chunks of all sequences, end to
+ *               end, are cut into one equal range per CTA (a sequence may be
+ *               cut into several segments, another lie within one range);
+ *               1..Lk = each sequence cut into that many equal segments.
  *   workspace   device buffer of at least
  *               rf_attn_decode_splitkv_workspace_size(...) bytes, 16-byte
- *               aligned, owned by the caller; holds the partial states
- *               between the two kernels.  Its contents need not be
- *               initialised and are unspecified on return.
+ *               aligned, owned by the caller; holds a ticket counter per
+ *               sequence (zeroed by a memset on `stream` before the kernel)
+ *               and the partial states of segments.  Its contents need not
+ *               be initialised and are unspecified on return.
  * Errors: RF_ERR_INVALID_ARG, RF_ERR_UNSUPPORTED, RF_ERR_WORKSPACE, RF_ERR_CUDA.
  */
 rf_status rf_attn_decode_splitkv(const void* Q, const void* K, const void* V, void* O,

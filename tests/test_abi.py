@@ -85,8 +85,11 @@ def test_validation_rejects_bad_arguments_without_a_gpu(rf):
     # an explicit split count needs no device: a too-small workspace is caught on the host
     assert L.rf_attn_decode_splitkv(p, p, p, p, 1, 8, 2, 64, 128, 0.1, 4, p, 16, None) == rf.RF_ERR_WORKSPACE
     assert L.rf_attn_decode_splitkv(p, p, p, p, 1, 8, 2, 64, 128, 0.1, 4, null, 1 << 20, None) == rf.RF_ERR_WORKSPACE
-    # one (m, l, o) partial state per (batch, query head, segment, warp of 4)
-    assert rf.rf_attn_decode_splitkv_workspace_size(2, 8, 2, 64, 128, 4) == 2 * 8 * 4 * 4 * (128 + 2) * 4
+    # ticket counter per (batch, kv head) padded to 256 bytes, then one (m, l, o)
+    # partial state per (batch, query head, segment): o padded to 256 bytes, then (m, l)
+    P, G, S = 2 * 2, 8 // 2, 4
+    assert rf.rf_attn_decode_splitkv_workspace_size(2, 8, 2, 64, 128, S) == \
+        256 + P * S * G * 128 * 4 + P * S * G * 2 * 4
     assert rf.rf_attn_decode_splitkv_num_splits(1, 6, 4, 64, 128, 0) == 0
     # latent-KV decode: sizes, head count, latent widths, workspace of a split request
     M = L.rf_mla_decode

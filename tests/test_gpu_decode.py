@@ -1,5 +1,6 @@
-"""GPU parity: multi-segment split-KV decode attention (partial + merge
-kernels) against the fp64 three-pass oracle, through the C ABI."""
+"""GPU parity: multi-segment split-KV decode attention (segment partial
+states merged inside the same kernel) against the fp64 three-pass oracle,
+through the C ABI."""
 import pytest
 import torch
 
@@ -43,6 +44,20 @@ def test_decode_small(rf, B, Hq, Hkv, Lk, splits):
     q, k, v = I.decode_inputs(sh)
     o = _run(rf, q, k, v, sh.scale, splits)
     assert_bf16_close(o, A.decode_attention(q, k, v, sh.scale), f"decode {B},{Hq},{Hkv},{Lk},{splits}")
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Lk", [
+    (1, 8, 1, 20000), (1, 4, 4, 5000), (2, 32, 8, 70), (1, 16, 2, 40000), (3, 8, 8, 33)])
+def test_decode_sequence_cut_by_many_ctas(rf, B, Hq, Hkv, Lk):
+    """The automatic partition gives every CTA the same number of key chunks,
+    so few, long sequences are each cut into many segments (one sequence of
+    20000 keys: one per SM), merged by whichever CTA finishes last; and with
+    fewer chunks than SMs each CTA gets one chunk."""
+    sh = I.AttnShape(B, Hq, Hkv, 1, Lk, 128, "bf16", seed=2000 + Lk)
+    q, k, v = I.decode_inputs(sh)
+    assert rf.rf_attn_decode_splitkv_num_splits(B, Hq, Hkv, Lk, 128, 0) >= 1
+    o = _run(rf, q, k, v, sh.scale)
+    assert_bf16_close(o, A.decode_attention(q, k, v, sh.scale), f"decode {B},{Hq},{Hkv},{Lk}")
 
 
 def test_decode_2k_full(rf):

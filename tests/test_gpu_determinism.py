@@ -2,8 +2,8 @@
 every call, also when the calls are interleaved with the other paths (which
 changes what sits in L2 and how the CTAs race).  A lost ordering between
 cooperating CTAs or kernels -- the MoE gate's cluster exchange of partial
-scores, the split-KV merge launched as a programmatic dependent, the FP8
-GEMM started before the quantisation kernel has finished -- would show up as
+scores, the split-KV merge by the last CTA to finish a sequence, the FP8
+GEMM reading a block of codes before its quantiser warps published it -- would show up as
 a call whose bits differ."""
 import pytest
 import torch

@@ -53,7 +53,7 @@ def test_noalloc_refuses_requests_beyond_its_scratch():
     import cascaded_reductions_loop_gb300 as rf
 
     B, Hq, Hkv, Lk, d = 32, 32, 8, 32768, 128
-    splits = 1024                     # partial states of 32*32*1024*4*(128+2)*4 B > 16 MiB
+    splits = 1024                     # partial states of 32*32*1024*(128+2)*4 B > 16 MiB
     assert rf.rf_attn_decode_splitkv_workspace_size(B, Hq, Hkv, Lk, d, splits) > \
         rf.RF_DECODE_NOALLOC_SCRATCH_BYTES
     q = torch.zeros(B, Hq, d, dtype=torch.bfloat16, device="cuda")
