@@ -16,7 +16,7 @@ def _ops():
 
 def test_step_calls_and_order():
     assert [op.name for op in bench.make_ops()] == [
-        "decode_32k", "bert_prefill", "moe_gate", "fp8_gemm", "decode_2k"]
+        "decode_2k", "moe_gate", "fp8_gemm", "bert_prefill", "decode_32k"]
 
 
 def test_decode_bytes_and_flops():
@@ -75,7 +75,7 @@ def test_roofline_time_and_bound_at_fallback_peaks():
 
 def test_workload_config_names_the_calls():
     step = bench.workload_config(bench.make_ops(), 1)
-    assert step["workload"] == "decode32k+bert_prefill+moe_gate+fp8_gemm+decode2k"
+    assert step["workload"] == "decode2k+moe_gate+fp8_gemm+bert_prefill+decode32k"
     assert "exceed" not in step["l2"] and "> 129 MB L2" in step["l2"]
     mla = bench.workload_config([_ops()["mla_decode"]], 1)
     assert mla["workload"] == "mla_decode" and "mla" in mla and "decode" not in mla
