@@ -25,8 +25,8 @@
 // Per CTA: its Q dims sit in tensor memory (written once by the softmax
 // warps) as the A operand of the score products, and so does P (bf16) for the
 // P . V products; the cache rows stream by TMA through a 4-stage ring (64 rows
-// x 64 dims per block, 128-byte swizzle), with the tiles beyond the ring
-// prefetched into L2; S has one buffer in tensor memory, O accumulates there.
+// x 64 dims per block, 128-byte swizzle; prefetching further tiles into L2
+// measured slower); S has one buffer in tensor memory, O accumulates there.
 // The MMA warp issues whichever product is ready (S_t once the softmax warps
 // have taken S_{t-1} and the tile has landed; P_j V_j once P_j is written).
 //
@@ -65,7 +65,6 @@ constexpr int BH = 128;                            // head rows (MMA M)
 constexpr int BN = 64;                             // cache rows per tile
 constexpr int kMaxBlk = 5;                         // 64-dim blocks per CTA
 constexpr int kStages = 4;
-constexpr int kPrefetch = 4;                       // tiles beyond the ring prefetched into L2
 constexpr int kChBytes = BN * 128;                 // one 64-dim block of a tile: 8 KB
 constexpr int kStageBytes = kMaxBlk * kChBytes;    // 40 KB
 constexpr int kXBytes = BH * BN * 4;               // one partial score tile: 32 KB
@@ -170,12 +169,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ------------------------------------------------ TMA producer
       const uint64_t pol = policy_evict_first();       // every cache row is read once
       const int32_t row0 = b * Lk + lo;
-      // next tile to prefetch into L2; never the segment's last tile, the one
-      // that can reach past the end of the tensor
-      int issued = 0, pf = kStages;
+      int issued = 0;
       for (int t = 0; t < nt && !*abort_flag; ++t) {
-        for (; pf < nt - 1 && pf < t + kStages + kPrefetch; ++pf)
-          for (int c = 0; c < nblk; ++c) tma_prefetch_2d(&tmC, 64 * dim_block(rank, c), row0 + pf * BN);
         const int st = t % kStages;
         if (t >= kStages &&
             !mbar_wait(smem_u32(&bars->empty[st]), (uint32_t)(((t / kStages) - 1) & 1))) {
