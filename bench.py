@@ -244,14 +244,19 @@ class Step:
             d["fp8_gemm"] = [x_d, self.wq, self.sw]
             self.sx = torch.empty(sf.M, dtype=torch.float32, device=cuda)
             self.xq = torch.empty(sf.M, sf.K, dtype=torch.uint8, device=cuda)
+        if "moe_gate" in d:
+            # W_gate in the [D][E] layout of the problem statement (x @ W_gate);
+            # the generator (and the oracle) hold it as [E][D]
+            x_m, w_m = d["moe_gate"]
+            d["moe_gate"] = [x_m, w_m.t().contiguous()]
         self.calls = {
             "decode_32k": lambda: rf.rf_attn_decode_splitkv(*d["decode_32k"], self.o32, s32.scale,
                                                             self.ws32, args_splits(32768)),
             "bert_prefill": lambda: rf.rf_attn_fwd(*d["bert_prefill"], self.ob, sb.scale),
             "bert_prefill_causal": lambda: rf.rf_attn_fwd(*d["bert_prefill_causal"], self.ob,
                                                           sb.scale, 1),
-            "moe_gate": lambda: rf.rf_moe_gate_topk_softmax(*d["moe_gate"], sm.k, self.idx,
-                                                            self.wts),
+            "moe_gate": lambda: rf.rf_moe_gate_topk_softmax_ex(*d["moe_gate"], sm.k, rf.RF_GATE_W_DE,
+                                                               self.idx, self.wts),
             "fp8_gemm": lambda: rf.rf_absmax_fp8_gemm(*d["fp8_gemm"], self.y, self.wsf),
             "decode_2k": lambda: rf.rf_attn_decode_splitkv(*d["decode_2k"], self.o2, s2.scale,
                                                            self.ws2, args_splits(2048)),
@@ -534,6 +539,8 @@ def run_ours(args, world, rank, local):
     call_host = dict(host)
     if "fp8_gemm" in host:
         call_host["fp8_gemm"] = [host["fp8_gemm"][0], step.wq.cpu(), step.sw.cpu()]
+    if "moe_gate" in host:
+        call_host["moe_gate"] = [host["moe_gate"][0], host["moe_gate"][1].t().contiguous()]
 
     # parity: the first call of every op against the oracle (rank 0)
     parity = None
@@ -672,7 +679,7 @@ def workload_config(ops, world):
     if names & {"bert_prefill", "bert_prefill_causal"}:
         cfg["prefill"] = "B8 H16 L512 d64 bf16"
     if "moe_gate" in names:
-        cfg["moe"] = "T8192 D4096 E64 top2 bf16"
+        cfg["moe"] = "T8192 D4096 E64 top2 bf16, W_gate [D][E]"
     if "fp8_gemm" in names:
         cfg["fp8"] = "M=N=K=4096 e4m3 (bf16 X in, bf16 Y out)"
     if "mla_decode" in names:

@@ -24,18 +24,19 @@ __all__ = [
     "rf_attn_decode_splitkv_num_splits",
     "rf_attn_decode_splitkv_workspace_size", "rf_attn_decode_splitkv_noalloc",
     "RF_DECODE_NOALLOC_SCRATCH_BYTES", "rf_mla_decode", "rf_mla_decode_num_splits",
-    "rf_mla_decode_workspace_size", "rf_moe_gate_topk_softmax",
+    "rf_mla_decode_workspace_size", "rf_moe_gate_topk_softmax", "rf_moe_gate_topk_softmax_ex",
     "rf_absmax_fp8_gemm", "rf_absmax_fp8_gemm_workspace_size", "rf_absmax_quant_fp8",
     "rf_selftest_wait_timeout",
     "RF_OK", "RF_ERR_INVALID_ARG", "RF_ERR_UNSUPPORTED", "RF_ERR_WORKSPACE", "RF_ERR_CUDA",
     "RF_ERR_DEVICE_TIMEOUT", "RF_ERR_DEVICE_INPUT", "RF_ERR_DEVICE_LAYOUT", "RF_F32", "RF_BF16",
-    "RF_ATTN_AUTO", "RF_ATTN_INCREMENTAL", "RF_ATTN_TWO_PASS",
+    "RF_ATTN_AUTO", "RF_ATTN_INCREMENTAL", "RF_ATTN_TWO_PASS", "RF_GATE_W_ED", "RF_GATE_W_DE",
 ]
 
 RF_OK, RF_ERR_INVALID_ARG, RF_ERR_UNSUPPORTED, RF_ERR_WORKSPACE, RF_ERR_CUDA, \
     RF_ERR_DEVICE_TIMEOUT, RF_ERR_DEVICE_INPUT, RF_ERR_DEVICE_LAYOUT = range(8)
 RF_F32, RF_BF16 = 0, 1
 RF_ATTN_AUTO, RF_ATTN_INCREMENTAL, RF_ATTN_TWO_PASS = 0, 1, 2
+RF_GATE_W_ED, RF_GATE_W_DE = 0, 1                # layouts of W_gate: [E][D], [D][E]
 RF_DECODE_NOALLOC_SCRATCH_BYTES = 16 << 20   # as in rf.h
 
 LIB_PATH = _build.LIB_PATH
@@ -69,6 +70,7 @@ _SIGS = {
     "rf_mla_decode_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I]),
     "rf_mla_decode": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
     "rf_moe_gate_topk_softmax": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P]),
+    "rf_moe_gate_topk_softmax_ex": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "rf_absmax_fp8_gemm_workspace_size": (_Z, [_I, _I, _I]),
     "rf_absmax_fp8_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _Z, _P]),
     "rf_absmax_quant_fp8": (_I, [_P, _I, _I, _P, _P, _P]),
@@ -271,6 +273,26 @@ def rf_moe_gate_topk_softmax(x, w_gate, k: int, idx, weights, stream=None) -> No
     _check(lib.rf_moe_gate_topk_softmax(_ptr(x), _ptr(w_gate), T, D, E, int(k), _ptr(idx),
                                         _ptr(weights), _stream(stream)),
            "rf_moe_gate_topk_softmax")
+
+
+def rf_moe_gate_topk_softmax_ex(x, w_gate, k: int, w_layout: int, idx, weights,
+                                stream=None) -> None:
+    """Fused MoE gate with the layout of W_gate given.  x: [T,D] bf16;
+    w_gate: [E,D] bf16 (RF_GATE_W_ED) or [D,E] bf16 (RF_GATE_W_DE, E a
+    multiple of 64, at most 256); idx: [T,k] int32 out; weights: [T,k] fp32 out."""
+    T, D = x.shape
+    if w_layout == RF_GATE_W_DE:
+        E = w_gate.shape[1]
+        _need(w_gate, torch.bfloat16, (D, E), "w_gate")
+    else:
+        E = w_gate.shape[0]
+        _need(w_gate, torch.bfloat16, (E, D), "w_gate")
+    _need(x, torch.bfloat16, (T, D), "x")
+    _need(idx, torch.int32, (T, k), "idx")
+    _need(weights, torch.float32, (T, k), "weights")
+    _check(lib.rf_moe_gate_topk_softmax_ex(_ptr(x), _ptr(w_gate), T, D, E, int(k), int(w_layout),
+                                           _ptr(idx), _ptr(weights), _stream(stream)),
+           "rf_moe_gate_topk_softmax_ex")
 
 
 def rf_absmax_fp8_gemm_workspace_size(M, N, K) -> int:

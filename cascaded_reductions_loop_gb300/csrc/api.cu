@@ -355,16 +355,23 @@ rf_status rf_mla_decode(const void* Q, const void* CKV, void* O, int B, int Hq, 
                                      reinterpret_cast<cudaStream_t>(stream)));
 }
 
-rf_status rf_moe_gate_topk_softmax(const void* X, const void* Wg, int T, int D, int E, int k,
-                                   int32_t* idx, float* w, rf_stream_t stream) {
+rf_status rf_moe_gate_topk_softmax_ex(const void* X, const void* Wg, int T, int D, int E, int k,
+                                      int w_layout, int32_t* idx, float* w, rf_stream_t stream) {
   if (!ptr_ok(X) || !ptr_ok(Wg) || !ptr_ok(idx) || !ptr_ok(w)) return RF_ERR_INVALID_ARG;
   if (T < 1 || D < 1 || E < 1 || k < 1 || k > E) return RF_ERR_INVALID_ARG;
   if (D % 8 != 0) return RF_ERR_INVALID_ARG;   // 16-byte row pitch for TMA
+  if (w_layout != RF_GATE_W_ED && w_layout != RF_GATE_W_DE) return RF_ERR_INVALID_ARG;
   if (E > 256 || k > 8) return RF_ERR_UNSUPPORTED;
+  if (w_layout == RF_GATE_W_DE && E % 64 != 0) return RF_ERR_UNSUPPORTED;
   unsigned* err = device_error_word();
   if (!err) return RF_ERR_CUDA;
-  return from_cuda(launch_moe_gate(X, Wg, T, D, E, k, idx, w, err,
+  return from_cuda(launch_moe_gate(X, Wg, T, D, E, k, w_layout == RF_GATE_W_DE, idx, w, err,
                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+rf_status rf_moe_gate_topk_softmax(const void* X, const void* Wg, int T, int D, int E, int k,
+                                   int32_t* idx, float* w, rf_stream_t stream) {
+  return rf_moe_gate_topk_softmax_ex(X, Wg, T, D, E, k, RF_GATE_W_ED, idx, w, stream);
 }
 
 size_t rf_absmax_fp8_gemm_workspace_size(int M, int N, int K) {

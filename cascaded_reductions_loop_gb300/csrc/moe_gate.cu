@@ -5,9 +5,12 @@
 // tiles fill the SMs evenly) and one slice of the reduction dimension D; the
 // CTAs covering the slices of the same tile form a thread-block cluster
 // (split-K).  Per CTA: a TMA producer warp streams bm x 64 tiles of x and
-// E x 64 tiles of W_gate (both K-major, 128-byte swizzled) through a ring of
+// the matching 64-dim slices of W_gate (128-byte swizzled) through a ring of
 // stages (for E <= 64 two adjacent tiles of each per stage, so that every
-// row's 256 bytes are fetched together); one thread issues tcgen05.mma
+// row's 256 bytes are fetched together).  W_gate may be expert-major, [E][D]
+// (a K-major B operand: E rows of 64 dims per slice), or dim-major, [D][E]
+// (an MN-major B operand: per slice, 64 rows of D, each 64 experts wide, one
+// 8 KB box per 64 experts); one thread issues tcgen05.mma
 // kind::f16 (bf16 x bf16 -> fp32, M = 128, N = NE, the expert count rounded
 // up to 32, 64, 128 or 256) into tensor memory.  The epilogue warps copy the
 // partial score tile out of TMEM: after a cluster barrier (every peer's ring
@@ -239,12 +242,16 @@ __device__ __forceinline__ void st_peer_v4(uint32_t addr, float4 v) {
                : "memory");
 }
 
-template <int NE>
+// DE: W_gate is [D][E] (E a multiple of 64); else [E][D].
+template <int NE, bool DE>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gate_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                     int T, int D, int E, int k, int bm, int32_t* __restrict__ idx_out,
                     float* __restrict__ w_out, unsigned* err) {
   using C = GateCfg<NE>;
+  // [D][E]: the MN-major B operand; its 64-expert atoms are 8 KB apart
+  constexpr uint32_t kIdesc = DE ? make_idesc(BM, NE, /*bf16*/ 1, 0, /*B MN-major*/ 1) : C::kIdesc;
+  constexpr int kAtom = 64 * BK * 2;               // 64 experts x 64 dims, bf16
   constexpr int KB = C::KB, kRedStride = C::kRedStride;
   const Ring rg = ring_layout<NE>(bm, E);
   const int nst = rg.stages;
@@ -279,7 +286,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int bx = 0; bx < C::kBoxes; ++bx) {
       const int x = ((int)crank + i * (int)csize) * KB + bx * BK;
       tma_load_2d_hint(smem_u32(a + bx * rg.a_box), &tmX, bar, x, m0, pol_x);
-      tma_load_2d_hint(smem_u32(a + C::kBoxes * rg.a_box + bx * rg.w_box), &tmW, bar, x, 0, pol_w);
+      uint8_t* wb = a + C::kBoxes * rg.a_box + bx * rg.w_box;
+      if (DE) {
+        for (int e0 = 0; e0 < E; e0 += 64)       // box: 64 experts x 64 rows of D
+          tma_load_2d_hint(smem_u32(wb + (e0 / 64) * kAtom), &tmW, bar, e0, x, pol_w);
+      } else {
+        tma_load_2d_hint(smem_u32(wb), &tmW, bar, x, 0, pol_w);
+      }
     }
   };
 
@@ -337,9 +350,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < KB / 16; ++kk) {
           const uint32_t ao = (kk / (BK / 16)) * rg.a_box + (kk % (BK / 16)) * 32;
-          const uint32_t bo = (kk / (BK / 16)) * rg.w_box + (kk % (BK / 16)) * 32;
-          mma_bf16_ss(tmem, sw128_desc(a + ao, 1024, 16), sw128_desc(b + bo, 1024, 16), C::kIdesc,
-                      (i | kk) != 0);
+          // K-major: 16 dims = 32 bytes along a row; MN-major: 16 rows of D
+          const uint32_t bo = (kk / (BK / 16)) * rg.w_box + (kk % (BK / 16)) * (DE ? 16 * 128 : 32);
+          mma_bf16_ss(tmem, sw128_desc(a + ao, 1024, 16),
+                      sw128_desc(b + bo, 1024, DE ? (uint32_t)kAtom : 16u), kIdesc, (i | kk) != 0);
         }
         mma_commit(smem_u32(&empty[slot]));
       }
@@ -427,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Host side: tensor maps, the cluster split and the launch for one width.
-template <int NE>
+template <int NE, bool DE>
 cudaError_t launch_ne(const void* X, const void* Wg, int T, int D, int E, int k, int32_t* idx,
                       float* w, unsigned* err, cudaStream_t s) {
   using C = GateCfg<NE>;
@@ -471,11 +485,13 @@ cudaError_t launch_ne(const void* X, const void* Wg, int T, int D, int E, int k,
   if (tiles > 65535) return cudaErrorInvalidValue;
   if (!encode_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)D, (uint64_t)T,
                       (uint64_t)D * 2, BK, (uint32_t)bm, true) ||
-      !encode_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Wg, (uint64_t)D, (uint64_t)E,
-                      (uint64_t)D * 2, BK, (uint32_t)E, true))
+      !(DE ? encode_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Wg, (uint64_t)E, (uint64_t)D,
+                            (uint64_t)E * 2, 64, BK, true)
+           : encode_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Wg, (uint64_t)D, (uint64_t)E,
+                            (uint64_t)D * 2, BK, (uint32_t)E, true)))
     return cudaErrorInvalidValue;
 
-  cudaError_t e = cudaFuncSetAttribute(moe_gate_kernel<NE>,
+  cudaError_t e = cudaFuncSetAttribute(moe_gate_kernel<NE, DE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -490,17 +506,23 @@ cudaError_t launch_ne(const void* X, const void* Wg, int T, int D, int E, int k,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, moe_gate_kernel<NE>, tmX, tmW, T, D, E, k, bm, idx, w, err);
+  return cudaLaunchKernelEx(&cfg, moe_gate_kernel<NE, DE>, tmX, tmW, T, D, E, k, bm, idx, w, err);
 }
 
 }  // namespace
 
 cudaError_t launch_moe_gate(const void* X, const void* Wg, int T, int D, int E, int k,
-                            int32_t* idx, float* w, unsigned* err, cudaStream_t s) {
-  if (E <= 32) return launch_ne<32>(X, Wg, T, D, E, k, idx, w, err, s);
-  if (E <= 64) return launch_ne<64>(X, Wg, T, D, E, k, idx, w, err, s);
-  if (E <= 128) return launch_ne<128>(X, Wg, T, D, E, k, idx, w, err, s);
-  if (E <= 256) return launch_ne<256>(X, Wg, T, D, E, k, idx, w, err, s);
+                            bool w_de, int32_t* idx, float* w, unsigned* err, cudaStream_t s) {
+  if (w_de) {                                      // [D][E]: E % 64 == 0, checked by the caller
+    if (E == 64) return launch_ne<64, true>(X, Wg, T, D, E, k, idx, w, err, s);
+    if (E == 128) return launch_ne<128, true>(X, Wg, T, D, E, k, idx, w, err, s);
+    if (E == 192 || E == 256) return launch_ne<256, true>(X, Wg, T, D, E, k, idx, w, err, s);
+    return cudaErrorInvalidValue;
+  }
+  if (E <= 32) return launch_ne<32, false>(X, Wg, T, D, E, k, idx, w, err, s);
+  if (E <= 64) return launch_ne<64, false>(X, Wg, T, D, E, k, idx, w, err, s);
+  if (E <= 128) return launch_ne<128, false>(X, Wg, T, D, E, k, idx, w, err, s);
+  if (E <= 256) return launch_ne<256, false>(X, Wg, T, D, E, k, idx, w, err, s);
   return cudaErrorInvalidValue;
 }
 

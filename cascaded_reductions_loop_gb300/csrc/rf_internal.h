@@ -76,8 +76,9 @@ size_t mla_workspace_bytes(int B, int Hq, int S);
 cudaError_t launch_mla_decode(const void* Q, const void* CKV, void* O, int B, int Hq, int Lk,
                               float scale, int S, void* workspace, unsigned* err, cudaStream_t s);
 
+// w_de: W_gate is [D][E] (E in {64, 128, 192, 256}); else [E][D].
 cudaError_t launch_moe_gate(const void* X, const void* Wg, int T, int D, int E, int k,
-                            int32_t* idx, float* w, unsigned* err, cudaStream_t s);
+                            bool w_de, int32_t* idx, float* w, unsigned* err, cudaStream_t s);
 
 // FP8: the workspace holds the kernel's row counters, then (when the caller
 // keeps no copy) the codes and the row scales.

@@ -298,6 +298,22 @@ rf_status rf_mla_decode(const void* Q, const void* CKV, void* O, int B, int Hq, 
 rf_status rf_moe_gate_topk_softmax(const void* X, const void* Wg, int T, int D, int E, int k,
                                    int32_t* idx, float* w, rf_stream_t stream);
 
+/* Layouts of W_gate for rf_moe_gate_topk_softmax_ex. */
+#define RF_GATE_W_ED 0 /* [E][D]: expert-major, a linear layer's weight  */
+#define RF_GATE_W_DE 1 /* [D][E]: dim-major, scores = X . W_gate           */
+
+/*
+ * rf_moe_gate_topk_softmax with the layout of W_gate given: the same
+ * computation, arguments and errors, with
+ *   w_layout  RF_GATE_W_ED: Wg [E][D] (as rf_moe_gate_topk_softmax);
+ *             RF_GATE_W_DE: Wg [D][E] bf16, scores[t][e] = sum_d X[t][d]
+ *             Wg[d][e] ([E] §4.2 writes the gate as x . W_gate); E must be
+ *             64, 128, 192 or 256 (else RF_ERR_UNSUPPORTED); any other
+ *             w_layout value: RF_ERR_INVALID_ARG.
+ */
+rf_status rf_moe_gate_topk_softmax_ex(const void* X, const void* Wg, int T, int D, int E, int k,
+                                      int w_layout, int32_t* idx, float* w, rf_stream_t stream);
+
 /*
  * Workspace bytes rf_absmax_fp8_gemm needs when neither sx_out nor xq_out is
  * given (0 for an invalid shape).  With both outputs given it needs only the

@@ -120,6 +120,12 @@ def test_validation_rejects_bad_arguments_without_a_gpu(rf):
     assert L.rf_moe_gate_topk_softmax(p, p, 16, 128, 257, 2, p, p, None) == rf.RF_ERR_UNSUPPORTED
     assert L.rf_moe_gate_topk_softmax(p, p, 16, 128, 4, 5, p, p, None) == rf.RF_ERR_INVALID_ARG
     assert L.rf_moe_gate_topk_softmax(p, p, 16, 128, 64, 9, p, p, None) == rf.RF_ERR_UNSUPPORTED
+    # W_gate layout: an unknown layout, and [D][E] with E not a multiple of 64
+    Mx = L.rf_moe_gate_topk_softmax_ex
+    assert Mx(p, p, 16, 128, 64, 2, 2, p, p, None) == rf.RF_ERR_INVALID_ARG
+    assert Mx(p, p, 16, 128, 20, 2, rf.RF_GATE_W_DE, p, p, None) == rf.RF_ERR_UNSUPPORTED
+    assert Mx(p, p, 16, 128, 320, 2, rf.RF_GATE_W_DE, p, p, None) == rf.RF_ERR_UNSUPPORTED
+    assert Mx(p, p, 16, 100, 64, 2, rf.RF_GATE_W_DE, p, p, None) == rf.RF_ERR_INVALID_ARG
     # FP8: K not a multiple of 16, missing workspace
     assert L.rf_absmax_fp8_gemm(p, p, p, p, 16, 16, 40, p, p, null, 0, None) == rf.RF_ERR_INVALID_ARG
     assert L.rf_absmax_fp8_gemm(p, p, p, p, 16, 16, 64, null, null, null, 0, None) == rf.RF_ERR_WORKSPACE

@@ -56,6 +56,39 @@ def test_moe_gate_small(rf, T, D, k):
     _check(x, w, k, idx, wts, f"MoE {T}x{D} k={k}")
 
 
+def _run_de(rf, x, w, k):
+    """The same call with W_gate given dim-major, [D][E]."""
+    T = x.shape[0]
+    idx = Guarded((T, k), torch.int32, fill=-1)
+    wts = Guarded((T, k), torch.float32)
+    w_de = Guarded(tuple(w.t().shape), torch.bfloat16)
+    w_de.t.copy_(w.t())
+    rf.rf_moe_gate_topk_softmax_ex(x.cuda(), w_de.t, k, rf.RF_GATE_W_DE, idx.t, wts.t)
+    assert rf.rf_get_device_status() == rf.RF_OK
+    idx.check("expert indices")
+    wts.check("expert weights")
+    w_de.check("W_gate (read only)")
+    return idx.t.cpu().numpy(), wts.t.cpu().numpy()
+
+
+def test_moe_gate_full_dim_major(rf):
+    """The full workload with W_gate in the [D][E] layout of the problem
+    statement (x @ W_gate): indices bit-exact, as with [E][D]."""
+    s = I.MOE_GATE
+    x, w = I.moe_inputs(s)
+    idx, wts = _run_de(rf, x, w, s.k)
+    _check(x, w, s.k, idx, wts, "MoE 8192x4096x64 [D][E]")
+
+
+@pytest.mark.parametrize("T,D,E,k", [(300, 256, 64, 2), (129, 1024, 128, 4), (64, 4096, 192, 8),
+                                     (513, 200, 256, 2), (1, 64, 64, 1), (1000, 2048, 256, 8),
+                                     (777, 8, 128, 3)])
+def test_moe_gate_dim_major(rf, T, D, E, k):
+    x, w = I.moe_inputs(I.MoEShape(T=T, D=D, E=E, k=k, seed=7 * T + D + E + k))
+    idx, wts = _run_de(rf, x, w, k)
+    _check(x, w, k, idx, wts, f"MoE {T}x{D}x{E} k={k} [D][E]")
+
+
 def test_moe_gate_all_equal_scores(rf):
     """All scores equal: the first k experts, uniform weights."""
     x = torch.ones(130, 128, dtype=torch.bfloat16)
