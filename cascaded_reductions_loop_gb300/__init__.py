@@ -26,20 +26,22 @@ __all__ = [
     "RF_DECODE_NOALLOC_SCRATCH_BYTES", "rf_mla_decode", "rf_mla_decode_num_splits",
     "rf_mla_decode_workspace_size", "rf_moe_gate_topk_softmax", "rf_moe_gate_topk_softmax_ex",
     "rf_absmax_fp8_gemm", "rf_absmax_fp8_gemm_workspace_size", "rf_absmax_quant_fp8",
-    "rf_selftest_wait_timeout",
+    "rf_selftest_wait_timeout", "rf_selftest_bounds",
     "RF_OK", "RF_ERR_INVALID_ARG", "RF_ERR_UNSUPPORTED", "RF_ERR_WORKSPACE", "RF_ERR_CUDA",
-    "RF_ERR_DEVICE_TIMEOUT", "RF_ERR_DEVICE_INPUT", "RF_ERR_DEVICE_LAYOUT", "RF_F32", "RF_BF16",
+    "RF_ERR_DEVICE_TIMEOUT", "RF_ERR_DEVICE_INPUT", "RF_ERR_DEVICE_LAYOUT", "RF_ERR_DEVICE_BOUNDS",
+    "RF_F32", "RF_BF16",
     "RF_ATTN_AUTO", "RF_ATTN_INCREMENTAL", "RF_ATTN_TWO_PASS", "RF_GATE_W_ED", "RF_GATE_W_DE",
 ]
 
 RF_OK, RF_ERR_INVALID_ARG, RF_ERR_UNSUPPORTED, RF_ERR_WORKSPACE, RF_ERR_CUDA, \
-    RF_ERR_DEVICE_TIMEOUT, RF_ERR_DEVICE_INPUT, RF_ERR_DEVICE_LAYOUT = range(8)
+    RF_ERR_DEVICE_TIMEOUT, RF_ERR_DEVICE_INPUT, RF_ERR_DEVICE_LAYOUT, RF_ERR_DEVICE_BOUNDS = range(9)
 RF_F32, RF_BF16 = 0, 1
 RF_ATTN_AUTO, RF_ATTN_INCREMENTAL, RF_ATTN_TWO_PASS = 0, 1, 2
 RF_GATE_W_ED, RF_GATE_W_DE = 0, 1                # layouts of W_gate: [E][D], [D][E]
 RF_DECODE_NOALLOC_SCRATCH_BYTES = 16 << 20   # as in rf.h
 
-LIB_PATH = _build.LIB_PATH
+# RF_GB300_LIB=debug selects the bounds-checked debug build of the same library
+LIB_PATH = _build.DEBUG_LIB_PATH if os.environ.get("RF_GB300_LIB") == "debug" else _build.LIB_PATH
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
@@ -75,6 +77,7 @@ _SIGS = {
     "rf_absmax_fp8_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _Z, _P]),
     "rf_absmax_quant_fp8": (_I, [_P, _I, _I, _P, _P, _P]),
     "rf_selftest_wait_timeout": (_I, [_I, _P]),
+    "rf_selftest_bounds": (_I, [_P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -336,3 +339,11 @@ def rf_absmax_quant_fp8(x, sx_out, xq_out, stream=None) -> None:
 def rf_selftest_wait_timeout(timeout_us: int, stream=None) -> None:
     _check(lib.rf_selftest_wait_timeout(int(timeout_us), _stream(stream)),
            "rf_selftest_wait_timeout")
+
+
+def rf_selftest_bounds(stream=None) -> int:
+    """Bounds-check self-test: in the debug build, one thread asks the bounds
+    check about an index past a tensor's end (reported as
+    RF_ERR_DEVICE_BOUNDS by rf_get_device_status, the access never made);
+    returns the call's status (RF_ERR_UNSUPPORTED in the normal build)."""
+    return lib.rf_selftest_bounds(_stream(stream))

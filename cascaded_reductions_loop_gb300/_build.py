@@ -2,7 +2,11 @@
 
 Every translation unit is compiled for sm_103a only, in parallel, then linked
 with the static CUDA runtime into ``_lib/librf_gb300.so`` inside the package.
-A rebuild happens only when a source or header is newer than the library.
+The same sources are also built with RF_DEBUG_BOUNDS into
+``_lib/librf_gb300_dbg.so``: the bounds-checked debug build, in which every
+global load or store a kernel thread issues is checked against its tensor
+(an access outside is skipped and reported as RF_ERR_DEVICE_BOUNDS).  A
+rebuild happens only when a source or header is newer than a library.
 """
 from __future__ import annotations
 
@@ -21,10 +25,14 @@ OUT_DIR = os.path.join(PKG_DIR, "_lib")
 OBJ_DIR = os.path.join(OUT_DIR, "obj")
 LIB_NAME = "librf_gb300.so"
 LIB_PATH = os.path.join(OUT_DIR, LIB_NAME)
+DEBUG_LIB_PATH = os.path.join(OUT_DIR, "librf_gb300_dbg.so")
+DEBUG_OBJ_DIR = os.path.join(OUT_DIR, "obj_dbg")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "--expt-relaxed-constexpr", "-I", INCLUDE]
+# (library, object directory, extra flags) of each build
+VARIANTS = [(LIB_PATH, OBJ_DIR, []), (DEBUG_LIB_PATH, DEBUG_OBJ_DIR, ["-DRF_DEBUG_BOUNDS"])]
 
 
 def nvcc_path() -> str:
@@ -43,10 +51,10 @@ def _deps():
             + glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)])
 
 
-def is_stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def is_stale(lib: str = LIB_PATH) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(p) > t for p in _deps())
 
 
@@ -58,23 +66,29 @@ def _run(cmd):
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compiles and links the library if needed; returns its path."""
-    if not force and not is_stale():
+    """Compiles and links both libraries if needed (all objects in one
+    parallel pool); returns the path of the normal one."""
+    todo = [v for v in VARIANTS if force or is_stale(v[0])]
+    if not todo:
         return LIB_PATH
     nvcc = nvcc_path()
-    os.makedirs(OBJ_DIR, exist_ok=True)
     srcs = _sources()
-    objs = [os.path.join(OBJ_DIR, os.path.basename(s)[:-3] + ".o") for s in srcs]
-    cmds = [[nvcc, *ARCH, *NVCC_FLAGS, "-c", s, "-o", o] for s, o in zip(srcs, objs)]
+    cmds, links = [], []
+    for lib, obj_dir, flags in todo:
+        os.makedirs(obj_dir, exist_ok=True)
+        objs = [os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o") for src in srcs]
+        cmds += [[nvcc, *ARCH, *NVCC_FLAGS, *flags, "-c", src, "-o", o] for src, o in zip(srcs, objs)]
+        links.append((lib, objs))
     with ThreadPoolExecutor(max_workers=min(len(cmds), os.cpu_count() or 4)) as ex:
         outs = list(ex.map(_run, cmds))
     if verbose:
         for o in outs:
             if o.strip():
                 print(o, file=sys.stderr)
-    tmp = LIB_PATH + ".tmp"
-    _run([nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs])
-    os.replace(tmp, LIB_PATH)
+    for lib, objs in links:
+        tmp = lib + ".tmp"
+        _run([nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs])
+        os.replace(tmp, lib)
     return LIB_PATH
 
 

@@ -152,6 +152,14 @@ cudaError_t launch_selftest_wait_timeout(int timeout_us, unsigned* err, cudaStre
   return cudaGetLastError();
 }
 
+#ifdef RF_DEBUG_BOUNDS
+// Asks the bounds check about an index one past the end of a 16-element
+// tensor: it records kDevErrBounds and the (never made) access is skipped.
+__global__ void selftest_bounds_kernel(unsigned* err, int64_t n, unsigned* sink) {
+  if (RF_IN(err, n, n)) *sink = 1u;
+}
+#endif
+
 }  // namespace rf
 
 // ================================================================ C ABI
@@ -188,6 +196,8 @@ const char* rf_status_string(int status) {
       return "RF_ERR_DEVICE_INPUT: device-side sizes (cu_seqlens) were inconsistent";
     case RF_ERR_DEVICE_LAYOUT:
       return "RF_ERR_DEVICE_LAYOUT: a kernel's shared memory was not aligned as its tiles need";
+    case RF_ERR_DEVICE_BOUNDS:
+      return "RF_ERR_DEVICE_BOUNDS: a global access fell outside its tensor (bounds-checked build)";
     default: return "unknown rf_status";
   }
 }
@@ -206,6 +216,7 @@ rf_status rf_get_device_status(rf_stream_t stream) {
     if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) return RF_ERR_CUDA;
   }
   if (v & kDevErrTimeout) return RF_ERR_DEVICE_TIMEOUT;
+  if (v & kDevErrBounds) return RF_ERR_DEVICE_BOUNDS;
   if (v & kDevErrLayout) return RF_ERR_DEVICE_LAYOUT;
   return (v & kDevErrInput) ? RF_ERR_DEVICE_INPUT : RF_OK;
 }
@@ -235,10 +246,12 @@ rf_status rf_attn_fwd_ex(int dtype, const void* Q, const void* K, const void* V,
   if (dtype == RF_F32) {
     if (d != 64 && d != 128) return RF_ERR_UNSUPPORTED;
     if (mode == RF_ATTN_TWO_PASS) return RF_ERR_UNSUPPORTED;
+    unsigned* err = device_error_word();
+    if (!err) return RF_ERR_CUDA;
     return from_cuda(launch_attn_fwd_f32(static_cast<const float*>(Q),
                                          static_cast<const float*>(K),
                                          static_cast<const float*>(V), static_cast<float*>(O), B,
-                                         H, Lq, Lk, d, scale, causal, s));
+                                         H, Lq, Lk, d, scale, causal, err, s));
   }
   if (d != 64) return RF_ERR_UNSUPPORTED;
   if (mode == RF_ATTN_TWO_PASS && Lk > 256) return RF_ERR_UNSUPPORTED;
@@ -400,7 +413,9 @@ rf_status rf_absmax_quant_fp8(const void* X, int M, int K, float* sx_out, uint8_
   if (!ptr_ok(X) || !ptr_ok(sx_out) || !ptr_ok(xq_out)) return RF_ERR_INVALID_ARG;
   if (M < 1 || K < 16 || K % 16 != 0) return RF_ERR_INVALID_ARG;
   if ((int64_t)M * K >= (1ll << 40)) return RF_ERR_INVALID_ARG;
-  return from_cuda(launch_absmax_quant(X, M, K, sx_out, xq_out,
+  unsigned* err = device_error_word();
+  if (!err) return RF_ERR_CUDA;
+  return from_cuda(launch_absmax_quant(X, M, K, sx_out, xq_out, err,
                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -410,6 +425,18 @@ rf_status rf_selftest_wait_timeout(int timeout_us, rf_stream_t stream) {
   if (!err) return RF_ERR_CUDA;
   return from_cuda(launch_selftest_wait_timeout(timeout_us, err,
                                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+rf_status rf_selftest_bounds(rf_stream_t stream) {
+#ifdef RF_DEBUG_BOUNDS
+  unsigned* err = device_error_word();
+  if (!err) return RF_ERR_CUDA;
+  selftest_bounds_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(err, 16, err);
+  return from_cuda(cudaGetLastError());
+#else
+  (void)stream;
+  return RF_ERR_UNSUPPORTED;
+#endif
 }
 
 }  // extern "C"

@@ -121,9 +121,11 @@ __device__ __forceinline__ Item item_of(int it, int n_bh, int nq, int Lq_, int L
     w.ok = true;
   } else {
     const int b = bh / H, h = bh % H;
-    const int a0 = cu_q[b], a1 = cu_q[b + 1], c0 = cu_k[b], c1 = cu_k[b + 1];
-    w.ok = 0 <= a0 && a0 <= a1 && a1 <= total_q && a1 - a0 <= Lq_ && 0 <= c0 && c0 <= c1 &&
-           c1 <= total_k;
+    const bool cu_ok = RF_IN(err, b + 1, n_bh / H + 1);     // cu_q, cu_k have B + 1 entries
+    const int a0 = cu_ok ? cu_q[b] : 0, a1 = cu_ok ? cu_q[b + 1] : 0;
+    const int c0 = cu_ok ? cu_k[b] : 0, c1 = cu_ok ? cu_k[b + 1] : 0;
+    w.ok = cu_ok && 0 <= a0 && a0 <= a1 && a1 <= total_q && a1 - a0 <= Lq_ && 0 <= c0 &&
+           c0 <= c1 && c1 <= total_k;
     if (!w.ok) {
       if (threadIdx.x == 0 && w.qt == 0) raise_error(err, kDevErrInput);
       w.Lq = w.Lk = w.nkv = 0;
@@ -604,9 +606,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       gk += nkv;
       if (!ok) break;
-      if (qt * BQ + r < w.Lq) {
+      const int64_t o_first = w.o_row0 + (int64_t)(qt * BQ + r) * w.o_stride;
+      const int64_t n_o = kVarlen ? (int64_t)total_q * H * kD : (int64_t)n_bh * Lq_ * kD;
+      if (qt * BQ + r < w.Lq && RF_IN(err, o_first + kD - 1, n_o)) {
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;   // no key read: O = 0
-        uint4* dst = reinterpret_cast<uint4*>(O + w.o_row0 + (int64_t)(qt * BQ + r) * w.o_stride);
+        uint4* dst = reinterpret_cast<uint4*>(O + o_first);
 #pragma unroll
         for (int c = 0; c < kD / 8; ++c) {
           float o[8];

@@ -43,10 +43,12 @@ __device__ __forceinline__ Rows fixed_rows(int Lq, int Lk, int D) {
 __device__ __forceinline__ Rows varlen_rows(const int* cu_q, const int* cu_k, int H, int max_q,
                                             int total_q, int total_k, int D, unsigned* err) {
   const int b = blockIdx.y / H, h = blockIdx.y % H;
-  const int q0 = cu_q[b], q1 = cu_q[b + 1], k0 = cu_k[b], k1 = cu_k[b + 1];
+  const bool cu_ok = RF_IN(err, b + 1, gridDim.y / H + 1);  // cu_q, cu_k have B + 1 entries
+  const int q0 = cu_ok ? cu_q[b] : 0, q1 = cu_ok ? cu_q[b + 1] : 0;
+  const int k0 = cu_ok ? cu_k[b] : 0, k1 = cu_ok ? cu_k[b + 1] : 0;
   Rows r;
-  r.ok = 0 <= q0 && q0 <= q1 && q1 <= total_q && q1 - q0 <= max_q && 0 <= k0 && k0 <= k1 &&
-         k1 <= total_k;
+  r.ok = cu_ok && 0 <= q0 && q0 <= q1 && q1 <= total_q && q1 - q0 <= max_q && 0 <= k0 &&
+         k0 <= k1 && k1 <= total_k;
   if (!r.ok) {
     if (threadIdx.x == 0 && blockIdx.x == 0) raise_error(err, kDevErrInput);
     return r;
@@ -74,6 +76,9 @@ __global__ void __launch_bounds__(kWarps * 32)
 
   const Rows g = cu_q ? varlen_rows(cu_q, cu_k, H, Lq_, total_q, total_k, D, err)
                       : fixed_rows(Lq_, Lk_, D);
+  // elements of Q/O and of K/V (debug-build bounds checks)
+  const int64_t n_q = cu_q ? (int64_t)total_q * H * D : (int64_t)gridDim.y * Lq_ * D;
+  const int64_t n_k = cu_q ? (int64_t)total_k * H * D : (int64_t)gridDim.y * Lk_ * D;
   if (!g.ok || (int)blockIdx.x * kWarps >= g.Lq) return;   // uniform over the CTA
   const int Lq = g.Lq, Lk = g.Lk;
   const size_t st = g.stride;
@@ -85,7 +90,7 @@ __global__ void __launch_bounds__(kWarps * 32)
   const float* Vp = V + g.kv;
 
   const float* Qp = Q + g.qo + (size_t)(active ? row : 0) * st;
-  for (int i = lane; i < D; i += 32) qs[warp][i] = Qp[i];
+  for (int i = lane; i < D; i += 32) qs[warp][i] = RF_IN(err, Qp + i - Q, n_q) ? Qp[i] : 0.f;
 
   // keys this row reads, and keys any row of the CTA reads
   const int off = Lk - Lq;
@@ -102,8 +107,9 @@ __global__ void __launch_bounds__(kWarps * 32)
     for (int i = threadIdx.x; i < kTileKeys * D; i += kWarps * 32) {
       const int r = i / D, cidx = i % D;
       const bool ok = t0 + r < Lk;
-      ks[r][cidx] = ok ? Kp[(size_t)(t0 + r) * st + cidx] : 0.f;
-      vs[r][cidx] = ok ? Vp[(size_t)(t0 + r) * st + cidx] : 0.f;
+      const int64_t kv_i = Kp + (size_t)(t0 + r) * st + cidx - K;
+      ks[r][cidx] = ok && RF_IN(err, kv_i, n_k) ? Kp[(size_t)(t0 + r) * st + cidx] : 0.f;
+      vs[r][cidx] = ok && RF_IN(err, kv_i, n_k) ? Vp[(size_t)(t0 + r) * st + cidx] : 0.f;
     }
     __syncthreads();
 
@@ -135,7 +141,8 @@ __global__ void __launch_bounds__(kWarps * 32)
   if (active) {
     float* Op = O + g.qo + (size_t)row * st;
 #pragma unroll
-    for (int c = 0; c < C; ++c) Op[c * 32 + lane] = l > 0.f ? o[c] / l : 0.f;
+    for (int c = 0; c < C; ++c)
+      if (RF_IN(err, Op + c * 32 + lane - O, n_q)) Op[c * 32 + lane] = l > 0.f ? o[c] / l : 0.f;
   }
 }
 
@@ -143,15 +150,15 @@ __global__ void __launch_bounds__(kWarps * 32)
 
 cudaError_t launch_attn_fwd_f32(const float* Q, const float* K, const float* V, float* O, int B,
                                 int H, int Lq, int Lk, int d, float scale, int causal,
-                                cudaStream_t s) {
+                                unsigned* err, cudaStream_t s) {
   dim3 grid((Lq + kWarps - 1) / kWarps, B * H);
   if (grid.y > 65535u) return cudaErrorInvalidValue;
   if (d == 64)
     attn_fwd_f32_kernel<64><<<grid, kWarps * 32, 0, s>>>(Q, K, V, O, Lq, Lk, scale, causal,
-                                                         nullptr, nullptr, H, 0, 0, nullptr);
+                                                         nullptr, nullptr, H, 0, 0, err);
   else
     attn_fwd_f32_kernel<128><<<grid, kWarps * 32, 0, s>>>(Q, K, V, O, Lq, Lk, scale, causal,
-                                                          nullptr, nullptr, H, 0, 0, nullptr);
+                                                          nullptr, nullptr, H, 0, 0, err);
   return cudaGetLastError();
 }
 

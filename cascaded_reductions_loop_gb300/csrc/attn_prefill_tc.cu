@@ -406,9 +406,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
       tc_fence_before();                               // O read before the next P.V may overwrite it
       const int row = (w.qa + x) * BQ + r;
-      if (row < Lq) {
+      const int64_t o_first = ((int64_t)w.bh * Lq + row) * kD;
+      if (row < Lq && RF_IN(err, o_first + kD - 1, (int64_t)n_bh * Lq * kD)) {
         const float inv = 1.f / l_run;
-        uint4* dst = reinterpret_cast<uint4*>(O + ((int64_t)w.bh * Lq + row) * kD);
+        uint4* dst = reinterpret_cast<uint4*>(O + o_first);
 #pragma unroll
         for (int c = 0; c < kD / 8; ++c) {
           const uint32_t* u = &v[c >> 2][(c & 3) * 8];

@@ -220,7 +220,8 @@ __device__ __forceinline__ void merge_into(float Mx, float m, float l, float4 o,
 }
 
 __device__ __forceinline__ void store_out(__nv_bfloat16* O, int64_t row, int lane, float L,
-                                          float4 o) {
+                                          float4 o, int64_t n_o, unsigned* err) {
+  if (!RF_IN(err, row * kD + 4 * lane + 3, n_o)) return;
   const float inv = 1.f / L;
   uint2 out;
   out.x = pack_bf16x2(o.x * inv, o.y * inv);
@@ -265,6 +266,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = (int)blockIdx.x;
   const int np = plan_num_pieces(pl, cta);
+  // elements of Q and O, of the partial-state slots (debug-build bounds checks)
+  const int64_t n_qo = (int64_t)pl.P * G * kD;
+  const int64_t n_ml = plan_slots(pl) * G;
   const bool consumer = warp < kWarps;
 
   if (threadIdx.x == 0) {
@@ -354,19 +358,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       if (pc.npieces == 1) {
 #pragma unroll
-        for (int h = 0; h < G; ++h) store_out(O, (int64_t)pc.p * G + h, lane, Lh[h], Oh[h]);
+        for (int h = 0; h < G; ++h) store_out(O, (int64_t)pc.p * G + h, lane, Lh[h], Oh[h], n_qo, err);
         continue;
       }
       // partial state of the piece -> workspace; ticket on the sequence
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        reinterpret_cast<float4*>(ws_o + ((int64_t)pc.slot * G + h) * kD)[lane] = Oh[h];
-        if (lane == 0) ws_ml[(int64_t)pc.slot * G + h] = make_float2(Mh[h], Lh[h]);
+        const int64_t sh = (int64_t)pc.slot * G + h;
+        if (RF_IN(err, sh, n_ml)) {
+          reinterpret_cast<float4*>(ws_o + sh * kD)[lane] = Oh[h];
+          if (lane == 0) ws_ml[sh] = make_float2(Mh[h], Lh[h]);
+        }
       }
       __threadfence();
       __syncwarp();
       unsigned t = 0;
-      if (lane == 0) t = atomicAdd(&tickets[pc.p], 1u);
+      if (lane == 0 && RF_IN(err, pc.p, pl.P)) t = atomicAdd(&tickets[pc.p], 1u);
       t = __shfl_sync(0xffffffffu, t, 0);
       if (t != (unsigned)(pc.npieces - 1)) continue;
       __threadfence();               // the other pieces' states are visible now
@@ -395,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (sj == pc.slot) {
               ml[u][h] = make_float2(Mh[h], Lh[h]);
               oj[u][h] = Oh[h];
-            } else if (sj >= 0) {
+            } else if (sj >= 0 && RF_IN(err, (int64_t)sj * G + h, n_ml)) {
               ml[u][h] = __ldcg(&ws_ml[(int64_t)sj * G + h]);
               oj[u][h] =
                   __ldcg(reinterpret_cast<const float4*>(ws_o + ((int64_t)sj * G + h) * kD) + lane);
@@ -423,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
       }
 #pragma unroll
-      for (int h = 0; h < G; ++h) store_out(O, (int64_t)pc.p * G + h, lane, Lt[h], Ot[h]);
+      for (int h = 0; h < G; ++h) store_out(O, (int64_t)pc.p * G + h, lane, Lt[h], Ot[h], n_qo, err);
     }
     return;
   }
@@ -440,12 +447,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto load_q = [&](int k, uint32_t (&q)[8][2]) {
     if (k >= np) return;
     const DecodePiece pc = plan_piece(pl, cta, plan_order(pl, np, k));
-    const uint32_t* qp = reinterpret_cast<const uint32_t*>(
-        Q + ((int64_t)pc.p * G + (hrow < G ? hrow : 0)) * kD);
+    const int64_t q_row = ((int64_t)pc.p * G + (hrow < G ? hrow : 0)) * kD;
+    const uint32_t* qp = reinterpret_cast<const uint32_t*>(Q + q_row);
+    const bool q_ok = hrow < G && RF_IN(err, q_row + kD - 1, n_qo);
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
-      q[ks][0] = hrow < G ? __ldg(qp + ((ks * 16 + kq) >> 1)) : 0u;
-      q[ks][1] = hrow < G ? __ldg(qp + ((ks * 16 + kq + 8) >> 1)) : 0u;
+      q[ks][0] = q_ok ? __ldg(qp + ((ks * 16 + kq) >> 1)) : 0u;
+      q[ks][1] = q_ok ? __ldg(qp + ((ks * 16 + kq + 8) >> 1)) : 0u;
     }
   };
   uint32_t qa[8][2], qn[8][2];

@@ -184,21 +184,22 @@ __device__ __forceinline__ void quant_row_long(const uint4* __restrict__ xr, uin
 // warp with its whole row in flight.
 __global__ void __launch_bounds__(kQuantWarps * 32, 4)
     absmax_quant_regs_kernel(const uint4* __restrict__ X, uint8_t* __restrict__ Xq,
-                             float* __restrict__ sx, int M, int K) {
+                             float* __restrict__ sx, int M, int K, unsigned* err) {
   const int lane = threadIdx.x & 31;
   const int nw = gridDim.x * kQuantWarps;
   const int nvec = K >> 3;
   for (int row = blockIdx.x * kQuantWarps + (threadIdx.x >> 5); row < M; row += nw)
-    quant_row_regs<true>(X + (size_t)row * nvec, reinterpret_cast<uint2*>(Xq + (size_t)row * K),
-                         sx + row, nvec, lane);
+    if (RF_IN(err, row, M))
+      quant_row_regs<true>(X + (size_t)row * nvec, reinterpret_cast<uint2*>(Xq + (size_t)row * K),
+                           sx + row, nvec, lane);
 }
 
 __global__ void __launch_bounds__(kQuantWarps * 32)
     absmax_quant_long_kernel(const uint4* __restrict__ X, uint8_t* __restrict__ Xq,
-                             float* __restrict__ sx, int M, int K) {
+                             float* __restrict__ sx, int M, int K, unsigned* err) {
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * kQuantWarps + (threadIdx.x >> 5);
-  if (row >= M) return;
+  if (row >= M || !RF_IN(err, row, M)) return;
   const int nvec = K >> 3;
   quant_row_long(X + (size_t)row * nvec, reinterpret_cast<uint2*>(Xq + (size_t)row * K), sx + row,
                  nvec, lane);
@@ -443,7 +444,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         break;
       }
       tc_fence_after();
-      const float srow = (row < M) ? sx[row] : 0.f;
+      const bool row_in = row < M && RF_IN(err, (int64_t)row * N + N - 1, (int64_t)M * N);
+      const float srow = row_in ? sx[row] : 0.f;
 #pragma unroll 1
       for (int c0 = 0; c0 < w.ncols; c0 += 32) {
         if (n0 + c0 >= N) break;
@@ -471,7 +473,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int j = 0; j < 16; ++j)
           packed[j] = pack_bf16x2(__uint_as_float(r[2 * j]) * srow * swv[2 * j],
                                   __uint_as_float(r[2 * j + 1]) * srow * swv[2 * j + 1]);
-        if (row < M) {
+        if (row_in) {
           __nv_bfloat16* yp = Y + (size_t)row * N + n0 + c0;
           if (vec_ok && full_chunk) {
             uint4* y4 = reinterpret_cast<uint4*>(yp);
@@ -507,7 +509,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (qw == 0 && lane == 0)                    // claim the next batch early
         bars->qbase[(k + 1) & 1] = (int)atomicAdd(ctr, (unsigned)kFusedQuantWarps);
       const int row = base + qw;
-      if (row < M) {
+      if (row < M && RF_IN(err, row, M)) {
         const uint4* xr = X + (size_t)row * nvec;
         uint2* qr = reinterpret_cast<uint2*>(Xq + (size_t)row * K);
         if (K <= kRegRowMax) quant_row_regs<false>(xr, qr, sx + row, nvec, lane);
@@ -564,17 +566,17 @@ size_t fp8_workspace_bytes(int M, int N, int K, bool need_xq, bool need_sx) {
 }
 
 cudaError_t launch_absmax_quant(const void* X, int M, int K, float* sx, uint8_t* xq,
-                                cudaStream_t s) {
+                                unsigned* err, cudaStream_t s) {
   const int qblocks = (M + kQuantWarps - 1) / kQuantWarps;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidValue;
   if (K <= kRegRowMax) {
     const int resident = 4 * sms;                      // four 4-warp CTAs per SM
     absmax_quant_regs_kernel<<<qblocks < resident ? qblocks : resident, kQuantWarps * 32, 0, s>>>(
-        static_cast<const uint4*>(X), xq, sx, M, K);
+        static_cast<const uint4*>(X), xq, sx, M, K, err);
   } else {
     absmax_quant_long_kernel<<<qblocks, kQuantWarps * 32, 0, s>>>(static_cast<const uint4*>(X), xq,
-                                                                   sx, M, K);
+                                                                   sx, M, K, err);
   }
   return cudaGetLastError();
 }

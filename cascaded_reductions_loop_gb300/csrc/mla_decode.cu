@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rank = (int)cluster_ctarank(), peer = rank ^ 1;
   const int item = blockIdx.x >> 1;
   const int b = item / S, seg = item % S;
+  const int64_t n_bat = (int64_t)(gridDim.x >> 1) / S;   // batches (debug-build bounds checks)
   const int ntiles = (Lk + BN - 1) / BN;
   const int t0 = seg * tps;
   int nt = min(tps, ntiles - t0);
@@ -257,13 +258,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // are fetched together rather than one round trip per block.
     {
       const uint4* qrow = reinterpret_cast<const uint4*>(Q + (row_ok ? bh : 0) * kDqk);
+      const bool q_ok = row_ok && RF_IN(err, bh * kDqk + kDqk - 1, n_bat * Hq * kDqk);
       uint4 w[kMaxBlk][8];
 #pragma unroll
       for (int c = 0; c < kMaxBlk; ++c) {
         const int db = dim_block(rank, c);
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          w[c][i] = row_ok && c < nblk ? qrow[db * 8 + i] : make_uint4(0u, 0u, 0u, 0u);
+          w[c][i] = q_ok && c < nblk ? qrow[db * 8 + i] : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
       for (int c = 0; c < kMaxBlk; ++c) {
@@ -436,12 +438,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (S == 1) {
           const float inv = 1.f / l_run;
           uint4* dst = reinterpret_cast<uint4*>(O + bh * kDv + 256 * rank);
+          const bool o_ok = row_ok && RF_IN(err, bh * kDv + 256 * rank + 255, n_bat * Hq * kDv);
 #pragma unroll 1
           for (int blk = 0; blk < 8; ++blk) {
             uint32_t v[32];
             tmem_ld32(tm + lane_off + 32 * blk, v);
             tmem_ld_wait();
-            if (row_ok) {
+            if (o_ok) {
 #pragma unroll
               for (int c = 0; c < 4; ++c) {
                 const float* f = reinterpret_cast<const float*>(v + 8 * c);
@@ -455,18 +458,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           const int64_t ps = bh * S + seg;
           uint4* dst = reinterpret_cast<uint4*>(part_o + ps * kDv + 256 * rank);
+          const bool p_ok = row_ok && RF_IN(err, ps, n_bat * Hq * S);
 #pragma unroll 1
           for (int blk = 0; blk < 8; ++blk) {
             uint32_t v[32];
             tmem_ld32(tm + lane_off + 32 * blk, v);
             tmem_ld_wait();
-            if (row_ok) {
+            if (p_ok) {
 #pragma unroll
               for (int c = 0; c < 8; ++c)
                 dst[blk * 8 + c] = make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
             }
           }
-          if (rank == 0 && row_ok)
+          if (rank == 0 && p_ok)
             reinterpret_cast<float2*>(part_ml)[ps] = make_float2(m_run, l_run);
         }
       }
@@ -494,9 +498,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // the partial kernel; waits for it (griddepcontrol.wait) before reading.
 __global__ void __launch_bounds__(kMergeThreads)
     mla_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
-                     __nv_bfloat16* __restrict__ O, int S) {
+                     __nv_bfloat16* __restrict__ O, int S, unsigned* err) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t bh = blockIdx.x;
+  // every state of this (batch, head) and its output row lie in the buffers
+  if (!RF_IN(err, bh * S + S - 1, (int64_t)gridDim.x * S)) return;
   const float2* ml = reinterpret_cast<const float2*>(part_ml) + bh * S;
   const float4* po = reinterpret_cast<const float4*>(part_o + bh * S * kDv) + threadIdx.x;
   float M = -INFINITY;
@@ -611,7 +617,7 @@ cudaError_t launch_mla_decode(const void* Q, const void* CKV, void* O, int B, in
   mcfg.attrs = mattr;
   mcfg.numAttrs = 1;
   return cudaLaunchKernelEx(&mcfg, mla_merge_kernel, (const float*)part_o, (const float*)part_ml,
-                            static_cast<__nv_bfloat16*>(O), S);
+                            static_cast<__nv_bfloat16*>(O), S, err);
 }
 
 }  // namespace rf

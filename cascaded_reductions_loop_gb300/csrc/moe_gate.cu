@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (tpr < 8 && 2 * tpr * rows_fin <= 128) tpr *= 2;
     const int row = t / tpr, part = t % tpr;
     const int tok = m0 + r_lo + row;
-    const bool live = row < rows_fin && tok < T;
+    const bool live = row < rows_fin && tok < T && RF_IN(err, (int64_t)tok * k + k - 1, (int64_t)T * k);
     const float* srow = red + (live ? row : 0) * kRedStride;
     const int ns = (int)csize;
     int32_t* io = idx_out + (size_t)(live ? tok : 0) * k;

@@ -17,6 +17,7 @@ namespace rf {
 constexpr unsigned kDevErrTimeout = 1u;
 constexpr unsigned kDevErrInput = 2u;     // inconsistent device-side sizes (clamped, skipped)
 constexpr unsigned kDevErrLayout = 4u;    // shared memory not aligned as the tiles need (no work done)
+constexpr unsigned kDevErrBounds = 8u;    // debug builds: a thread's global access outside its tensor (skipped)
 
 // Default wait limit of a bounded wait, in nanoseconds of %globaltimer.
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;   // 2 s
@@ -30,6 +31,23 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 __device__ __forceinline__ void raise_error(unsigned* err, unsigned bits) {
   if (err) atomicOr(err, bits);
 }
+
+// Bounds checks of the debug build (RF_DEBUG_BOUNDS): RF_IN(err, i, n) is
+// true when element index i lies in [0, n); otherwise it records
+// kDevErrBounds and the caller skips the access.  In the normal build it is
+// the constant true and costs nothing.  Every global load or store a thread
+// issues itself (TMA copies are bounded by their tensor maps) goes through
+// it, with i the last element the access touches.
+__device__ __forceinline__ bool bounds_ok(unsigned* err, int64_t i, int64_t n) {
+  const bool ok = i >= 0 && i < n;
+  if (!ok) raise_error(err, kDevErrBounds);
+  return ok;
+}
+#ifdef RF_DEBUG_BOUNDS
+#define RF_IN(err, i, n) (::rf::bounds_ok((err), (int64_t)(i), (int64_t)(n)))
+#else
+#define RF_IN(err, i, n) (true)
+#endif
 
 // ----------------------------------------------------------------- smem
 

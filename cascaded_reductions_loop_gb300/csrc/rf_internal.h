@@ -40,7 +40,7 @@ bool encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
 // causal = 1: query row i reads keys j <= i + (Lk - Lq) only.
 cudaError_t launch_attn_fwd_f32(const float* Q, const float* K, const float* V, float* O, int B,
                                 int H, int Lq, int Lk, int d, float scale, int causal,
-                                cudaStream_t s);
+                                unsigned* err, cudaStream_t s);
 
 // two_pass = 1: non-incremental form (requires Lk <= 256).
 cudaError_t launch_attn_fwd_bf16_tc(const void* Q, const void* K, const void* V, void* O, int B,
@@ -85,7 +85,7 @@ cudaError_t launch_moe_gate(const void* X, const void* Wg, int T, int D, int E, 
 size_t fp8_counter_bytes(int M);
 size_t fp8_workspace_bytes(int M, int N, int K, bool need_xq, bool need_sx);
 cudaError_t launch_absmax_quant(const void* X, int M, int K, float* sx, uint8_t* xq,
-                                cudaStream_t s);
+                                unsigned* err, cudaStream_t s);
 cudaError_t launch_absmax_fp8_gemm(const void* X, const uint8_t* Wq, const float* sw, void* Y,
                                    int M, int N, int K, float* sx, uint8_t* xq, void* workspace,
                                    unsigned* err, cudaStream_t s);

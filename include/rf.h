@@ -52,7 +52,8 @@ typedef enum {
   RF_ERR_CUDA = 4,            /* a CUDA runtime call or launch failed       */
   RF_ERR_DEVICE_TIMEOUT = 5,  /* a kernel's bounded wait ran out            */
   RF_ERR_DEVICE_INPUT = 6,    /* device-resident sizes were inconsistent    */
-  RF_ERR_DEVICE_LAYOUT = 7    /* a kernel's shared memory was misaligned    */
+  RF_ERR_DEVICE_LAYOUT = 7,   /* a kernel's shared memory was misaligned    */
+  RF_ERR_DEVICE_BOUNDS = 8    /* debug build: an access outside its tensor  */
 } rf_status;
 
 typedef enum { RF_F32 = 0, RF_BF16 = 1 } rf_dtype;
@@ -79,9 +80,12 @@ const char* rf_last_cuda_error(void);
  * cumulative sequence lengths of rf_attn_fwd_varlen, inconsistent with the
  * host-side sizes; it skipped that work and wrote nothing out of bounds),
  * RF_ERR_DEVICE_LAYOUT (a kernel found its dynamic shared memory not aligned
- * as its swizzled tiles need; it did no work) or RF_ERR_CUDA (the
- * synchronisation itself failed).  When several kinds occurred, the first
- * of TIMEOUT, LAYOUT, INPUT in that order is returned.
+ * as its swizzled tiles need; it did no work), RF_ERR_DEVICE_BOUNDS (only in
+ * the bounds-checked debug build of the library, librf_gb300_dbg.so: a
+ * thread's global load or store would have fallen outside its tensor; it was
+ * skipped) or RF_ERR_CUDA (the synchronisation itself failed).  When several
+ * kinds occurred, the first of TIMEOUT, BOUNDS, LAYOUT, INPUT in that order is
+ * returned.
  */
 rf_status rf_get_device_status(rf_stream_t stream);
 
@@ -377,6 +381,17 @@ rf_status rf_absmax_quant_fp8(const void* X, int M, int K, float* sx_out, uint8_
  * context usable; rf_get_device_status then reports it.
  */
 rf_status rf_selftest_wait_timeout(int timeout_us, rf_stream_t stream);
+
+/*
+ * Bounds-check self-test (no counterpart in the paper).  In the
+ * bounds-checked debug build (librf_gb300_dbg.so, built with
+ * RF_DEBUG_BOUNDS) it launches one thread that asks the kernels' bounds check
+ * about an element index one past the end of a 16-element tensor: the check
+ * records it, the access is never made, and rf_get_device_status then reports
+ * RF_ERR_DEVICE_BOUNDS.  In the normal build it returns RF_ERR_UNSUPPORTED
+ * and launches nothing.
+ */
+rf_status rf_selftest_bounds(rf_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -40,9 +40,22 @@ def test_library_exports_every_declared_symbol(rf):
         assert hasattr(rf, n), f"{n} has no Python binding"
 
 
+def test_debug_build_exports_the_same_symbols(rf):
+    """The bounds-checked debug build is built beside the library and
+    exports the same boundary."""
+    lib = ctypes.CDLL(_build.DEBUG_LIB_PATH)
+    for n in _declared():
+        assert hasattr(lib, n), f"{n} not exported by the debug build"
+
+
+def test_bounds_selftest_only_in_debug_build(rf):
+    # the normal build returns before any CUDA call
+    assert rf.lib.rf_selftest_bounds(None) == rf.RF_ERR_UNSUPPORTED
+
+
 def test_status_strings(rf):
     assert rf.rf_status_string(0) == "RF_OK"
-    for s in range(1, 8):
+    for s in range(1, 9):
         assert rf.rf_status_string(s).startswith("RF_ERR_")
     assert "aligned" in rf.rf_status_string(rf.RF_ERR_DEVICE_LAYOUT)
     assert "unknown" in rf.rf_status_string(99)
