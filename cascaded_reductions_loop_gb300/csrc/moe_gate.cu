@@ -6,8 +6,8 @@
 // CTAs covering the slices of the same tile form a thread-block cluster
 // (split-K).  Per CTA: a TMA producer warp streams bm x 64 tiles of x and
 // the matching 64-dim slices of W_gate (128-byte swizzled) through a ring of
-// stages (for E <= 64 four adjacent tiles of each per stage, so that every
-// row's 512 bytes are fetched together).  W_gate may be expert-major, [E][D]
+// stages (for E <= 64 two adjacent tiles of each per stage, so that every
+// row's 256 bytes are fetched together).  W_gate may be expert-major, [E][D]
 // (a K-major B operand: E rows of 64 dims per slice), or dim-major, [D][E]
 // (an MN-major B operand: per slice, 64 rows of D, each 64 experts wide, one
 // 8 KB box per 64 experts); one thread issues tcgen05.mma
@@ -46,7 +46,7 @@ constexpr int kMaxStages = 8;
 // feed accumulator rows / columns that are never read.
 template <int NE>
 struct GateCfg {
-  static constexpr int kBoxes = NE <= 64 ? 4 : 1;          // boxes per stage
+  static constexpr int kBoxes = NE <= 64 ? 2 : 1;          // boxes per stage
   static constexpr int KB = BK * kBoxes;                   // bf16 elements per k-block
   static constexpr int kRedStride = NE + 4;                // padded fp32 row of the score tile
   static constexpr int kRedBytes = (BM + 8) * kRedStride * 4;   // cs slots of ceil(bm/cs) rows
