@@ -303,28 +303,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const int valid = min(BKV, Lk - j * BKV);      // keys of this tile that exist
         const bool full = valid == BKV;
-        // pass 1: row max of the raw scores (four independent chains; two
-        // 32-column blocks in flight together)
+        // the row's 128 scores read from tensor memory once (four loads in
+        // flight together) and kept in registers for both passes
+        uint32_t v[4][32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_ld32(s_addr + q * 32, v[q]);
+        tmem_ld_wait();
+        // pass 1: row max (four independent chains)
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int qq = 0; qq < 2; ++qq) {
-          uint32_t v[2][32];
-          tmem_ld32(s_addr + (2 * qq) * 32, v[0]);
-          tmem_ld32(s_addr + (2 * qq + 1) * 32, v[1]);
-          tmem_ld_wait();
+        for (int q = 0; q < 4; ++q) {
+          if (full) {
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int q = 2 * qq + h;
-            if (full) {
+            for (int i = 0; i < 32; i += 2)
+              mx4[(i >> 1) & 3] =
+                  fmax3(mx4[(i >> 1) & 3], __uint_as_float(v[q][i]), __uint_as_float(v[q][i + 1]));
+          } else {
 #pragma unroll
-              for (int i = 0; i < 32; i += 2)
-                mx4[(i >> 1) & 3] =
-                    fmax3(mx4[(i >> 1) & 3], __uint_as_float(v[h][i]), __uint_as_float(v[h][i + 1]));
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (q * 32 + i < valid) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(v[h][i]));
-            }
+            for (int i = 0; i < 32; ++i)
+              if (q * 32 + i < valid) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(v[q][i]));
           }
         }
         const float mt = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]) * c_log2;
@@ -339,15 +336,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           need = true;
         }
         const uint64_t negm2 = f2(-m_ref, -m_ref);
-        // pass 2: P = 2^(S c - m) as bf16 pairs, row sum (four chains), per
-        // half of the row (S read again), each half of P stored as formed
+        // pass 2: P = 2^(S c - m) as bf16 pairs, row sum (four chains); P
+        // goes over S columns 0-63, all of S being in registers by now
         uint64_t sum4[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          uint32_t v[2][32];
-          tmem_ld32(s_addr + (2 * hh) * 32, v[0]);
-          tmem_ld32(s_addr + (2 * hh + 1) * 32, v[1]);
-          tmem_ld_wait();
           uint32_t pk[32];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
@@ -355,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               float t0, t1;
-              f2_split(ffma2(f2(__uint_as_float(v[h][2 * i]), __uint_as_float(v[h][2 * i + 1])), c2,
+              f2_split(ffma2(f2(__uint_as_float(v[q][2 * i]), __uint_as_float(v[q][2 * i + 1])), c2,
                              negm2),
                        t0, t1);
               float p0 = ex2(t0), p1 = ex2(t1);
@@ -368,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               pk[h * 16 + i] = pack_bf16x2(p0, p1);
             }
           }
-          tmem_st32(s_addr + hh * 32, pk);              // S columns 0-63: read in half 0
+          tmem_st32(s_addr + hh * 32, pk);
         }
         float s_lo, s_hi;
         f2_split(fadd2(fadd2(sum4[0], sum4[1]), fadd2(sum4[2], sum4[3])), s_lo, s_hi);
