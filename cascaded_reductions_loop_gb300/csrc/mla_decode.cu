@@ -27,8 +27,10 @@
 // P . V products; the cache rows stream by TMA through a 4-stage ring (64 rows
 // x 64 dims per block, 128-byte swizzle; prefetching further tiles into L2
 // measured slower); S has one buffer in tensor memory, O accumulates there.
-// The MMA warp issues whichever product is ready (S_t once the softmax warps
-// have taken S_{t-1} and the tile has landed; P_j V_j once P_j is written).
+// Two threads issue the products: one the score products (S_t once the
+// softmax warps have taken S_{t-1} and the tile has landed), one the P . V
+// products (P_j V_j once P_j is written), so that a ready P . V enters the
+// tensor core between score products instead of after all of them.
 //
 // Exchange, one tile ahead: at tile j the softmax warps add the peer's
 // partial S_j to their own, then at once take their own S_{j+1} out of tensor
@@ -73,7 +75,8 @@ constexpr int kStOff = 0;
 constexpr int kXOff = kStOff + kStages * kStageBytes;   // 160 KB
 constexpr int kBarOff = kXOff + kNX * kXBytes;          // 224 KB
 constexpr int kSmem = kBarOff + 512;
-constexpr int kThreads = 192;                      // warp 0 TMA, 1 MMA, 2-5 softmax
+constexpr int kThreads = 224;                      // warp 0 TMA, 1 MMA (S), 2-5 softmax, 6 MMA (P.V)
+constexpr int kPvWarp = 6;
 constexpr int kTmemCols = 512;
 constexpr int kTmemS = 256, kTmemP = 320, kTmemQ = 352;
 constexpr float kLazy = 8.f;
@@ -97,7 +100,7 @@ struct Bars {
   uint64_t p_full;                  // P_j in tensor memory
   uint64_t pv_done;                 // P_j V_j accumulated into O (P_j read)
   uint64_t x_full[kNX][4];          // rows 32 w .. of the peer's partial S_t in slot t % 2
-  uint64_t drain;
+  uint64_t drain, drain_pv;         // every MMA of the S / P.V issuer has completed
   uint32_t tmem;
   int abort;
 };
@@ -148,6 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kNX; ++i)
       for (int w = 0; w < 4; ++w) mbar_init(smem_u32(&bars->x_full[i][w]), 1);
     mbar_init(smem_u32(&bars->drain), 1);
+    mbar_init(smem_u32(&bars->drain_pv), 1);
     bars->abort = 0;
     fence_mbar_init();
     // armed for the peer's first two partial tiles; re-armed as slots are read
@@ -195,46 +199,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0 && nt > 0) {
-      // ------------------------------------------------ MMA issuer (event loop)
+      // ------------------------------------------------ MMA issuer: score products
       bool ok = mbar_wait(smem_u32(&bars->q_full), 0);
-      if (ok) tc_fence_after();
-      int ns = 0, npv = 0;                             // next S / next P.V to issue
-      uint64_t t_prog = globaltimer_ns();
-      uint32_t idle = 0;
-      while (ok && npv < nt) {
-        if (npv < ns && mbar_test_wait(smem_u32(&bars->p_full), (uint32_t)(npv & 1))) {
-          // O (+)= P_j V_j over all 256 value dims, P_j from tensor memory
-          tc_fence_after();
-          const int st = npv % kStages;
-          const uint32_t sb = smem_u32(smem + kStOff + st * kStageBytes);
+      for (int ns = 0; ok && ns < nt; ++ns) {
+        // S_t once the softmax warps have taken S_{t-1} and the tile has landed
+        ok = (ns == 0 || mbar_wait(smem_u32(&bars->s_free), (uint32_t)((ns - 1) & 1))) &&
+             mbar_wait(smem_u32(&bars->full[ns % kStages]), (uint32_t)((ns / kStages) & 1)) &&
+             !*abort_flag;
+        if (!ok) break;
+        // partial S_t = Q_r C_t,r^T over this CTA's dims
+        tc_fence_after();
+        const uint32_t sb = smem_u32(smem + kStOff + (ns % kStages) * kStageBytes);
+        for (int c = 0; c < nblk; ++c) {
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_bf16_ts(tm, tm + kTmemP + kk * 8, sw128_desc(sb + kk * 16 * 128, 1024, kChBytes),
-                        kIdescO, (npv | kk) != 0);
-          mma_commit(smem_u32(&bars->pv_done));
-          mma_commit(smem_u32(&bars->empty[st]));
-          ++npv;
-          t_prog = globaltimer_ns();
-        } else if (ns < nt &&
-                   (ns == 0 || mbar_test_wait(smem_u32(&bars->s_free), (uint32_t)((ns - 1) & 1))) &&
-                   mbar_test_wait(smem_u32(&bars->full[ns % kStages]), (uint32_t)((ns / kStages) & 1))) {
-          // partial S_t = Q_r C_t,r^T over this CTA's dims
-          tc_fence_after();
-          const uint32_t sb = smem_u32(smem + kStOff + (ns % kStages) * kStageBytes);
-          for (int c = 0; c < nblk; ++c) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_bf16_ts(tm + kTmemS, tm + kTmemQ + c * 32 + kk * 8,
-                          sw128_desc(sb + c * kChBytes + kk * 32, 1024, 16), kIdescS,
-                          (c | kk) != 0);
-          }
-          mma_commit(smem_u32(&bars->s_full));
-          ++ns;
-          t_prog = globaltimer_ns();
-        } else if ((++idle & 63u) == 0 &&
-                   (*abort_flag || globaltimer_ns() - t_prog > kDefaultWaitNs)) {
-          ok = false;
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ts(tm + kTmemS, tm + kTmemQ + c * 32 + kk * 8,
+                        sw128_desc(sb + c * kChBytes + kk * 32, 1024, 16), kIdescS, (c | kk) != 0);
         }
+        mma_commit(smem_u32(&bars->s_full));
       }
       if (!ok) {
         raise_error(err, kDevErrTimeout);
@@ -242,6 +224,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mma_commit(smem_u32(&bars->drain));
       (void)mbar_wait(smem_u32(&bars->drain), 0, 1000000000ull);
+    }
+  } else if (warp == kPvWarp) {
+    if (lane == 0 && nt > 0) {
+      // ------------------------------------------------ MMA issuer: P.V products
+      // A thread of its own, so that a ready P.V does not wait behind the
+      // issue of a later tile's score products.  S_j has completed before
+      // P_j exists (the softmax warps read it first), so the stage release
+      // committed after P_j V_j covers both products that read the stage.
+      bool ok = true;
+      for (int npv = 0; ok && npv < nt; ++npv) {
+        ok = mbar_wait(smem_u32(&bars->p_full), (uint32_t)(npv & 1)) && !*abort_flag;
+        if (!ok) break;
+        // O (+)= P_j V_j over all 256 value dims, P_j from tensor memory
+        tc_fence_after();
+        const int st = npv % kStages;
+        const uint32_t sb = smem_u32(smem + kStOff + st * kStageBytes);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_bf16_ts(tm, tm + kTmemP + kk * 8, sw128_desc(sb + kk * 16 * 128, 1024, kChBytes),
+                      kIdescO, (npv | kk) != 0);
+        mma_commit(smem_u32(&bars->pv_done));
+        mma_commit(smem_u32(&bars->empty[st]));
+      }
+      if (!ok) {
+        raise_error(err, kDevErrTimeout);
+        *abort_flag = 1;
+      }
+      mma_commit(smem_u32(&bars->drain_pv));
+      (void)mbar_wait(smem_u32(&bars->drain_pv), 0, 1000000000ull);
     }
   } else if (nt > 0) {
     // ------------------------------------------------ softmax / exchange / epilogue
