@@ -192,7 +192,11 @@ size_t rf_attn_decode_splitkv_workspace_size(int B, int Hq, int Hkv, int Lk, int
  *   num_splits  0 = automatic: the 32-key chunks of all sequences, end to
  *               end, are cut into one equal range per CTA (a sequence may be
  *               cut into several segments, another lie within one range);
- *               1..Lk = each sequence cut into that many equal segments.
+ *               1..Lk = each sequence cut into that many equal segments
+ *               (the segments are handed to the CTAs round-robin; every
+ *               segment adds a fence, a ticket and a merge step, so large
+ *               counts are much slower than the automatic partition and
+ *               are meant for exercising the merge).
  *   workspace   device buffer of at least
  *               rf_attn_decode_splitkv_workspace_size(...) bytes, 16-byte
  *               aligned, owned by the caller; holds a ticket counter per
