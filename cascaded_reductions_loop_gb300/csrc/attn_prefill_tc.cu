@@ -7,31 +7,33 @@
 // One CTA per SM takes a pair of 128-row query tiles (a, b) of one (batch,
 // head) at a time; both tiles read every key/value tile of that head, so K
 // and V are loaded once for 256 query rows.  Per key tile j and query tile x:
-//   1. MMA warp:   S_x = Q_x K_j^T              (tcgen05 kind::f16, M=128,
+//   1. MMA thread x: S_x = Q_x K_j^T           (tcgen05 kind::f16, M=128,
 //                                               N=128, fp32 in tensor memory)
-//   2. softmax warpgroup x (thread = query row): row max of its S_x row (read
-//      from tensor memory); the running reference m moves only when the
-//      tile's max exceeds it by more than kLazy (log2 units), and then O_x and
-//      l are rescaled by 2^(m - m'); P = 2^(S*c - m) (c = scale * log2 e),
-//      l += sum P; P is written as bf16 pairs over the first 64 columns of S_x
-//   3. MMA warp:   O_x += P_x V_j               (M=128, N=64, K=128; P is the
+//   2. softmax warpgroup x (thread = query row): reads its 128 scores of S_x
+//      into registers once (the MMA thread may then compute S_x(j+1) into
+//      the same columns), takes the row max; the running reference m moves
+//      only when the tile's max exceeds it by more than kLazy (log2 units),
+//      and then O_x and l are rescaled by 2^(m - m'); P = 2^(S*c - m)
+//      (c = scale * log2 e), l += sum P; P is written as bf16 pairs to
+//      tensor-memory columns of its own once the previous P_x V has read them
+//   3. MMA thread x: O_x += P_x V_j            (M=128, N=64, K=128; P is the
 //                                               tensor-memory A operand, V the
 //                                               MN-major shared-memory B operand)
-// After the last key tile the warpgroup reads O_x from tensor memory and
-// writes O_x / l as bf16.  S, P and O never leave the SM.
+// After the last key tile the warpgroup reads O_x from tensor memory, stages
+// O_x / l as bf16 in shared memory and writes it with one bulk tensor store.
+// S, P and O never leave the SM.
 //
-// The MMA warp issues S_a, S_b, then for each tile P_a V, S_a(next), P_b V,
-// S_b(next): the tensor core computes one query tile's products while the
-// other warpgroup runs its exponentials.  The tensor core executes one
-// thread's MMAs in issue order, so S_x(next) overwrites P_x only after P_x V
-// has read it, and a completed S_x(j) implies a completed P_x V(j - 1).  Any
-// reference m gives the same result ([S] Methodologie 1: the dependent
-// factor 2^-m is invertible); with m at least the true running max minus
-// kLazy, every P is at most 2^kLazy.
+// Each query tile has an MMA-issuing thread of its own, so one tile's
+// products never wait behind the other tile's softmax; within a tile the
+// next S is issued as soon as the current one has been read, the P.V as soon
+// as P is written (at a pair's last key tile the P.V first, so O is complete
+// early).  Any reference m gives the same result ([S] Methodologie 1: the
+// dependent factor 2^-m is invertible); with m at least the true running max
+// minus kLazy, every P is at most 2^kLazy.
 //
 // A TMA warp loads the pair's Q tiles (two slots, so the next item's Q lands
 // while the current one runs) and streams K and V tiles through kStages-deep
-// rings.  Every wait is bounded.
+// rings; both MMA threads release each stage.  Every wait is bounded.
 #include <math.h>
 
 #include "rf_device.cuh"
@@ -47,16 +49,20 @@ constexpr int kTile = 128 * kD * 2;                   // 16 KB: 128 rows x 128 B
 constexpr int kQOff = 0;                              // [slot][x] Q tiles
 constexpr int kKOff = kQOff + 4 * kTile;
 constexpr int kVOff = kKOff + kStages * kTile;
-constexpr int kBarOff = kVOff + kStages * kTile;
-constexpr int kSmem = kBarOff + 256 + 1024;           // + alignment slack
-constexpr int kThreads = 320;                         // warp 0 TMA, 1 MMA, 2-5 / 6-9 softmax a / b
+constexpr int kStOff = kVOff + kStages * kTile;       // [x] O tiles staged for the bulk store
+constexpr int kBarOff = kStOff + 2 * kTile;
+constexpr int kSmem = kBarOff + 512 + 1024;           // + alignment slack
+constexpr int kThreads = 352;   // warp 0 TMA, 1 / 10 MMA of tile a / b, 2-5 / 6-9 softmax a / b
+constexpr int kMmaWarpB = 10;
 constexpr int kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128;          // S_x, fp32 (P_x as bf16 pairs in its first 64)
+constexpr uint32_t kColS0 = 0, kColS1 = 128;          // S_x, fp32
 constexpr uint32_t kColO0 = 256, kColO1 = 320;        // O_x, fp32
+constexpr uint32_t kColP0 = 384, kColP1 = 448;        // P_x, bf16 pairs
 constexpr uint32_t kIdescS = make_idesc(BQ, BKV, /*bf16*/ 1, 0, 0);
 constexpr uint32_t kIdescO = make_idesc(BQ, kD, /*bf16*/ 1, 0, /*V MN-major*/ 1);
 constexpr float kLazy = 8.f;                          // reference may trail the max by 2^8
 static_assert(kSmem <= 227 * 1024, "shared memory");
+static_assert(kStOff % 1024 == 0, "staged O tiles on 1 KB (swizzle atom) boundaries");
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -66,15 +72,20 @@ __device__ __forceinline__ float ex2(float x) {
 
 __device__ __forceinline__ uint32_t col_s(int x) { return x ? kColS1 : kColS0; }
 __device__ __forceinline__ uint32_t col_o(int x) { return x ? kColO1 : kColO0; }
+__device__ __forceinline__ uint32_t col_p(int x) { return x ? kColP1 : kColP0; }
 
 struct Bars {
   uint64_t q_full[2], q_empty[2];                    // per Q slot (both tiles of an item)
   uint64_t k_full[kStages], k_empty[kStages];
   uint64_t v_full[kStages], v_empty[kStages];
   uint64_t s_full[2];                                // per query tile x: S_x complete
+  uint64_t s_read[2];                                // per x: S_x is in the softmax registers (4 warps)
   uint64_t p_full[2];                                // per x: P_x written (128 arrivals)
+  uint64_t pv_done[2];                               // per x: the last P_x V has completed
   uint64_t o_done[2];                                // per x: the item's last P_x V complete
-  uint64_t drain;
+  uint64_t drain[2];                                 // per issuer: its MMAs have completed
+  uint64_t st_full[2];                               // per x: the staged O tile is written (4 warps)
+  uint64_t st_free[2];                               // per x: the last bulk store has read it
   uint32_t tmem;
   int abort;
 };
@@ -96,8 +107,9 @@ __device__ __forceinline__ Item item_of(int it, int n_bh, int nq) {
 __global__ void __launch_bounds__(kThreads, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap tmQ,
                         const __grid_constant__ CUtensorMap tmK,
-                        const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
-                        int Lq, int Lk, float c_log2, int n_bh, int nq, unsigned* err) {
+                        const __grid_constant__ CUtensorMap tmV,
+                        const __grid_constant__ CUtensorMap tmO, int Lq, int Lk, float c_log2,
+                        int n_bh, int nq, unsigned* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -111,20 +123,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmQ);
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
+    prefetch_tmap(&tmO);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars->q_full[i]), 1);
-      mbar_init(smem_u32(&bars->q_empty[i]), 1);
+      mbar_init(smem_u32(&bars->q_empty[i]), 2);     // one commit per issuer
       mbar_init(smem_u32(&bars->s_full[i]), 1);
+      mbar_init(smem_u32(&bars->s_read[i]), 4);
       mbar_init(smem_u32(&bars->p_full[i]), BQ);
+      mbar_init(smem_u32(&bars->pv_done[i]), 1);
       mbar_init(smem_u32(&bars->o_done[i]), 1);
+      mbar_init(smem_u32(&bars->st_full[i]), 4);
+      mbar_init(smem_u32(&bars->st_free[i]), 1);
     }
     for (int i = 0; i < kStages; ++i) {
       mbar_init(smem_u32(&bars->k_full[i]), 1);
-      mbar_init(smem_u32(&bars->k_empty[i]), 1);
+      mbar_init(smem_u32(&bars->k_empty[i]), 2);
       mbar_init(smem_u32(&bars->v_full[i]), 1);
-      mbar_init(smem_u32(&bars->v_empty[i]), 1);
+      mbar_init(smem_u32(&bars->v_empty[i]), 2);
     }
-    mbar_init(smem_u32(&bars->drain), 1);
+    mbar_init(smem_u32(&bars->drain[0]), 1);
+    mbar_init(smem_u32(&bars->drain[1]), 1);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -188,13 +206,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == kMmaWarpB) {
     if (lane == 0) {
-      // ------------------------------------------------ MMA issuer
+      // ------------------------------------------------ MMA issuers, one per query tile
+      // Thread x issues its tile's products in the tile's own order: S_x(j+1)
+      // as soon as the softmax warps have read S_x(j), P_x V(j) once P_x(j)
+      // is written; neither tile waits behind the other's events.  Both
+      // threads release every K/V stage and Q slot (barrier counts 2), each
+      // after waiting for that stage itself, so neither runs a phase ahead.
+      const int x = warp == 1 ? 0 : 1;
       bool ok = true;
-      int np[2] = {0, 0};                            // P tiles consumed per query tile
-      // S_x(g) = Q_x K_g^T, Q from slot qs
-      auto issue_s = [&](int x, int g, int qs) {
+      int np = 0;                                    // P tiles consumed
+      int nsr = 0;                                   // S reads waited for
+      bool unread = false;                           // an issued S_x not yet known to be read
+      // S_x(g) = Q_x K_g^T, Q from slot qs; S_x's columns are free once the
+      // softmax warps have read the previous S_x into registers
+      auto issue_s = [&](int g, int qs) -> bool {
+        if (unread) {
+          if (!mbar_wait(smem_u32(&bars->s_read[x]), (uint32_t)(nsr & 1))) return false;
+          ++nsr;
+          tc_fence_after();
+        }
         const uint32_t qa = smem_u32(smem + kQOff + (2 * qs + x) * kTile);
         const uint32_t ka = smem_u32(smem + kKOff + (g % kStages) * kTile);
 #pragma unroll
@@ -202,21 +234,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ss(tmem + col_s(x), sw128_desc(qa + kk * 32, 1024, 16),
                       sw128_desc(ka + kk * 32, 1024, 16), kIdescS, kk != 0);
         mma_commit(smem_u32(&bars->s_full[x]));
-      };
-      // the softmax warpgroup has written P_x (and read S_x)
-      auto wait_p = [&](int x) -> bool {
-        if (!mbar_wait(smem_u32(&bars->p_full[x]), (uint32_t)(np[x] & 1))) return false;
-        tc_fence_after();
-        ++np[x];
+        unread = true;
         return true;
       };
-      // O_x (+)= P_x V_g, P_x from the first 64 columns of S_x
-      auto issue_pv = [&](int x, int g, bool first) {
+      // O_x (+)= P_x V_g, P_x from its own columns; pv_done[x] tells the
+      // softmax warps when P_x may be overwritten and O_x is up to date
+      auto issue_pv = [&](int g, bool first) {
         const uint32_t va = smem_u32(smem + kVOff + (g % kStages) * kTile);
 #pragma unroll
         for (int kk = 0; kk < BKV / 16; ++kk)
-          mma_bf16_ts(tmem + col_o(x), tmem + col_s(x) + kk * 8,
+          mma_bf16_ts(tmem + col_o(x), tmem + col_p(x) + kk * 8,
                       sw128_desc(va + kk * 16 * 128, 1024, kTile), kIdescO, (!first || kk != 0));
+        mma_commit(smem_u32(&bars->pv_done[x]));
       };
       auto wait_kv = [&](uint64_t* full, int g) -> bool {
         if (!mbar_wait(smem_u32(&full[g % kStages]), (uint32_t)((g / kStages) & 1))) return false;
@@ -228,44 +257,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       Item w = item_of(it, n_bh, nq);
       if (it < n_items) {
         ok = mbar_wait(smem_u32(&bars->q_full[0]), 0) && wait_kv(bars->k_full, 0);
-        if (ok) {
-          tc_fence_after();
-          issue_s(0, 0, 0);
-          if (w.has_b) issue_s(1, 0, 0);
-          mma_commit(smem_u32(&bars->k_empty[0]));
-        }
+        if (ok && (x == 0 || w.has_b)) ok = issue_s(0, 0);
+        if (ok) mma_commit(smem_u32(&bars->k_empty[0]));
       }
       for (; ok && it < n_items; it += gridDim.x, ++ni) {
         const int qs = ni & 1;
         const int it_next = it + gridDim.x;
         const Item wn = item_of(it_next, n_bh, nq);
+        const bool mine = x == 0 || w.has_b;
         for (int j = 0; ok && j < nkv; ++j, ++g) {
           const bool last = j == nkv - 1;
           // next tile: the same item's, or the next item's first
           const bool has_next = !last || it_next < n_items;
           const int qs_next = last ? qs ^ 1 : qs;
-          const bool next_b = last ? wn.has_b : w.has_b;
-          if (has_next && last &&
-              !(ok = mbar_wait(smem_u32(&bars->q_full[qs_next]), (uint32_t)(((ni + 1) >> 1) & 1))))
-            break;
-          // query tile a: P.V, then its next S (which overwrites P_a)
-          if (!(ok = wait_p(0) && wait_kv(bars->v_full, g))) break;
-          issue_pv(0, g, j == 0);
-          if (last) mma_commit(smem_u32(&bars->o_done[0]));
-          if (has_next) {
-            if (!(ok = wait_kv(bars->k_full, g + 1))) break;
-            issue_s(0, g + 1, qs_next);
-          }
-          // query tile b likewise
-          if (w.has_b) {
-            if (!(ok = wait_p(1))) break;
-            issue_pv(1, g, j == 0);
-            if (last) mma_commit(smem_u32(&bars->o_done[1]));
-          }
-          if (has_next && next_b) issue_s(1, g + 1, qs_next);
-          mma_commit(smem_u32(&bars->v_empty[g % kStages]));
-          if (has_next) mma_commit(smem_u32(&bars->k_empty[(g + 1) % kStages]));
-          if (last) mma_commit(smem_u32(&bars->q_empty[qs]));   // every S of the item issued
+          const bool next_mine = x == 0 || (last ? wn.has_b : w.has_b);
+          // the next S, as soon as the softmax warps have read the current
+          // one (their exponentials then overlap this product)
+          auto next_s = [&]() -> bool {
+            if (!has_next) return true;
+            if (last && !mbar_wait(smem_u32(&bars->q_full[qs_next]), (uint32_t)(((ni + 1) >> 1) & 1)))
+              return false;
+            if (!wait_kv(bars->k_full, g + 1)) return false;
+            if (next_mine && !issue_s(g + 1, qs_next)) return false;
+            mma_commit(smem_u32(&bars->k_empty[(g + 1) % kStages]));
+            return true;
+          };
+          // this key tile's P.V
+          auto this_pv = [&]() -> bool {
+            if (!wait_kv(bars->v_full, g)) return false;
+            if (mine) {
+              if (!mbar_wait(smem_u32(&bars->p_full[x]), (uint32_t)(np & 1))) return false;
+              tc_fence_after();
+              ++np;
+              issue_pv(g, j == 0);
+              if (last) mma_commit(smem_u32(&bars->o_done[x]));
+            }
+            mma_commit(smem_u32(&bars->v_empty[g % kStages]));
+            if (last) mma_commit(smem_u32(&bars->q_empty[qs]));   // every S of the item issued
+            return true;
+          };
+          // within an item the next S goes first; at its last key tile the
+          // P.V goes first, so the epilogue's O is complete as early as
+          // possible (the softmax warps store O before they read the next S)
+          ok = last ? (this_pv() && next_s()) : (next_s() && this_pv());
         }
         w = wn;
       }
@@ -275,8 +309,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // nothing may still run on the tensor core when TMEM and shared memory
       // are released
-      mma_commit(smem_u32(&bars->drain));
-      (void)mbar_wait(smem_u32(&bars->drain), 0, 1000000000ull);
+      mma_commit(smem_u32(&bars->drain[x]));
+      (void)mbar_wait(smem_u32(&bars->drain[x]), 0, 1000000000ull);
     }
   } else {
     // ------------------------------------------------ softmax warpgroups
@@ -286,6 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
     const uint32_t s_addr = tmem + lane_off + col_s(x);
     const uint32_t o_addr = tmem + lane_off + col_o(x);
+    static_assert(kColP1 - kColO1 == kColP0 - kColO0, "P_x at a fixed offset from O_x");
+    const uint32_t p_addr = o_addr + (kColP0 - kColO0);
     const uint64_t c2 = f2(c_log2, c_log2);
     bool ok = true;
     int cnt = 0, icnt = 0;                             // tiles and items of this warpgroup
@@ -309,6 +345,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q = 0; q < 4; ++q) tmem_ld32(s_addr + q * 32, v[q]);
         tmem_ld_wait();
+        // S_x is in registers: the MMA warp may compute the next S_x into
+        // the same columns while this tile's exponentials run
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->s_read[x]));
         // pass 1: row max (four independent chains)
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
@@ -336,9 +377,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           need = true;
         }
         const uint64_t negm2 = f2(-m_ref, -m_ref);
-        // pass 2: P = 2^(S c - m) as bf16 pairs, row sum (four chains); P
-        // goes over S columns 0-63, all of S being in registers by now
+        // pass 2: P = 2^(S c - m) as bf16 pairs, row sum (four chains),
+        // written to P_x half by half; before the first half, the previous
+        // P_x V must have completed: P_x may then be overwritten and O_x
+        // holds every earlier tile (warp-uniform: the TMEM accesses are
+        // warp-collective)
         uint64_t sum4[4] = {0ull, 0ull, 0ull, 0ull};
+        bool pv_ok = true;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           uint32_t pk[32];
@@ -361,13 +406,23 @@ __global__ void __launch_bounds__(kThreads, 1)
               pk[h * 16 + i] = pack_bf16x2(p0, p1);
             }
           }
-          tmem_st32(s_addr + hh * 32, pk);
+          if (hh == 0 && cnt > 0) {
+            pv_ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->pv_done[x]),
+                                                      (uint32_t)((cnt - 1) & 1)));
+            if (!pv_ok) break;
+            tc_fence_after();
+          }
+          tmem_st32(p_addr + hh * 32, pk);
+        }
+        if (!pv_ok) {
+          ok = false;
+          break;
         }
         float s_lo, s_hi;
         f2_split(fadd2(fadd2(sum4[0], sum4[1]), fadd2(sum4[2], sum4[3])), s_lo, s_hi);
         l_run += s_lo + s_hi;
         // a moved reference: O_x (complete through the previous tile, since
-        // S_x of this tile is) is rescaled before this tile's P.V adds to it
+        // its P.V is) is rescaled before this tile's P.V adds to it
         if (__any_sync(0xffffffffu, need)) {
           uint32_t o[2][32];
           tmem_ld32(o_addr, o[0]);
@@ -391,29 +446,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
         break;
       }
-      ++icnt;
+      const int e = icnt++;                              // items of this warpgroup so far
       tc_fence_after();
       uint32_t v[2][32];
       tmem_ld32(o_addr, v[0]);
       tmem_ld32(o_addr + 32, v[1]);
       tmem_ld_wait();
       tc_fence_before();                               // O read before the next P.V may overwrite it
-      const int row = (w.qa + x) * BQ + r;
-      const int64_t o_first = ((int64_t)w.bh * Lq + row) * kD;
-      if (row < Lq && RF_IN(err, o_first + kD - 1, (int64_t)n_bh * Lq * kD)) {
-        const float inv = 1.f / l_run;
-        uint4* dst = reinterpret_cast<uint4*>(O + o_first);
-#pragma unroll
-        for (int c = 0; c < kD / 8; ++c) {
-          const uint32_t* u = &v[c >> 2][(c & 3) * 8];
-          dst[c] = make_uint4(
-              pack_bf16x2(__uint_as_float(u[0]) * inv, __uint_as_float(u[1]) * inv),
-              pack_bf16x2(__uint_as_float(u[2]) * inv, __uint_as_float(u[3]) * inv),
-              pack_bf16x2(__uint_as_float(u[4]) * inv, __uint_as_float(u[5]) * inv),
-              pack_bf16x2(__uint_as_float(u[6]) * inv, __uint_as_float(u[7]) * inv));
+      // O_x / l as bf16, staged in shared memory as 128-byte swizzled rows
+      // and written by one bulk tensor store per tile (rows past Lq are
+      // outside the tensor map and are not written).  The staging tile is
+      // reused once the previous store has read it.
+      const bool issuer = sub == 0 && lane == 0;
+      if (e > 0) {
+        if (issuer) {
+          bulk_wait_group_read0();
+          mbar_arrive(smem_u32(&bars->st_free[x]));
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->st_free[x]), (uint32_t)((e - 1) & 1)))) {
+          ok = false;
+          break;
         }
       }
+      uint8_t* st = smem + kStOff + x * kTile + r * 128;
+      const float inv = 1.f / l_run;
+#pragma unroll
+      for (int c = 0; c < kD / 8; ++c) {
+        const uint32_t* u = &v[c >> 2][(c & 3) * 8];
+        *reinterpret_cast<uint4*>(st + ((c ^ (r & 7)) << 4)) = make_uint4(
+            pack_bf16x2(__uint_as_float(u[0]) * inv, __uint_as_float(u[1]) * inv),
+            pack_bf16x2(__uint_as_float(u[2]) * inv, __uint_as_float(u[3]) * inv),
+            pack_bf16x2(__uint_as_float(u[4]) * inv, __uint_as_float(u[5]) * inv),
+            pack_bf16x2(__uint_as_float(u[6]) * inv, __uint_as_float(u[7]) * inv));
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->st_full[x]));
+      bool st_ok = true;
+      if (issuer) {
+        st_ok = mbar_wait(smem_u32(&bars->st_full[x]), (uint32_t)(e & 1)) &&
+                RF_IN(err, w.bh, n_bh) && RF_IN(err, (w.qa + x) * BQ, Lq);
+        if (st_ok) {
+          tma_store_3d(&tmO, smem_u32(smem + kStOff + x * kTile), 0, (w.qa + x) * BQ, w.bh);
+          bulk_commit_group();
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, st_ok, 0)) {
+        ok = false;
+        break;
+      }
     }
+    // every bulk store of this warpgroup has completed before the CTA exits
+    if (sub == 0 && lane == 0 && icnt > 0) bulk_wait_group0();
     if (!ok) {
       raise_error(err, kDevErrTimeout);
       *abort_flag = 1;
@@ -433,9 +517,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_attn_prefill_tc(const void* Q, const void* K, const void* V, void* O, int B,
                                    int H, int Lq, int Lk, float scale, unsigned* err,
                                    cudaStream_t s) {
-  CUtensorMap tmQ, tmK, tmV;
+  CUtensorMap tmQ, tmK, tmV, tmO;
   const uint64_t q_rows = (uint64_t)B * H * Lq, kv_rows = (uint64_t)B * H * Lk;
+  // O as [B*H][Lq][64]: a store box of 128 rows is clipped at its head's Lq
   if (!encode_tmap_2d(&tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Q, kD, q_rows, kD * 2, kD, BQ, true) ||
+      !encode_tmap_3d(&tmO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, O, kD, (uint64_t)Lq, (uint64_t)B * H,
+                      kD * 2, (uint64_t)Lq * kD * 2, kD, BQ, 1, true) ||
       !encode_tmap_2d(&tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, kD, kv_rows, kD * 2, kD, BKV, true) ||
       !encode_tmap_2d(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, kD, kv_rows, kD * 2, kD, BKV, true))
     return cudaErrorInvalidValue;
@@ -450,8 +537,8 @@ cudaError_t launch_attn_prefill_tc(const void* Q, const void* K, const void* V, 
   const int64_t per_cta = (items + sms - 1) / sms;
   const int grid = (int)((items + per_cta - 1) / per_cta);
   const float c_log2 = scale * 1.4426950408889634f;
-  attn_prefill_kernel<<<grid, kThreads, kSmem, s>>>(tmQ, tmK, tmV, static_cast<__nv_bfloat16*>(O),
-                                                    Lq, Lk, c_log2, n_bh, nq, err);
+  attn_prefill_kernel<<<grid, kThreads, kSmem, s>>>(tmQ, tmK, tmV, tmO, Lq, Lk, c_log2, n_bh, nq,
+                                                    err);
   return cudaGetLastError();
 }
 
