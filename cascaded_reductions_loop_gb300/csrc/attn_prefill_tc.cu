@@ -27,7 +27,8 @@
 // products never wait behind the other tile's softmax; within a tile the
 // next S is issued as soon as the current one has been read, the P.V as soon
 // as P is written (at a pair's last key tile the P.V first, so O is complete
-// early).  Any reference m gives the same result ([S] Methodologie 1: the
+// early).  Tile b starts once tile a's softmax has taken its first row
+// maxima, so the two softmax warpgroups run out of phase.  Any reference m gives the same result ([S] Methodologie 1: the
 // dependent factor 2^-m is invertible); with m at least the true running max
 // minus kLazy, every P is at most 2^kLazy.
 //
@@ -86,6 +87,7 @@ struct Bars {
   uint64_t drain[2];                                 // per issuer: its MMAs have completed
   uint64_t st_full[2];                               // per x: the staged O tile is written (4 warps)
   uint64_t st_free[2];                               // per x: the last bulk store has read it
+  uint64_t a_max0;                                   // tile a's first row maxima are taken (4 warps)
   uint32_t tmem;
   int abort;
 };
@@ -141,6 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bars->v_full[i]), 1);
       mbar_init(smem_u32(&bars->v_empty[i]), 2);
     }
+    mbar_init(smem_u32(&bars->a_max0), 4);
     mbar_init(smem_u32(&bars->drain[0]), 1);
     mbar_init(smem_u32(&bars->drain[1]), 1);
     bars->abort = 0;
@@ -257,6 +260,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       Item w = item_of(it, n_bh, nq);
       if (it < n_items) {
         ok = mbar_wait(smem_u32(&bars->q_full[0]), 0) && wait_kv(bars->k_full, 0);
+        // tile b starts once tile a's softmax has taken its first row maxima,
+        // so that the two softmax warpgroups run out of phase (one's
+        // exponentials beside the other's max pass) rather than both loading
+        // the MUFU at once
+        if (ok && x == 1 && w.has_b) ok = mbar_wait(smem_u32(&bars->a_max0), 0);
         if (ok && (x == 0 || w.has_b)) ok = issue_s(0, 0);
         if (ok) mma_commit(smem_u32(&bars->k_empty[0]));
       }
@@ -366,6 +374,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         const float mt = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]) * c_log2;
+        if (x == 0 && cnt == 0) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bars->a_max0));
+        }
         float alpha = 1.f;
         bool need = false;
         if (j == 0) {
