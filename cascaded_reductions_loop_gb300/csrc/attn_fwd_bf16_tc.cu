@@ -656,7 +656,7 @@ cudaError_t launch_attn_fwd_bf16_tc(const void* Q, const void* K, const void* V,
                                     int H, int Lq, int Lk, int d, float scale, int causal,
                                     int two_pass, unsigned* err, cudaStream_t s) {
   (void)d;
-  if (!two_pass && !causal) return launch_attn_prefill_tc(Q, K, V, O, B, H, Lq, Lk, scale, err, s);
+  if (!two_pass) return launch_attn_prefill_tc(Q, K, V, O, B, H, Lq, Lk, scale, causal, err, s);
   CUtensorMap tmQ, tmK, tmV;
   const uint64_t q_rows = (uint64_t)B * H * Lq, kv_rows = (uint64_t)B * H * Lk;
   if (!encode_tmap_2d(&tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Q, kD, q_rows, kD * 2, kD, BQ, true) ||

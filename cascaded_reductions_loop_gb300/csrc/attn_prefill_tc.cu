@@ -1,6 +1,9 @@
 // attn_prefill_tc.cu -- single-segment fused attention, fixed-length layout
-// [B][H][L][64], no mask: the BERT-style prefill path (bf16 in, fp32
-// accumulation and softmax state, bf16 out).
+// [B][H][L][64], with or without the causal mask: the BERT-style prefill path
+// (bf16 in, fp32 accumulation and softmax state, bf16 out).  Under the causal
+// mask row i reads keys j <= i + Lk - Lq; each query tile reads only the key
+// tiles its last row needs, scores of keys a row does not read are set to
+// -inf (their P is 0), and a row that reads no key is written as zeros.
 //
 // Safe-softmax cascade ([E] §2.2) in the single-loop incremental form ([E]
 // §2.3, §4.1; [S] Methodologie 2, single-segment strategy of Methodologie 3).
@@ -96,16 +99,31 @@ struct Bars {
 struct Item {
   int bh, qa;
   bool has_b;
+  int nkv_a, nkv_b, nkv;   // key tiles tile a / tile b read; key tiles loaded for the pair
 };
 
-__device__ __forceinline__ Item item_of(int it, int n_bh, int nq) {
+// Keys the last row of query tile qt may read (all Lk without the causal
+// mask; with it, keys j <= i + Lk - Lq of row i, clamped to 0..Lk), as a
+// count of 128-key tiles, at least one: a tile whose rows read no key still
+// runs one fully masked key tile and writes zeros.
+__device__ __forceinline__ int tiles_of(int qt, int Lq, int Lk, bool causal) {
+  int end = Lk;
+  if (causal) end = max(0, min(Lk, min((qt + 1) * BQ, Lq) + (Lk - Lq)));
+  return max(1, (end + BKV - 1) / BKV);
+}
+
+__device__ __forceinline__ Item item_of(int it, int n_bh, int nq, int Lq, int Lk, bool causal) {
   Item w;
   w.bh = it % n_bh;
   w.qa = 2 * (it / n_bh);
   w.has_b = w.qa + 1 < nq;
+  w.nkv_a = tiles_of(w.qa, Lq, Lk, causal);
+  w.nkv_b = w.has_b ? tiles_of(w.qa + 1, Lq, Lk, causal) : 0;
+  w.nkv = max(w.nkv_a, w.nkv_b);
   return w;
 }
 
+template <bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap tmQ,
                         const __grid_constant__ CUtensorMap tmK,
@@ -119,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_items = n_bh * ((nq + 1) / 2);
-  const int nkv = (Lk + BKV - 1) / BKV;
+  constexpr bool causal = kCausal;
 
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmQ);
@@ -165,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int ni = 0, g = 0;                             // items and K/V tiles issued
       for (int it = blockIdx.x; ok && it < n_items && !*abort_flag; it += gridDim.x, ++ni) {
-        const Item w = item_of(it, n_bh, nq);
+        const Item w = item_of(it, n_bh, nq, Lq, Lk, causal);
         const int slot = ni & 1;
         if (ni >= 2 &&
             !mbar_wait(smem_u32(&bars->q_empty[slot]), (uint32_t)(((ni >> 1) - 1) & 1))) {
@@ -178,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(smem_u32(smem + kQOff + (2 * slot) * kTile), &tmQ, qb, 0, q_row);
         if (w.has_b) tma_load_2d(smem_u32(smem + kQOff + (2 * slot + 1) * kTile), &tmQ, qb, 0, q_row + BQ);
         const int kv_row = w.bh * Lk;
-        for (int j = 0; j < nkv; ++j, ++g) {
+        for (int j = 0; j < w.nkv; ++j, ++g) {
           const int st = g % kStages;
           const uint32_t ph = (uint32_t)(((g / kStages) + 1) & 1);
           if (g >= kStages && !mbar_wait(smem_u32(&bars->k_empty[st]), ph)) {
@@ -257,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       int ni = 0, g = 0;
       int it = blockIdx.x;
-      Item w = item_of(it, n_bh, nq);
+      Item w = item_of(it, n_bh, nq, Lq, Lk, causal);
       if (it < n_items) {
         ok = mbar_wait(smem_u32(&bars->q_full[0]), 0) && wait_kv(bars->k_full, 0);
         // tile b starts once tile a's softmax has taken its first row maxima,
@@ -271,14 +289,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (; ok && it < n_items; it += gridDim.x, ++ni) {
         const int qs = ni & 1;
         const int it_next = it + gridDim.x;
-        const Item wn = item_of(it_next, n_bh, nq);
-        const bool mine = x == 0 || w.has_b;
-        for (int j = 0; ok && j < nkv; ++j, ++g) {
-          const bool last = j == nkv - 1;
+        const Item wn = item_of(it_next, n_bh, nq, Lq, Lk, causal);
+        // key tiles this query tile reads (0 for a missing tile b); the
+        // pair's loaded tiles may run past them under the causal mask
+        const int nkv_x = x == 0 ? w.nkv_a : w.nkv_b;
+        for (int j = 0; ok && j < w.nkv; ++j, ++g) {
+          const bool last = j == w.nkv - 1;            // the pair's last key tile
+          const bool mine = j < nkv_x;
           // next tile: the same item's, or the next item's first
           const bool has_next = !last || it_next < n_items;
           const int qs_next = last ? qs ^ 1 : qs;
-          const bool next_mine = x == 0 || (last ? wn.has_b : w.has_b);
+          const bool next_mine = last ? (x == 0 || wn.has_b) : j + 1 < nkv_x;
           // the next S, as soon as the softmax warps have read the current
           // one (their exponentials then overlap this product)
           auto next_s = [&]() -> bool {
@@ -298,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_fence_after();
               ++np;
               issue_pv(g, j == 0);
-              if (last) mma_commit(smem_u32(&bars->o_done[x]));
+              if (j == nkv_x - 1) mma_commit(smem_u32(&bars->o_done[x]));
             }
             mma_commit(smem_u32(&bars->v_empty[g % kStages]));
             if (last) mma_commit(smem_u32(&bars->q_empty[qs]));   // every S of the item issued
@@ -334,10 +355,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int cnt = 0, icnt = 0;                             // tiles and items of this warpgroup
     for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-      const Item w = item_of(it, n_bh, nq);
+      const Item w = item_of(it, n_bh, nq, Lq, Lk, causal);
       if (x == 1 && !w.has_b) continue;
+      const int nkv_x = x == 0 ? w.nkv_a : w.nkv_b;
+      // keys this row reads: all Lk, or under the causal mask j <= i + Lk - Lq
+      const int kv_row =
+          causal ? max(0, min(Lk, (w.qa + x) * BQ + r + (Lk - Lq) + 1)) : Lk;
       float m_ref = -INFINITY, l_run = 0.f;
-      for (int j = 0; j < nkv; ++j, ++cnt) {
+      for (int j = 0; j < nkv_x; ++j, ++cnt) {
         // warp-uniform decision: the TMEM loads below are warp-collective
         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[x]), (uint32_t)(cnt & 1)) &&
                                          !*abort_flag)) {
@@ -345,7 +370,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const int valid = min(BKV, Lk - j * BKV);      // keys of this tile that exist
+        // keys of this tile the row reads (a prefix; 0 for a row that reads
+        // none: its P is all zero and its output row zero)
+        const int valid = max(0, min(BKV, kv_row - j * BKV));
         const bool full = valid == BKV;
         // the row's 128 scores read from tensor memory once (four loads in
         // flight together) and kept in registers for both passes
@@ -358,21 +385,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->s_read[x]));
+        // keys the row does not read score -inf: their P is 2^-inf = 0, so
+        // both passes below run without per-key tests
+        if (!full) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              v[q][i] = q * 32 + i < valid ? v[q][i] : 0xff800000u;
+        }
         // pass 1: row max (four independent chains)
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (full) {
+        for (int q = 0; q < 4; ++q)
 #pragma unroll
-            for (int i = 0; i < 32; i += 2)
-              mx4[(i >> 1) & 3] =
-                  fmax3(mx4[(i >> 1) & 3], __uint_as_float(v[q][i]), __uint_as_float(v[q][i + 1]));
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (q * 32 + i < valid) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(v[q][i]));
-          }
-        }
+          for (int i = 0; i < 32; i += 2)
+            mx4[(i >> 1) & 3] =
+                fmax3(mx4[(i >> 1) & 3], __uint_as_float(v[q][i]), __uint_as_float(v[q][i + 1]));
         const float mt = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]) * c_log2;
         if (x == 0 && cnt == 0) {
           __syncwarp();
@@ -388,7 +417,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_ref = mt;
           need = true;
         }
-        const uint64_t negm2 = f2(-m_ref, -m_ref);
+        // a row that has read no key yet (m = -inf) takes 0 as its reference:
+        // its P is then 2^-inf = 0, not NaN
+        const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+        const uint64_t negm2 = f2(-m_use, -m_use);
         // pass 2: P = 2^(S c - m) as bf16 pairs, row sum (four chains),
         // written to P_x half by half; before the first half, the previous
         // P_x V must have completed: P_x may then be overwritten and O_x
@@ -408,12 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               f2_split(ffma2(f2(__uint_as_float(v[q][2 * i]), __uint_as_float(v[q][2 * i + 1])), c2,
                              negm2),
                        t0, t1);
-              float p0 = ex2(t0), p1 = ex2(t1);
-              if (!full) {
-                const int c0 = q * 32 + 2 * i;
-                p0 = c0 < valid ? p0 : 0.f;
-                p1 = c0 + 1 < valid ? p1 : 0.f;
-              }
+              const float p0 = ex2(t0), p1 = ex2(t1);
               sum4[i & 3] = fadd2(sum4[i & 3], f2(p0, p1));
               pk[h * 16 + i] = pack_bf16x2(p0, p1);
             }
@@ -481,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       uint8_t* st = smem + kStOff + x * kTile + r * 128;
-      const float inv = 1.f / l_run;
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;   // a row that read no key: zeros
 #pragma unroll
       for (int c = 0; c < kD / 8; ++c) {
         const uint32_t* u = &v[c >> 2][(c & 3) * 8];
@@ -527,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_attn_prefill_tc(const void* Q, const void* K, const void* V, void* O, int B,
-                                   int H, int Lq, int Lk, float scale, unsigned* err,
+                                   int H, int Lq, int Lk, float scale, int causal, unsigned* err,
                                    cudaStream_t s) {
   CUtensorMap tmQ, tmK, tmV, tmO;
   const uint64_t q_rows = (uint64_t)B * H * Lq, kv_rows = (uint64_t)B * H * Lk;
@@ -538,8 +565,8 @@ cudaError_t launch_attn_prefill_tc(const void* Q, const void* K, const void* V, 
       !encode_tmap_2d(&tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, kD, kv_rows, kD * 2, kD, BKV, true) ||
       !encode_tmap_2d(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, kD, kv_rows, kD * 2, kD, BKV, true))
     return cudaErrorInvalidValue;
-  cudaError_t e =
-      cudaFuncSetAttribute(attn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  auto kern = causal ? attn_prefill_kernel<true> : attn_prefill_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   const int nq = (Lq + BQ - 1) / BQ, n_bh = B * H;
   const int64_t items = (int64_t)n_bh * ((nq + 1) / 2);
@@ -549,8 +576,7 @@ cudaError_t launch_attn_prefill_tc(const void* Q, const void* K, const void* V, 
   const int64_t per_cta = (items + sms - 1) / sms;
   const int grid = (int)((items + per_cta - 1) / per_cta);
   const float c_log2 = scale * 1.4426950408889634f;
-  attn_prefill_kernel<<<grid, kThreads, kSmem, s>>>(tmQ, tmK, tmV, tmO, Lq, Lk, c_log2, n_bh, nq,
-                                                    err);
+  kern<<<grid, kThreads, kSmem, s>>>(tmQ, tmK, tmV, tmO, Lq, Lk, c_log2, n_bh, nq, err);
   return cudaGetLastError();
 }
 

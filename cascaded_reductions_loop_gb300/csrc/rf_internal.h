@@ -50,7 +50,7 @@ cudaError_t launch_attn_fwd_bf16_tc(const void* Q, const void* K, const void* V,
 // Fixed-length, unmasked, incremental: two query tiles per CTA in ping-pong,
 // P and O in tensor memory (the BERT-style prefill path).
 cudaError_t launch_attn_prefill_tc(const void* Q, const void* K, const void* V, void* O, int B,
-                                   int H, int Lq, int Lk, float scale, unsigned* err,
+                                   int H, int Lq, int Lk, float scale, int causal, unsigned* err,
                                    cudaStream_t s);
 
 // Packed variable-length layout: Q/O [total_q][H][d], K/V [total_k][H][d],
