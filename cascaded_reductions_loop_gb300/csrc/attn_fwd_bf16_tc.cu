@@ -1,6 +1,13 @@
 // attn_fwd_bf16_tc.cu -- single-segment fused attention on the tcgen05 tensor
 // cores (bf16 in, fp32 accumulation and softmax state, bf16 out), d = 64.
 //
+// The calls it serves: the non-incremental (two-pass) mode below.  The
+// single-pass calls, fixed-length and packed, with or without the causal
+// mask, go to attn_prefill_kernel (attn_prefill_tc.cu), which keeps two
+// query tiles per CTA and issues their products from one thread each; the
+// incremental path of this kernel (which the two-pass mode is built on) and
+// its packed layout are no longer launched.
+//
 // Safe-softmax cascade ([E] §2.2) in the single-loop incremental form ([E]
 // §2.3, §4.1; [S] Methodologie 2, single-segment strategy of Methodologie 3):
 // one CTA owns 128 query rows of one (batch, head) and walks all key tiles of
@@ -663,11 +670,8 @@ cudaError_t launch_attn_fwd_bf16_tc(const void* Q, const void* K, const void* V,
       !encode_tmap_2d(&tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, kD, kv_rows, kD * 2, kD, BKV, true) ||
       !encode_tmap_2d(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, kD, kv_rows, kD * 2, kD, BKV, true))
     return cudaErrorInvalidValue;
-  if (two_pass && Lk > kKV * BKV) return cudaErrorInvalidValue;
-  auto kern = two_pass ? (causal ? attn_fwd_bf16_kernel<false, true, true>
-                                 : attn_fwd_bf16_kernel<false, true, false>)
-                       : (causal ? attn_fwd_bf16_kernel<false, false, true>
-                                 : attn_fwd_bf16_kernel<false, false, false>);
+  if (Lk > kKV * BKV) return cudaErrorInvalidValue;
+  auto kern = causal ? attn_fwd_bf16_kernel<false, true, true> : attn_fwd_bf16_kernel<false, true, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   const int nq = (Lq + BQ - 1) / BQ, n_bh = B * H;
@@ -683,28 +687,8 @@ cudaError_t launch_attn_fwd_bf16_tc_varlen(const void* Q, const void* K, const v
                                            const int* cu_q, const int* cu_k, int B, int H,
                                            int max_q, int total_q, int total_k, float scale,
                                            int causal, unsigned* err, cudaStream_t s) {
-  CUtensorMap tmQ, tmK, tmV;
-  const uint64_t pitch = (uint64_t)H * kD * 2;     // bytes between tokens
-  if (!encode_tmap_3d(&tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Q, kD, H, total_q, kD * 2, pitch,
-                      kD, 1, BQ, true) ||
-      !encode_tmap_3d(&tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, kD, H, total_k, kD * 2, pitch,
-                      kD, 1, BKV, true) ||
-      !encode_tmap_3d(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, kD, H, total_k, kD * 2, pitch,
-                      kD, 1, BKV, true))
-    return cudaErrorInvalidValue;
-  auto kern = causal ? attn_fwd_bf16_kernel<true, false, true>
-                     : attn_fwd_bf16_kernel<true, false, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-  if (e != cudaSuccess) return e;
-  // items of very different cost (sequence lengths vary): one per CTA, so
-  // that the hardware's CTA scheduler balances them
-  const int nq = (max_q + BQ - 1) / BQ, n_bh = B * H;
-  const int grid = persistent_grid((int64_t)nq * n_bh, true);
-  if (grid <= 0) return cudaErrorInvalidValue;
-  const float c_log2 = scale * 1.4426950408889634f;
-  kern<<<grid, kThreads, kSmem, s>>>(tmQ, tmK, tmV, static_cast<__nv_bfloat16*>(O), max_q, 0,
-                                     c_log2, cu_q, cu_k, H, total_q, total_k, n_bh, nq, err);
-  return cudaGetLastError();
+  return launch_attn_prefill_tc_varlen(Q, K, V, O, cu_q, cu_k, B, H, max_q, total_q, total_k, scale,
+                                       causal, err, s);
 }
 
 }  // namespace rf

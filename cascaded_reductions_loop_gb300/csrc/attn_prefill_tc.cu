@@ -1,9 +1,12 @@
-// attn_prefill_tc.cu -- single-segment fused attention, fixed-length layout
-// [B][H][L][64], with or without the causal mask: the BERT-style prefill path
-// (bf16 in, fp32 accumulation and softmax state, bf16 out).  Under the causal
-// mask row i reads keys j <= i + Lk - Lq; each query tile reads only the key
-// tiles its last row needs, scores of keys a row does not read are set to
-// -inf (their P is 0), and a row that reads no key is written as zeros.
+// attn_prefill_tc.cu -- single-segment fused attention, single pass, bf16 in,
+// fp32 accumulation and softmax state, bf16 out: the BERT-style prefill path.
+// Two layouts: fixed-length [B][H][L][64], and packed variable-length
+// sequences [total][H][64] delimited by cumulative lengths (3-D tensor maps
+// over (dim, head, token); one CTA per item, since items differ in cost).
+// Under the causal mask row i reads keys j <= i + Lk - Lq of its sequence;
+// each query tile reads only the key tiles its last row needs, scores of keys
+// a row does not read are set to -inf (their P is 0), and a row that reads no
+// key is written as zeros.
 //
 // Safe-softmax cascade ([E] §2.2) in the single-loop incremental form ([E]
 // §2.3, §4.1; [S] Methodologie 2, single-segment strategy of Methodologie 3).
@@ -96,48 +99,111 @@ struct Bars {
 };
 
 // Item it = pair * n_bh + bh: query tiles 2 pair and 2 pair + 1 of (b, h) = bh.
+__host__ __device__ __forceinline__ int n_items_of(int n_bh, int nq) {
+  return n_bh * ((nq + 1) / 2);
+}
+
 struct Item {
-  int bh, qa;
-  bool has_b;
+  int bh, h;               // (batch or sequence, head); head (packed layout)
+  int qa;                  // query tile of a (tile b is qa + 1)
+  bool has_a, has_b;       // the tiles have rows (has_a: the item exists)
   int nkv_a, nkv_b, nkv;   // key tiles tile a / tile b read; key tiles loaded for the pair
+  int lq, lk;              // the sequence's query / key lengths
+  int q0, k0;              // fixed layout: rows bh * Lq / bh * Lk of the 2-D maps;
+                           // packed layout: the sequence's first query / key token
 };
 
-// Keys the last row of query tile qt may read (all Lk without the causal
-// mask; with it, keys j <= i + Lk - Lq of row i, clamped to 0..Lk), as a
+// Keys the last row of query tile qt may read (all lk without the causal
+// mask; with it, keys j <= i + lk - lq of row i, clamped to 0..lk), as a
 // count of 128-key tiles, at least one: a tile whose rows read no key still
 // runs one fully masked key tile and writes zeros.
-__device__ __forceinline__ int tiles_of(int qt, int Lq, int Lk, bool causal) {
-  int end = Lk;
-  if (causal) end = max(0, min(Lk, min((qt + 1) * BQ, Lq) + (Lk - Lq)));
+__device__ __forceinline__ int tiles_of(int qt, int lq, int lk, bool causal) {
+  int end = lk;
+  if (causal) end = max(0, min(lk, min((qt + 1) * BQ, lq) + (lk - lq)));
   return max(1, (end + BKV - 1) / BKV);
 }
 
-__device__ __forceinline__ Item item_of(int it, int n_bh, int nq, int Lq, int Lk, bool causal) {
+// Item it: pair p = it / n_bh of query tiles (2p, 2p + 1) of (batch, head)
+// bh = it % n_bh.  Fixed layout [B*H][L][64]: every item exists.  Packed
+// layout (tokens [total][H][64], sequence b = bh / H owns query tokens
+// cu_q[b] .. cu_q[b + 1] - 1 and key tokens cu_k[b] ..): an item whose first
+// tile lies past its sequence does not exist; lengths that contradict the
+// host-side totals are reported and the sequence skipped; with the causal
+// mask the heaviest pairs come first (one CTA per item, started in order).
+template <bool kCausal, bool kVarlen>
+__device__ __forceinline__ Item item_of(int it, int n_bh, int nq, int Lq, int Lk, const int* cu_q,
+                                        const int* cu_k, int H, int total_q, int total_k,
+                                        unsigned* err) {
   Item w;
+  const int npairs = (nq + 1) / 2;
+  int p = it / n_bh;
   w.bh = it % n_bh;
-  w.qa = 2 * (it / n_bh);
-  w.has_b = w.qa + 1 < nq;
-  w.nkv_a = tiles_of(w.qa, Lq, Lk, causal);
-  w.nkv_b = w.has_b ? tiles_of(w.qa + 1, Lq, Lk, causal) : 0;
+  if (kCausal && kVarlen) p = npairs - 1 - p;
+  w.qa = 2 * p;
+  bool ok = it < n_items_of(n_bh, nq);
+  if (!kVarlen) {
+    w.h = 0;
+    w.lq = Lq;
+    w.lk = Lk;
+    w.q0 = w.bh * Lq;
+    w.k0 = w.bh * Lk;
+  } else {
+    const int b = w.bh / H;
+    w.h = w.bh % H;
+    const bool cu_ok = ok && RF_IN(err, b + 1, n_bh / H + 1);   // cu_q, cu_k have B + 1 entries
+    const int a0 = cu_ok ? cu_q[b] : 0, a1 = cu_ok ? cu_q[b + 1] : 0;
+    const int c0 = cu_ok ? cu_k[b] : 0, c1 = cu_ok ? cu_k[b + 1] : 0;
+    const bool len_ok = cu_ok && 0 <= a0 && a0 <= a1 && a1 <= total_q && a1 - a0 <= Lq &&
+                        0 <= c0 && c0 <= c1 && c1 <= total_k;
+    if (cu_ok && !len_ok && p == 0 && threadIdx.x == 0) raise_error(err, kDevErrInput);
+    ok = len_ok;
+    w.lq = ok ? a1 - a0 : 0;
+    w.lk = ok ? c1 - c0 : 0;
+    w.q0 = a0;
+    w.k0 = c0;
+  }
+  w.has_a = ok && w.qa * BQ < w.lq;
+  w.has_b = ok && (w.qa + 1) * BQ < w.lq;
+  w.nkv_a = w.has_a ? tiles_of(w.qa, w.lq, w.lk, kCausal) : 0;
+  w.nkv_b = w.has_b ? tiles_of((w.qa + 1), w.lq, w.lk, kCausal) : 0;
   w.nkv = max(w.nkv_a, w.nkv_b);
   return w;
 }
 
-template <bool kCausal>
+// Fixed layout: tmQ/tmK/tmV are 2-D maps over rows [B*H*L][64] and tmO a
+// 3-D map [B*H][Lq][64].  Packed layout: all four are 3-D maps
+// [total][H][64]; Lq is the longest sequence (max_q) and Lk unused.
+template <bool kCausal, bool kVarlen>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap tmQ,
                         const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV,
-                        const __grid_constant__ CUtensorMap tmO, int Lq, int Lk, float c_log2,
-                        int n_bh, int nq, unsigned* err) {
+                        const __grid_constant__ CUtensorMap tmO, __nv_bfloat16* __restrict__ O,
+                        int Lq, int Lk, float c_log2, int n_bh, int nq, const int* __restrict__ cu_q,
+                        const int* __restrict__ cu_k, int H, int total_q, int total_k,
+                        unsigned* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + kBarOff);
   volatile int* abort_flag = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_items = n_bh * ((nq + 1) / 2);
-  constexpr bool causal = kCausal;
+  const int n_items = n_items_of(n_bh, nq);
+  auto item = [&](int it) {
+    return item_of<kCausal, kVarlen>(it, n_bh, nq, Lq, Lk, cu_q, cu_k, H, total_q, total_k, err);
+  };
+  // the next item of this CTA from `it` on that has rows (n_items if none)
+  auto next_item = [&](int it) {
+    while (it < n_items && !item(it).has_a) it += gridDim.x;
+    return it;
+  };
+  // TMA loads of 128 rows (query tile or key tile) of head h starting at
+  // row / token r0 of the map
+  auto load_rows = [&](uint32_t dst, const CUtensorMap* m, uint32_t bar, int h, int r0,
+                       uint64_t pol) {
+    if (kVarlen) tma_load_3d_hint(dst, m, bar, 0, h, r0, pol);
+    else tma_load_2d_hint(dst, m, bar, 0, r0, pol);
+  };
 
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmQ);
@@ -180,10 +246,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // ------------------------------------------------ TMA producer
       const uint64_t pol_kv = policy_evict_last();   // K/V are read by every pair of the head
+      const uint64_t pol_q = policy_evict_first();   // each Q tile is read once
       bool ok = true;
       int ni = 0, g = 0;                             // items and K/V tiles issued
-      for (int it = blockIdx.x; ok && it < n_items && !*abort_flag; it += gridDim.x, ++ni) {
-        const Item w = item_of(it, n_bh, nq, Lq, Lk, causal);
+      for (int it = next_item(blockIdx.x); ok && it < n_items && !*abort_flag;
+           it = next_item(it + gridDim.x), ++ni) {
+        const Item w = item(it);
         const int slot = ni & 1;
         if (ni >= 2 &&
             !mbar_wait(smem_u32(&bars->q_empty[slot]), (uint32_t)(((ni >> 1) - 1) & 1))) {
@@ -192,10 +260,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t qb = smem_u32(&bars->q_full[slot]);
         mbar_arrive_expect_tx(qb, (w.has_b ? 2 : 1) * kTile);
-        const int q_row = w.bh * Lq + w.qa * BQ;
-        tma_load_2d(smem_u32(smem + kQOff + (2 * slot) * kTile), &tmQ, qb, 0, q_row);
-        if (w.has_b) tma_load_2d(smem_u32(smem + kQOff + (2 * slot + 1) * kTile), &tmQ, qb, 0, q_row + BQ);
-        const int kv_row = w.bh * Lk;
+        load_rows(smem_u32(smem + kQOff + (2 * slot) * kTile), &tmQ, qb, w.h, w.q0 + w.qa * BQ,
+                  pol_q);
+        if (w.has_b)
+          load_rows(smem_u32(smem + kQOff + (2 * slot + 1) * kTile), &tmQ, qb, w.h,
+                    w.q0 + (w.qa + 1) * BQ, pol_q);
         for (int j = 0; j < w.nkv; ++j, ++g) {
           const int st = g % kStages;
           const uint32_t ph = (uint32_t)(((g / kStages) + 1) & 1);
@@ -204,15 +273,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(smem_u32(&bars->k_full[st]), kTile);
-          tma_load_2d_hint(smem_u32(smem + kKOff + st * kTile), &tmK, smem_u32(&bars->k_full[st]), 0,
-                           kv_row + j * BKV, pol_kv);
+          load_rows(smem_u32(smem + kKOff + st * kTile), &tmK, smem_u32(&bars->k_full[st]), w.h,
+                    w.k0 + j * BKV, pol_kv);
           if (g >= kStages && !mbar_wait(smem_u32(&bars->v_empty[st]), ph)) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(smem_u32(&bars->v_full[st]), kTile);
-          tma_load_2d_hint(smem_u32(smem + kVOff + st * kTile), &tmV, smem_u32(&bars->v_full[st]), 0,
-                           kv_row + j * BKV, pol_kv);
+          load_rows(smem_u32(smem + kVOff + st * kTile), &tmV, smem_u32(&bars->v_full[st]), w.h,
+                    w.k0 + j * BKV, pol_kv);
         }
       }
       if (!ok || *abort_flag) {
@@ -274,8 +343,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       int ni = 0, g = 0;
-      int it = blockIdx.x;
-      Item w = item_of(it, n_bh, nq, Lq, Lk, causal);
+      int it = next_item(blockIdx.x);
+      Item w = item(it);
       if (it < n_items) {
         ok = mbar_wait(smem_u32(&bars->q_full[0]), 0) && wait_kv(bars->k_full, 0);
         // tile b starts once tile a's softmax has taken its first row maxima,
@@ -286,10 +355,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && (x == 0 || w.has_b)) ok = issue_s(0, 0);
         if (ok) mma_commit(smem_u32(&bars->k_empty[0]));
       }
-      for (; ok && it < n_items; it += gridDim.x, ++ni) {
+      for (; ok && it < n_items; ++ni) {
         const int qs = ni & 1;
-        const int it_next = it + gridDim.x;
-        const Item wn = item_of(it_next, n_bh, nq, Lq, Lk, causal);
+        const int it_next = next_item(it + gridDim.x);
+        const bool next_has_b = it_next < n_items && item(it_next).has_b;
         // key tiles this query tile reads (0 for a missing tile b); the
         // pair's loaded tiles may run past them under the causal mask
         const int nkv_x = x == 0 ? w.nkv_a : w.nkv_b;
@@ -299,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // next tile: the same item's, or the next item's first
           const bool has_next = !last || it_next < n_items;
           const int qs_next = last ? qs ^ 1 : qs;
-          const bool next_mine = last ? (x == 0 || wn.has_b) : j + 1 < nkv_x;
+          const bool next_mine = last ? (x == 0 || next_has_b) : j + 1 < nkv_x;
           // the next S, as soon as the softmax warps have read the current
           // one (their exponentials then overlap this product)
           auto next_s = [&]() -> bool {
@@ -330,7 +399,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // possible (the softmax warps store O before they read the next S)
           ok = last ? (this_pv() && next_s()) : (next_s() && this_pv());
         }
-        w = wn;
+        it = it_next;
+        w = item(it);
       }
       if (!ok) {
         raise_error(err, kDevErrTimeout);
@@ -354,13 +424,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t c2 = f2(c_log2, c_log2);
     bool ok = true;
     int cnt = 0, icnt = 0;                             // tiles and items of this warpgroup
+    int ns = 0;                                        // of those, O tiles written by bulk store
     for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-      const Item w = item_of(it, n_bh, nq, Lq, Lk, causal);
-      if (x == 1 && !w.has_b) continue;
+      const Item w = item(it);
+      if (!w.has_a || (x == 1 && !w.has_b)) continue;
       const int nkv_x = x == 0 ? w.nkv_a : w.nkv_b;
-      // keys this row reads: all Lk, or under the causal mask j <= i + Lk - Lq
+      const int row0 = (w.qa + x) * BQ;                   // first row of this query tile
+      // keys this row reads: all lk, or under the causal mask j <= i + lk - lq
       const int kv_row =
-          causal ? max(0, min(Lk, (w.qa + x) * BQ + r + (Lk - Lq) + 1)) : Lk;
+          kCausal ? max(0, min(w.lk, row0 + r + (w.lk - w.lq) + 1)) : w.lk;
       float m_ref = -INFINITY, l_run = 0.f;
       for (int j = 0; j < nkv_x; ++j, ++cnt) {
         // warp-uniform decision: the TMEM loads below are warp-collective
@@ -485,17 +557,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
         break;
       }
-      const int e = icnt++;                              // items of this warpgroup so far
+      ++icnt;
       tc_fence_after();
       uint32_t v[2][32];
       tmem_ld32(o_addr, v[0]);
       tmem_ld32(o_addr + 32, v[1]);
       tmem_ld_wait();
       tc_fence_before();                               // O read before the next P.V may overwrite it
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;   // a row that read no key: zeros
+      auto out8 = [&](int c) {                         // 16-byte chunk c of the row's bf16 O
+        const uint32_t* u = &v[c >> 2][(c & 3) * 8];
+        return make_uint4(pack_bf16x2(__uint_as_float(u[0]) * inv, __uint_as_float(u[1]) * inv),
+                          pack_bf16x2(__uint_as_float(u[2]) * inv, __uint_as_float(u[3]) * inv),
+                          pack_bf16x2(__uint_as_float(u[4]) * inv, __uint_as_float(u[5]) * inv),
+                          pack_bf16x2(__uint_as_float(u[6]) * inv, __uint_as_float(u[7]) * inv));
+      };
+      if (kVarlen && row0 + BQ > w.lq) {
+        // the sequence's last, partial tile: a bulk store would run into the
+        // next sequence's rows, so each thread stores its own row
+        const int row = row0 + r;
+        const int64_t o_first = ((int64_t)(w.q0 + row) * H + w.h) * kD;
+        if (row < w.lq && RF_IN(err, o_first + kD - 1, (int64_t)total_q * H * kD)) {
+          uint4* dst = reinterpret_cast<uint4*>(O + o_first);
+#pragma unroll
+          for (int c = 0; c < kD / 8; ++c) dst[c] = out8(c);
+        }
+        continue;
+      }
       // O_x / l as bf16, staged in shared memory as 128-byte swizzled rows
-      // and written by one bulk tensor store per tile (rows past Lq are
-      // outside the tensor map and are not written).  The staging tile is
-      // reused once the previous store has read it.
+      // and written by one bulk tensor store per tile (fixed layout: rows
+      // past Lq are outside the tensor map and are not written).  The
+      // staging tile is reused once the previous store has read it.
+      const int e = ns++;
       const bool issuer = sub == 0 && lane == 0;
       if (e > 0) {
         if (issuer) {
@@ -508,25 +601,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       uint8_t* st = smem + kStOff + x * kTile + r * 128;
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;   // a row that read no key: zeros
 #pragma unroll
-      for (int c = 0; c < kD / 8; ++c) {
-        const uint32_t* u = &v[c >> 2][(c & 3) * 8];
-        *reinterpret_cast<uint4*>(st + ((c ^ (r & 7)) << 4)) = make_uint4(
-            pack_bf16x2(__uint_as_float(u[0]) * inv, __uint_as_float(u[1]) * inv),
-            pack_bf16x2(__uint_as_float(u[2]) * inv, __uint_as_float(u[3]) * inv),
-            pack_bf16x2(__uint_as_float(u[4]) * inv, __uint_as_float(u[5]) * inv),
-            pack_bf16x2(__uint_as_float(u[6]) * inv, __uint_as_float(u[7]) * inv));
-      }
+      for (int c = 0; c < kD / 8; ++c) *reinterpret_cast<uint4*>(st + ((c ^ (r & 7)) << 4)) = out8(c);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->st_full[x]));
       bool st_ok = true;
       if (issuer) {
-        st_ok = mbar_wait(smem_u32(&bars->st_full[x]), (uint32_t)(e & 1)) &&
-                RF_IN(err, w.bh, n_bh) && RF_IN(err, (w.qa + x) * BQ, Lq);
+        st_ok = mbar_wait(smem_u32(&bars->st_full[x]), (uint32_t)(e & 1)) && RF_IN(err, w.bh, n_bh) &&
+                RF_IN(err, row0, Lq);
         if (st_ok) {
-          tma_store_3d(&tmO, smem_u32(smem + kStOff + x * kTile), 0, (w.qa + x) * BQ, w.bh);
+          const uint32_t src = smem_u32(smem + kStOff + x * kTile);
+          if (kVarlen) tma_store_3d(&tmO, src, 0, w.h, w.q0 + row0);
+          else tma_store_3d(&tmO, src, 0, row0, w.bh);
           bulk_commit_group();
         }
       }
@@ -536,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // every bulk store of this warpgroup has completed before the CTA exits
-    if (sub == 0 && lane == 0 && icnt > 0) bulk_wait_group0();
+    if (sub == 0 && lane == 0 && ns > 0) bulk_wait_group0();
     if (!ok) {
       raise_error(err, kDevErrTimeout);
       *abort_flag = 1;
@@ -565,7 +652,7 @@ cudaError_t launch_attn_prefill_tc(const void* Q, const void* K, const void* V, 
       !encode_tmap_2d(&tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, kD, kv_rows, kD * 2, kD, BKV, true) ||
       !encode_tmap_2d(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, kD, kv_rows, kD * 2, kD, BKV, true))
     return cudaErrorInvalidValue;
-  auto kern = causal ? attn_prefill_kernel<true> : attn_prefill_kernel<false>;
+  auto kern = causal ? attn_prefill_kernel<true, false> : attn_prefill_kernel<false, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   const int nq = (Lq + BQ - 1) / BQ, n_bh = B * H;
@@ -576,7 +663,40 @@ cudaError_t launch_attn_prefill_tc(const void* Q, const void* K, const void* V, 
   const int64_t per_cta = (items + sms - 1) / sms;
   const int grid = (int)((items + per_cta - 1) / per_cta);
   const float c_log2 = scale * 1.4426950408889634f;
-  kern<<<grid, kThreads, kSmem, s>>>(tmQ, tmK, tmV, tmO, Lq, Lk, c_log2, n_bh, nq, err);
+  kern<<<grid, kThreads, kSmem, s>>>(tmQ, tmK, tmV, tmO, static_cast<__nv_bfloat16*>(O), Lq, Lk,
+                                     c_log2, n_bh, nq, nullptr, nullptr, H, 0, 0, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_prefill_tc_varlen(const void* Q, const void* K, const void* V, void* O,
+                                          const int* cu_q, const int* cu_k, int B, int H,
+                                          int max_q, int total_q, int total_k, float scale,
+                                          int causal, unsigned* err, cudaStream_t s) {
+  // [total][H][64] tokens: one head's 128 consecutive tokens are a box of
+  // 64 x 1 x 128 (coordinates: dim, head, token)
+  CUtensorMap tmQ, tmK, tmV, tmO;
+  const uint64_t pitch = (uint64_t)H * kD * 2;     // bytes between tokens
+  if (!encode_tmap_3d(&tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Q, kD, H, total_q, kD * 2, pitch,
+                      kD, 1, BQ, true) ||
+      !encode_tmap_3d(&tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, kD, H, total_k, kD * 2, pitch,
+                      kD, 1, BKV, true) ||
+      !encode_tmap_3d(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, kD, H, total_k, kD * 2, pitch,
+                      kD, 1, BKV, true) ||
+      !encode_tmap_3d(&tmO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, O, kD, H, total_q, kD * 2, pitch,
+                      kD, 1, BQ, true))
+    return cudaErrorInvalidValue;
+  auto kern = causal ? attn_prefill_kernel<true, true> : attn_prefill_kernel<false, true>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  const int nq = (max_q + BQ - 1) / BQ, n_bh = B * H;
+  const int64_t items = (int64_t)n_items_of(n_bh, nq);
+  if (items <= 0 || items >= (1ll << 31)) return cudaErrorInvalidValue;
+  // items of very different cost (sequence lengths vary, and pairs past a
+  // short sequence are empty): one CTA per item, so that the hardware's CTA
+  // scheduler balances them
+  const float c_log2 = scale * 1.4426950408889634f;
+  kern<<<(int)items, kThreads, kSmem, s>>>(tmQ, tmK, tmV, tmO, static_cast<__nv_bfloat16*>(O), max_q,
+                                           0, c_log2, n_bh, nq, cu_q, cu_k, H, total_q, total_k, err);
   return cudaGetLastError();
 }
 

@@ -52,6 +52,10 @@ cudaError_t launch_attn_fwd_bf16_tc(const void* Q, const void* K, const void* V,
 cudaError_t launch_attn_prefill_tc(const void* Q, const void* K, const void* V, void* O, int B,
                                    int H, int Lq, int Lk, float scale, int causal, unsigned* err,
                                    cudaStream_t s);
+cudaError_t launch_attn_prefill_tc_varlen(const void* Q, const void* K, const void* V, void* O,
+                                          const int* cu_q, const int* cu_k, int B, int H,
+                                          int max_q, int total_q, int total_k, float scale,
+                                          int causal, unsigned* err, cudaStream_t s);
 
 // Packed variable-length layout: Q/O [total_q][H][d], K/V [total_k][H][d],
 // sequence b = tokens cu_q[b] .. cu_q[b+1]-1 (device arrays of B + 1 int32).
