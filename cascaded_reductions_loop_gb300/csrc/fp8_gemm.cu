@@ -431,6 +431,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int sub = warp & 3;                    // TMEM lane quarter of this warp
     const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
     const bool vec_ok = (N % 8) == 0;
+    // 32-byte stores (whole L2 sectors) when every chunk start is 32-byte aligned
+    const bool v8_ok = (N % 16) == 0 && (reinterpret_cast<uintptr_t>(Y) & 31) == 0;
     for (int i = 0; i < my_tiles; ++i) {
       const int a = i & 1;
       const Tile w = tile_of(cid + i * ncl, tiles_n, n_full);
@@ -475,7 +477,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                   __uint_as_float(r[2 * j + 1]) * srow * swv[2 * j + 1]);
         if (row_in) {
           __nv_bfloat16* yp = Y + (size_t)row * N + n0 + c0;
-          if (vec_ok && full_chunk) {
+          if (v8_ok && full_chunk) {
+#pragma unroll
+            for (int q = 0; q < 2; ++q)
+              st_global_v8(yp + 16 * q, &packed[8 * q]);
+          } else if (vec_ok && full_chunk) {
             uint4* y4 = reinterpret_cast<uint4*>(yp);
 #pragma unroll
             for (int q = 0; q < 4; ++q)

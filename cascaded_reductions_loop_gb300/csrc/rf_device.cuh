@@ -207,6 +207,14 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
+// One 32-byte store (a whole L2 sector) of eight 32-bit words; the address
+// is 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy reads (tensor core operands written by threads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
