@@ -111,19 +111,22 @@ class Guarded:
     and behind it.  ``check()`` asserts that the kernel wrote nothing outside
     the tensor (the out-of-bounds-write detector of the ragged parity cases)."""
 
-    def __init__(self, shape, dtype, fill=None):
+    def __init__(self, shape, dtype, fill=None, shift=0):
+        """shift: extra bytes before the tensor (e.g. 16 for a start that is
+        16-byte but not 32-byte aligned)."""
         n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
         self.n = n
-        self.raw = torch.full((GUARD_FRONT + n + GUARD_BACK,), GUARD_BYTE, dtype=torch.uint8,
+        self.front = GUARD_FRONT + shift
+        self.raw = torch.full((self.front + n + GUARD_BACK,), GUARD_BYTE, dtype=torch.uint8,
                               device="cuda")
-        self.t = self.raw[GUARD_FRONT:GUARD_FRONT + n].view(dtype).view(shape)
+        self.t = self.raw[self.front:self.front + n].view(dtype).view(shape)
         if fill is None:
             fill = float("nan") if dtype.is_floating_point else 0x7F
         self.t.fill_(fill)
 
     def check(self, what=""):
-        front = self.raw[:GUARD_FRONT]
-        back = self.raw[GUARD_FRONT + self.n:]
+        front = self.raw[:self.front]
+        back = self.raw[self.front + self.n:]
         bad_f = int((front != GUARD_BYTE).sum().item())
         bad_b = int((back != GUARD_BYTE).sum().item())
         assert bad_f == 0 and bad_b == 0, \

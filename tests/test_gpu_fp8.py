@@ -32,12 +32,13 @@ def _weights(rf, w):
     return wq_d, sw_d, wq_o, sw_o
 
 
-def _run(rf, x, wq, sw, with_outputs=True):
+def _run(rf, x, wq, sw, with_outputs=True, y_shift=0):
     """Runs the fused call with guard bytes around every output; returns
-    (Y, sx, xq) on the host (sx, xq None when kept in the workspace)."""
+    (Y, sx, xq) on the host (sx, xq None when kept in the workspace).  Y
+    starts y_shift bytes past a 256-byte boundary."""
     M, K = x.shape
     N = wq.shape[0]
-    y = Guarded((M, N), torch.bfloat16)
+    y = Guarded((M, N), torch.bfloat16, shift=y_shift)
     sx = Guarded((M,), torch.float32) if with_outputs else None
     xq = Guarded((M, K), torch.uint8) if with_outputs else None
     need = rf.rf_absmax_fp8_gemm_workspace_size(M, N, K)
@@ -179,3 +180,14 @@ def test_quantisation_exhaustive_against_ieee_division(rf, fused):
         assert bad.numel() == 0, f"{bad.shape[0]} codes differ, first (row, col) {bad[:3].tolist()}"
         total += M * 4095
     assert total > 1_000_000_000
+
+
+def test_fp8_y_16_byte_aligned(rf):
+    """Y 16-byte but not 32-byte aligned: the epilogue stores 16-byte pieces
+    instead of 32-byte ones; the bits are the same."""
+    x, w = I.fp8_inputs(I.FP8Shape(M=300, N=512, K=256, seed=42))
+    wq_d, sw_d, wq_o, sw_o = _weights(rf, w)
+    y16, sx, xq = _run(rf, x, wq_d, sw_d, y_shift=16)
+    y32, _, _ = _run(rf, x, wq_d, sw_d)
+    _check_all(x, y16, sx, xq, wq_o, sw_o, "FP8 Y at a 16-byte offset")
+    assert torch.equal(y16, y32)

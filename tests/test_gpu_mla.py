@@ -18,14 +18,15 @@ def rf():
     return m
 
 
-def _run(rf, q, ckv, scale, num_splits=0):
-    """One call with guard bytes around the output and the workspace."""
+def _run(rf, q, ckv, scale, num_splits=0, shift=0):
+    """One call with guard bytes around the output and the workspace (both
+    starting `shift` bytes past a 256-byte boundary)."""
     B, Hq, _ = q.shape
     Lk = ckv.shape[1]
     qd, cd = q.cuda(), ckv.cuda()
-    o = Guarded((B, Hq, 512), torch.bfloat16)
+    o = Guarded((B, Hq, 512), torch.bfloat16, shift=shift)
     nbytes = rf.rf_mla_decode_workspace_size(B, Hq, Lk, 576, 512, num_splits)
-    ws = Guarded((nbytes,), torch.uint8, fill=0xFF) if nbytes else None
+    ws = Guarded((nbytes,), torch.uint8, fill=0xFF, shift=shift) if nbytes else None
     rf.rf_mla_decode(qd, cd, o.t, scale, None if ws is None else ws.t, num_splits)
     assert rf.rf_get_device_status() == rf.RF_OK
     o.check("mla output")
@@ -101,3 +102,16 @@ def test_mla_repeatable(rf):
     outs = [_run(rf, q, c, sh.scale, sp) for sp in (2, 2, 2)]
     for o in outs[1:]:
         assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+def test_mla_outputs_16_byte_aligned(rf, splits):
+    """O and the workspace 16-byte but not 32-byte aligned (the documented
+    minimum alignment): the result is the same as with aligned buffers."""
+    sh = I.MLAShape(2, 128, 300, seed=41)
+    q, c = I.mla_inputs(sh)
+    ref = A.mla_decode(q, c, sh.scale, 512)
+    o16 = _run(rf, q, c, sh.scale, splits, shift=16)
+    o32 = _run(rf, q, c, sh.scale, splits)
+    assert_bf16_close(o16, ref, "mla, 16-byte aligned outputs")
+    assert torch.equal(o16, o32)
