@@ -42,13 +42,17 @@ cudaError_t launch_attn_fwd_f32(const float* Q, const float* K, const float* V, 
                                 int H, int Lq, int Lk, int d, float scale, int causal,
                                 unsigned* err, cudaStream_t s);
 
-// two_pass = 1: non-incremental form (requires Lk <= 256).
-cudaError_t launch_attn_fwd_bf16_tc(const void* Q, const void* K, const void* V, void* O, int B,
-                                    int H, int Lq, int Lk, int d, float scale, int causal,
-                                    int two_pass, unsigned* err, cudaStream_t s);
+// bf16, d = 64, the non-incremental (two-pass) form: Lk <= 256, one CTA per
+// 128 query rows.
+cudaError_t launch_attn_two_pass_tc(const void* Q, const void* K, const void* V, void* O, int B,
+                                    int H, int Lq, int Lk, float scale, int causal, unsigned* err,
+                                    cudaStream_t s);
 
-// Fixed-length, unmasked, incremental: two query tiles per CTA in ping-pong,
-// P and O in tensor memory (the BERT-style prefill path).
+// bf16, d = 64, the incremental single-pass form (the BERT-style prefill
+// path): two query tiles per CTA, one MMA-issuing thread each, P and O in
+// tensor memory; fixed-length [B][H][L][64] or packed variable-length
+// [total][H][64] (sequence b = tokens cu_q[b] .. cu_q[b+1]-1, device arrays
+// of B + 1 int32), with or without the causal mask.
 cudaError_t launch_attn_prefill_tc(const void* Q, const void* K, const void* V, void* O, int B,
                                    int H, int Lq, int Lk, float scale, int causal, unsigned* err,
                                    cudaStream_t s);
@@ -63,10 +67,6 @@ cudaError_t launch_attn_fwd_f32_varlen(const float* Q, const float* K, const flo
                                        const int* cu_q, const int* cu_k, int B, int H,
                                        int max_q, int total_q, int total_k, int d, float scale,
                                        int causal, unsigned* err, cudaStream_t s);
-cudaError_t launch_attn_fwd_bf16_tc_varlen(const void* Q, const void* K, const void* V, void* O,
-                                           const int* cu_q, const int* cu_k, int B, int H,
-                                           int max_q, int total_q, int total_k, float scale,
-                                           int causal, unsigned* err, cudaStream_t s);
 
 int decode_num_splits(int B, int Hq, int Hkv, int Lk, int d, int requested);
 size_t decode_workspace_bytes(int B, int Hq, int Hkv, int Lk, int d, int requested);
