@@ -278,11 +278,11 @@ __device__ __forceinline__ bool wait_rows_ready(const unsigned* ready, int m0, i
   return true;
 }
 
-// Persistent: 2-CTA clusters, one CTA per SM, 320 threads.
-//   warp 0     TMA producer (both CTAs)
-//   warp 1     TMEM allocation (both CTAs); MMA issuer (rank 0, one thread)
-//   warps 2-5  epilogue (TMEM lane quarter = warp % 4)
-//   warps 6-9  quantisers
+// Persistent: 2-CTA clusters, one CTA per SM, 448 threads.
+//   warp 0      TMA producer (both CTAs)
+//   warp 1      TMEM allocation (both CTAs); MMA issuer (rank 0, one thread)
+//   warps 2-5   epilogue (TMEM lane quarter = warp % 4)
+//   warps 6-13  quantisers
 // Tile t (tile_of) covers output rows m0 .. m0 + 255 (CTA r: + 128 r) and
 // columns n0 .. n0 + ncols - 1 (CTA r loads B rows n0 + r ncols / 2 ..,
 // through tmB for full tiles and tmBh, with boxes of 64 rows, for halves);
