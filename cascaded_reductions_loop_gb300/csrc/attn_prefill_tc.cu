@@ -26,17 +26,20 @@
 //                                               tensor-memory A operand, V the
 //                                               MN-major shared-memory B operand)
 // After the last key tile the warpgroup reads O_x from tensor memory, stages
-// O_x / l as bf16 in shared memory and writes it with one bulk tensor store.
-// S, P and O never leave the SM.
+// O_x / l as bf16 in shared memory and writes it with one bulk tensor store
+// (a packed sequence's partial last tile: each thread stores its own row,
+// since the box would run into the next sequence).  S, P and O never leave
+// the SM.
 //
 // Each query tile has an MMA-issuing thread of its own, so one tile's
 // products never wait behind the other tile's softmax; within a tile the
 // next S is issued as soon as the current one has been read, the P.V as soon
 // as P is written (at a pair's last key tile the P.V first, so O is complete
 // early).  Tile b starts once tile a's softmax has taken its first row
-// maxima, so the two softmax warpgroups run out of phase.  Any reference m gives the same result ([S] Methodologie 1: the
-// dependent factor 2^-m is invertible); with m at least the true running max
-// minus kLazy, every P is at most 2^kLazy.
+// maxima, so the two softmax warpgroups run out of phase.  Any reference m
+// gives the same result ([S] Methodologie 1: the dependent factor 2^-m is
+// invertible); with m at least the true running max minus kLazy, every P is
+// at most 2^kLazy.
 //
 // A TMA warp loads the pair's Q tiles (two slots, so the next item's Q lands
 // while the current one runs) and streams K and V tiles through kStages-deep
