@@ -26,7 +26,7 @@ __all__ = [
     "RF_DECODE_NOALLOC_SCRATCH_BYTES", "rf_mla_decode", "rf_mla_decode_num_splits",
     "rf_mla_decode_workspace_size", "rf_moe_gate_topk_softmax", "rf_moe_gate_topk_softmax_ex",
     "rf_absmax_fp8_gemm", "rf_absmax_fp8_gemm_workspace_size", "rf_absmax_quant_fp8",
-    "rf_selftest_wait_timeout", "rf_selftest_bounds",
+    "rf_selftest_wait_timeout", "rf_selftest_bounds", "rf_selftest_decode_plan",
     "RF_OK", "RF_ERR_INVALID_ARG", "RF_ERR_UNSUPPORTED", "RF_ERR_WORKSPACE", "RF_ERR_CUDA",
     "RF_ERR_DEVICE_TIMEOUT", "RF_ERR_DEVICE_INPUT", "RF_ERR_DEVICE_LAYOUT", "RF_ERR_DEVICE_BOUNDS",
     "RF_F32", "RF_BF16",
@@ -78,6 +78,7 @@ _SIGS = {
     "rf_absmax_quant_fp8": (_I, [_P, _I, _I, _P, _P, _P]),
     "rf_selftest_wait_timeout": (_I, [_I, _P]),
     "rf_selftest_bounds": (_I, [_P]),
+    "rf_selftest_decode_plan": (_I, [_I, _I, _I, _I, _I]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -347,3 +348,10 @@ def rf_selftest_bounds(stream=None) -> int:
     RF_ERR_DEVICE_BOUNDS by rf_get_device_status, the access never made);
     returns the call's status (RF_ERR_UNSUPPORTED in the normal build)."""
     return lib.rf_selftest_bounds(_stream(stream))
+
+
+def rf_selftest_decode_plan(B: int, Hkv: int, Lk: int, num_splits: int, sms: int) -> int:
+    """Host-side check of the split-KV decode partition (no GPU needed):
+    0 when it is consistent, -1 for a refused shape, else the number of the
+    first failed check (see include/rf.h)."""
+    return lib.rf_selftest_decode_plan(int(B), int(Hkv), int(Lk), int(num_splits), int(sms))

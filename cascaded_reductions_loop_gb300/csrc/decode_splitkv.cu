@@ -46,7 +46,9 @@
 // boxes each).  The partial states are a few hundred KB, read back from L2.
 #include <math.h>
 
+#include <algorithm>
 #include <mutex>
+#include <vector>
 
 #include "rf_device.cuh"
 #include "rf_internal.h"
@@ -96,7 +98,7 @@ __host__ __device__ inline void plan_init(DecodePlan* pl, int P, int Lk, int S, 
   pl->P = P;
   pl->Lk = Lk;
   pl->S = S;
-  pl->nck = (uint32_t)((Lk + kCK - 1) / kCK);
+  pl->nck = (uint32_t)(((int64_t)Lk + kCK - 1) / kCK);   // Lk up to 2^31 - 1
   pl->T = (uint32_t)P * pl->nck;
   const int64_t units = S > 0 ? (int64_t)P * S : (int64_t)pl->T;
   pl->grid = (int)(units < sms ? units : sms);
@@ -143,10 +145,10 @@ __host__ __device__ __forceinline__ DecodePiece plan_piece(const DecodePlan& pl,
   const uint32_t p = r0 / pl.nck + (uint32_t)k;
   const uint32_t s0 = p * pl.nck, s1 = s0 + pl.nck;
   const uint32_t a = (r0 > s0 ? r0 : s0) - s0, b = (r1 < s1 ? r1 : s1) - s0;
-  const int hi = (int)(b * kCK);
+  const uint32_t hi = b * kCK;                      // up to 2^31: unsigned
   pc.p = (int)p;
   pc.lo = (int)(a * kCK);
-  pc.hi = hi < pl.Lk ? hi : pl.Lk;
+  pc.hi = hi < (uint32_t)pl.Lk ? (int)hi : pl.Lk;
   pc.slot = 2 * c + (k == 0 ? 0 : 1);
   // a piece strictly inside the range is a whole sequence
   pc.npieces = (s0 >= r0 && s1 <= r1) ? 1 : plan_owner(pl, s1 - 1) - plan_owner(pl, s0) + 1;
@@ -204,7 +206,7 @@ __device__ __forceinline__ uint32_t sw_off(int r, int c) {
 }
 
 __device__ __forceinline__ int piece_chunks(const DecodePiece& pc) {
-  return (pc.hi - pc.lo + kCK - 1) / kCK;
+  return (int)(((int64_t)pc.hi - pc.lo + kCK - 1) / kCK);
 }
 
 // Adds state (m, l, o) into the running merge (M, L, O) whose reference is
@@ -631,6 +633,65 @@ size_t ws_o_bytes(const DecodePlan& pl, int G) {
 }
 
 }  // namespace
+
+// Host-side check of the partition the kernel follows (the plan_* functions
+// above, shared by host and device), for P = B * Hkv sequences of Lk keys,
+// S explicit segments (0 = automatic) and a grid of at most `sms` CTAs.
+// Returns 0 when every invariant holds, -1 for a shape the decode call
+// refuses, else the number of the first invariant that fails:
+//   1 every CTA has at least one piece;
+//   2 plan_order visits each of a CTA's pieces once;
+//   3 every piece is a non-empty key range [lo, hi) of a sequence;
+//   4 pieces of split sequences have distinct workspace slots in range;
+//   5 the pieces of each sequence tile [0, Lk) with no gap or overlap;
+//   6 every piece knows how many pieces its sequence has;
+//   7 plan_slot lists a split sequence's slots in key order, which is the
+//     order the merge reads them in.
+int decode_plan_selfcheck(int P, int Lk, int S, int sms) {
+  if (P < 1 || Lk < 1 || S < 0 || S > Lk || sms < 1 || (int64_t)P * Lk >= (1ll << 31)) return -1;
+  DecodePlan pl;
+  plan_init(&pl, P, Lk, S, sms);
+  struct Rec {
+    int p, lo, hi, slot, np;
+  };
+  std::vector<Rec> all;
+  std::vector<unsigned char> used((size_t)plan_slots(pl), 0);
+  for (int c = 0; c < pl.grid; ++c) {
+    const int np = plan_num_pieces(pl, c);
+    if (np < 1) return 1;
+    std::vector<unsigned char> seen((size_t)np, 0);
+    for (int k = 0; k < np; ++k) {
+      const int o = plan_order(pl, np, k);
+      if (o < 0 || o >= np || seen[(size_t)o]++) return 2;
+    }
+    for (int k = 0; k < np; ++k) {
+      const DecodePiece pc = plan_piece(pl, c, k);
+      if (pc.p < 0 || pc.p >= P || pc.lo < 0 || pc.lo >= pc.hi || pc.hi > Lk) return 3;
+      if (pc.npieces > 1 && (pc.slot < 0 || pc.slot >= plan_slots(pl) || used[(size_t)pc.slot]++))
+        return 4;
+      all.push_back({pc.p, pc.lo, pc.hi, pc.slot, pc.npieces});
+    }
+  }
+  std::sort(all.begin(), all.end(),
+            [](const Rec& a, const Rec& b) { return a.p != b.p ? a.p < b.p : a.lo < b.lo; });
+  size_t i = 0;
+  for (int p = 0; p < P; ++p) {
+    size_t j = i;
+    int end = 0;
+    for (; j < all.size() && all[j].p == p; ++j) {
+      if (all[j].lo != end) return 5;
+      end = all[j].hi;
+    }
+    if (end != Lk) return 5;
+    const int n = (int)(j - i);
+    for (size_t t = i; t < j; ++t) {
+      if (all[t].np != n) return 6;
+      if (n > 1 && plan_slot(pl, p, (int)(t - i)) != all[t].slot) return 7;
+    }
+    i = j;
+  }
+  return i == all.size() ? 0 : 5;
+}
 
 int decode_num_splits(int B, int Hq, int Hkv, int Lk, int d, int requested) {
   (void)Hq;

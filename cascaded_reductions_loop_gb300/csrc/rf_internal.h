@@ -69,6 +69,8 @@ cudaError_t launch_attn_fwd_f32_varlen(const float* Q, const float* K, const flo
                                        int causal, unsigned* err, cudaStream_t s);
 
 int decode_num_splits(int B, int Hq, int Hkv, int Lk, int d, int requested);
+// host only: 0 when the split-KV partition of P sequences is consistent
+int decode_plan_selfcheck(int P, int Lk, int S, int sms);
 size_t decode_workspace_bytes(int B, int Hq, int Hkv, int Lk, int d, int requested);
 cudaError_t launch_decode_splitkv(const void* Q, const void* K, const void* V, void* O, int B,
                                   int Hq, int Hkv, int Lk, int d, float scale, int requested,

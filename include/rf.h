@@ -399,6 +399,20 @@ rf_status rf_selftest_wait_timeout(int timeout_us, rf_stream_t stream);
  */
 rf_status rf_selftest_bounds(rf_stream_t stream);
 
+/*
+ * Host-side check of the split-KV decode partition (no counterpart in the
+ * paper; no GPU needed, no CUDA call made).  For B * Hkv sequences of Lk keys,
+ * num_splits as in rf_attn_decode_splitkv (0 = automatic) and a device of
+ * `sms` SMs, it walks the pieces every CTA would take and checks that every
+ * CTA has work, that the pieces of each sequence cover its keys exactly once,
+ * that the workspace slots of split sequences are distinct and in range, and
+ * that the merge would read a sequence's slots in key order.  Returns 0 when
+ * all of that holds, -1 for a shape rf_attn_decode_splitkv refuses (sizes
+ * < 1, num_splits outside 0..Lk, B * Hkv * Lk >= 2^31, sms < 1), else the
+ * number (1..7) of the first check that fails.
+ */
+int rf_selftest_decode_plan(int B, int Hkv, int Lk, int num_splits, int sms);
+
 #ifdef __cplusplus
 }
 #endif
