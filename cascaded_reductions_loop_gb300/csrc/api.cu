@@ -431,7 +431,7 @@ rf_status rf_selftest_wait_timeout(int timeout_us, rf_stream_t stream) {
 }
 
 int rf_selftest_decode_plan(int B, int Hkv, int Lk, int num_splits, int sms) {
-  if (B < 1 || Hkv < 1 || (int64_t)B * Hkv * Lk >= (1ll << 31)) return -1;
+  if (B < 1 || Hkv < 1 || Lk < 1 || (int64_t)B * Hkv * Lk >= (1ll << 31)) return -1;
   return decode_plan_selfcheck(B * Hkv, Lk, num_splits, sms);
 }
 

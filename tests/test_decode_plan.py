@@ -62,5 +62,6 @@ def test_largest_shapes(rf):
 
 def test_refused_shapes(rf):
     for args in [(0, 1, 1, 0, 1), (1, 0, 1, 0, 1), (1, 1, 0, 0, 1), (1, 1, 10, 11, 1),
-                 (1, 1, 10, -1, 1), (1, 1, 10, 0, 0), (64, 64, 524288, 0, 152)]:
+                 (1, 1, 10, -1, 1), (1, 1, 10, 0, 0), (64, 64, 524288, 0, 152),
+                 (1 << 20, 1 << 20, 0, 0, 152), (1 << 16, 1 << 16, 1, 0, 152)]:
         assert rf.rf_selftest_decode_plan(*args) == -1, args
