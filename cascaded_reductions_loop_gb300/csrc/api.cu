@@ -435,6 +435,10 @@ int rf_selftest_decode_plan(int B, int Hkv, int Lk, int num_splits, int sms) {
   return decode_plan_selfcheck(B * Hkv, Lk, num_splits, sms);
 }
 
+int rf_selftest_fp8_schedule(int M, int N, int clusters) {
+  return fp8_schedule_selfcheck(M, N, clusters);
+}
+
 rf_status rf_selftest_bounds(rf_stream_t stream) {
 #ifdef RF_DEBUG_BOUNDS
   unsigned* err = device_error_word();

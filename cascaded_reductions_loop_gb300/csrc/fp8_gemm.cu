@@ -31,6 +31,8 @@
 // the first two steps alone (rf_absmax_quant_fp8).
 #include <math.h>
 
+#include <vector>
+
 #include "rf_device.cuh"
 #include "rf_internal.h"
 
@@ -234,7 +236,7 @@ struct Tile {
   int ncols;   // 256 or 128
 };
 
-__device__ __forceinline__ Tile tile_of(int t, int tiles_n, int n_full) {
+__host__ __device__ __forceinline__ Tile tile_of(int t, int tiles_n, int n_full) {
   Tile w;
   if (t < n_full) {
     w.m0 = (t / tiles_n) * (2 * BM);
@@ -249,6 +251,27 @@ __device__ __forceinline__ Tile tile_of(int t, int tiles_n, int n_full) {
   return w;
 }
 static_assert(kStages * kStageBytes + 256 + 1024 <= 227 * 1024, "shared memory");
+
+// The tile schedule of a launch over `clusters` CTA pairs: whole rounds of
+// 256 x 256 tiles first; the tiles left for a last, partial round are split
+// in column halves when that spreads them over the pairs.  Tiles t < n_full
+// are full, the rest halves; cluster c takes tiles c, c + clusters, ...
+struct Schedule {
+  int tiles_n;      // 256-column tiles per row of tiles
+  int64_t pairs;    // full tiles of the output
+  int n_full;       // of them, scheduled whole
+  int n_tiles;      // scheduled tiles, halves counted one by one
+};
+inline Schedule make_schedule(int M, int N, int clusters) {
+  Schedule sc;
+  sc.tiles_n = (N + BN - 1) / BN;
+  sc.pairs = (int64_t)sc.tiles_n * ((M + 2 * BM - 1) / (2 * BM));
+  const int full_rounds = (int)(sc.pairs / clusters);
+  const int left = (int)(sc.pairs - (int64_t)full_rounds * clusters);
+  sc.n_full = (left > 0 && 2 * left <= clusters) ? full_rounds * clusters : (int)sc.pairs;
+  sc.n_tiles = sc.n_full + 2 * ((int)sc.pairs - sc.n_full);
+  return sc;
+}
 
 struct GemmBars {
   uint64_t full[kStages];    // rank 0: both CTAs' tiles of a stage have landed
@@ -615,9 +638,8 @@ cudaError_t launch_absmax_fp8_gemm(const void* X, const uint8_t* Wq, const float
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(fp8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
   if (e != cudaSuccess) return e;
-  const int tiles_n = (N + BN - 1) / BN;
-  const int64_t pairs = (int64_t)tiles_n * ((M + 2 * BM - 1) / (2 * BM));
-  if (pairs >= (1ll << 29)) return cudaErrorInvalidValue;
+  if ((int64_t)((N + BN - 1) / BN) * ((M + 2 * BM - 1) / (2 * BM)) >= (1ll << 29))
+    return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = kGemmSmem;
@@ -635,15 +657,41 @@ cudaError_t launch_absmax_fp8_gemm(const void* X, const uint8_t* Wq, const float
   const int clusters = gemm_clusters(sms, cfg);
   if (clusters < 1) return cudaErrorInvalidConfiguration;
   cfg.gridDim = dim3(2 * clusters, 1, 1);
-  // whole rounds of full tiles; the tiles left over for a last, partial round
-  // are split in column halves when that lets them spread over the pairs
-  const int full_rounds = (int)(pairs / clusters);
-  const int left = (int)(pairs - (int64_t)full_rounds * clusters);
-  const int n_full = (left > 0 && 2 * left <= clusters) ? full_rounds * clusters : (int)pairs;
-  const int n_tiles = n_full + 2 * ((int)pairs - n_full);
+  const Schedule sc = make_schedule(M, N, clusters);
   return cudaLaunchKernelEx(&cfg, fp8_gemm_kernel, tmA, tmB, tmBh, static_cast<const uint4*>(X), xq,
-                            sx, sw, static_cast<__nv_bfloat16*>(Y), M, N, K, tiles_n, n_full, n_tiles,
-                            ctr, err);
+                            sx, sw, static_cast<__nv_bfloat16*>(Y), M, N, K, sc.tiles_n, sc.n_full,
+                            sc.n_tiles, ctr, err);
+}
+
+// Host-side check of the tile schedule (make_schedule, tile_of and the
+// kernel's per-cluster tile count) for an M x N output on `clusters` pairs.
+// Returns 0 when it holds, -1 for refused sizes, else the number of the
+// first check that fails:
+//   1 the per-cluster tile counts add up to the scheduled tiles;
+//   2 every tile is a full tile or a column half, on the 256 x 128 grid;
+//   3 every 256-row x 128-column block of the output is computed once.
+int fp8_schedule_selfcheck(int M, int N, int clusters) {
+  if (M < 1 || N < 1 || clusters < 1 || clusters > 4096) return -1;
+  const Schedule sc = make_schedule(M, N, clusters);
+  if (sc.pairs >= (1ll << 24)) return -1;          // keeps the coverage map small
+  int64_t counted = 0;
+  for (int c = 0; c < clusters; ++c)
+    counted += sc.n_tiles > c ? (sc.n_tiles - c + clusters - 1) / clusters : 0;
+  if (counted != sc.n_tiles) return 1;
+  const int rows = (M + 2 * BM - 1) / (2 * BM);
+  std::vector<unsigned char> cover((size_t)rows * sc.tiles_n * 2, 0);
+  for (int t = 0; t < sc.n_tiles; ++t) {
+    const Tile w = tile_of(t, sc.tiles_n, sc.n_full);
+    if (w.ncols != BN && w.ncols != BN / 2) return 2;
+    if (w.m0 % (2 * BM) != 0 || w.n0 % (BN / 2) != 0 || (w.ncols == BN && w.n0 % BN != 0)) return 2;
+    const int r = w.m0 / (2 * BM), h0 = w.n0 / (BN / 2);
+    if (r >= rows || h0 + w.ncols / (BN / 2) > 2 * sc.tiles_n) return 2;
+    for (int h = h0; h < h0 + w.ncols / (BN / 2); ++h)
+      if (cover[(size_t)r * 2 * sc.tiles_n + h]++) return 3;
+  }
+  for (unsigned char v : cover)
+    if (v != 1) return 3;
+  return 0;
 }
 
 }  // namespace rf

@@ -413,6 +413,18 @@ rf_status rf_selftest_bounds(rf_stream_t stream);
  */
 int rf_selftest_decode_plan(int B, int Hkv, int Lk, int num_splits, int sms);
 
+/*
+ * Host-side check of the tile schedule of rf_absmax_fp8_gemm (no
+ * counterpart in the paper; no GPU needed, no CUDA call made).  For an
+ * M x N output computed by `clusters` CTA pairs (1..4096) it checks that the
+ * pairs' tile counts add up, that every scheduled tile is a 256 x 256 tile
+ * or a 256 x 128 column half on that grid, and that every 256-row x
+ * 128-column block of the output is computed exactly once.  Returns 0 when
+ * all of that holds, -1 for sizes < 1, clusters outside 1..4096 or more than
+ * 2^24 tiles, else the number (1..3) of the first check that fails.
+ */
+int rf_selftest_fp8_schedule(int M, int N, int clusters);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,8 +1,11 @@
-"""Host logic of the split-KV decode: the partition of the sequences' keys
-into pieces, the CTA that takes each piece, the workspace slot of each
-partial state and the order in which the merge reads them.  The checks run
-in the library's own host code (rf_selftest_decode_plan, the same functions
-the kernel evaluates on the device) and need no GPU."""
+"""Host logic of the work partitions, checked in the library's own host code
+(the same functions the kernels evaluate on the device) through C-ABI
+self-checks that need no GPU:
+* the split-KV decode (rf_selftest_decode_plan): the partition of the
+  sequences' keys into pieces, the CTA that takes each piece, the workspace
+  slot of each partial state and the order in which the merge reads them;
+* the FP8 GEMM (rf_selftest_fp8_schedule): the tiles of the output, whole
+  and in column halves, over the CTA pairs."""
 import random
 
 import pytest
@@ -65,3 +68,26 @@ def test_refused_shapes(rf):
                  (1, 1, 10, -1, 1), (1, 1, 10, 0, 0), (64, 64, 524288, 0, 152),
                  (1 << 20, 1 << 20, 0, 0, 152), (1 << 16, 1 << 16, 1, 0, 152)]:
         assert rf.rf_selftest_decode_plan(*args) == -1, args
+
+
+# ------------------------------------------------ FP8 GEMM tile schedule
+
+
+@pytest.mark.parametrize("clusters", [1, 2, 3, 7, 64, 74, 76])
+@pytest.mark.parametrize("M,N", [(4096, 4096), (1, 1), (256, 256), (257, 255), (4096, 128),
+                                 (100, 4096), (5000, 3000), (33, 8000)])
+def test_fp8_schedule(rf, M, N, clusters):
+    assert rf.rf_selftest_fp8_schedule(M, N, clusters) == 0
+
+
+def test_fp8_schedule_random_shapes(rf):
+    rng = random.Random(777)
+    for _ in range(2000):
+        M, N = rng.randint(1, 9000), rng.randint(1, 9000)
+        clusters = rng.choice([1, 2, 3, 5, 64, 66, 74, 76, rng.randint(1, 300)])
+        assert rf.rf_selftest_fp8_schedule(M, N, clusters) == 0, (M, N, clusters)
+
+
+def test_fp8_schedule_refused(rf):
+    for args in [(0, 1, 1), (1, 0, 1), (1, 1, 0), (1, 1, 4097), (1 << 20, 1 << 20, 76)]:
+        assert rf.rf_selftest_fp8_schedule(*args) == -1, args
