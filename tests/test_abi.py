@@ -155,3 +155,13 @@ def test_validation_rejects_bad_arguments_without_a_gpu(rf):
     assert rf.rf_absmax_fp8_gemm_workspace_size(16, 16, 40) == 0
     # self-test: out-of-range limit
     assert L.rf_selftest_wait_timeout(0, None) == rf.RF_ERR_INVALID_ARG
+
+
+def test_every_declaration_is_documented():
+    """Each function of the boundary is preceded by its comment block (what
+    it computes, argument meaning and layout, ownership, errors)."""
+    text = open(os.path.join(ROOT, "include", "rf.h")).read()
+    decls = re.finditer(r"^(?:rf_status|int|size_t|const char\*)\s+(rf_[a-z0-9_]+)\s*\(",
+                        text, flags=re.M)
+    undocumented = [m.group(1) for m in decls if not text[:m.start()].rstrip().endswith("*/")]
+    assert not undocumented, undocumented
