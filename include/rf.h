@@ -151,7 +151,8 @@ rf_status rf_attn_fwd_ex(int dtype, const void* Q, const void* K, const void* V,
  *          last equals total_q (total_k).  Lengths may be 0; a sequence with
  *          no keys gives zero rows.
  *   max_seqlen_q   >= every query length (sizes the grid).
- *   total_q, total_k >= 1.  d = 64 (both dtypes) or 128 (RF_F32 only).
+ *   total_q, total_k >= 1; B * H <= 65535; total_q * H, total_k * H < 2^31.
+ *   d = 64 (both dtypes) or 128 (RF_F32 only).
  * The host does not read the device arrays.  A kernel that finds them
  * inconsistent with max_seqlen_q / total_q / total_k skips that sequence,
  * touches nothing out of bounds and makes rf_get_device_status report
