@@ -248,6 +248,7 @@ rf_status rf_attn_fwd_ex(int dtype, const void* Q, const void* K, const void* V,
   if (dtype == RF_F32) {
     if (d != 64 && d != 128) return RF_ERR_UNSUPPORTED;
     if (mode == RF_ATTN_TWO_PASS) return RF_ERR_UNSUPPORTED;
+    if ((int64_t)B * H > 65535) return RF_ERR_INVALID_ARG;     // the grid's y extent
     unsigned* err = device_error_word();
     if (!err) return RF_ERR_CUDA;
     return from_cuda(launch_attn_fwd_f32(static_cast<const float*>(Q),

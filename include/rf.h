@@ -102,16 +102,17 @@ rf_status rf_get_device_status(rf_stream_t stream);
  *           accumulation and softmax state, P rounded to bf16 for P.V.
  *   Q, O    [B][H][Lq][d];  K, V  [B][H][Lk][d]  (multi-head: one K/V head
  *           per query head).
- *   Sizes   B, H, Lq, Lk >= 1 (B*H*Lq and B*H*Lk below 2^31);
- *           d = 64 (both dtypes) or 128 (RF_F32 only).
+ *   Sizes   B, H, Lq, Lk >= 1 (B*H*Lq and B*H*Lk below 2^31; for RF_F32
+ *           also B*H <= 65535); d = 64 (both dtypes) or 128 (RF_F32 only).
  *   scale   finite and > 0 (the usual 1/sqrt(d)).
  *   causal  0: every row reads every key.  1: autoregressive mask aligned
  *           to the end of the keys (the pages define no mask; this is the
  *           usual reading): row i reads keys j <= i + (Lk - Lq) only, so the
  *           last row reads all Lk keys; a row that reads no key (possible
  *           only when Lq > Lk) is written as zeros.
- * Errors: RF_ERR_INVALID_ARG (null/misaligned pointer, size < 1, causal not
- * 0 or 1, bad dtype), RF_ERR_UNSUPPORTED (d not covered), RF_ERR_CUDA.
+ * Errors: RF_ERR_INVALID_ARG (null/misaligned pointer, size < 1 or beyond
+ * the limits above, causal not 0 or 1, bad dtype), RF_ERR_UNSUPPORTED (d not
+ * covered), RF_ERR_CUDA.
  */
 rf_status rf_attn_fwd(int dtype, const void* Q, const void* K, const void* V, void* O,
                       int B, int H, int Lq, int Lk, int d, float scale, int causal,

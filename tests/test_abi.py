@@ -77,6 +77,8 @@ def test_validation_rejects_bad_arguments_without_a_gpu(rf):
     assert L.rf_attn_fwd(1, p, p, p, p, 1, 1, 64, 64, 64, -1.0, 0, None) == rf.RF_ERR_INVALID_ARG
     assert L.rf_attn_fwd(1, p, p, p, p, 1, 1, 64, 64, 96, 0.125, 0, None) == rf.RF_ERR_UNSUPPORTED
     assert L.rf_attn_fwd(0, p, p, p, p, 1, 1, 64, 64, 48, 0.125, 0, None) == rf.RF_ERR_UNSUPPORTED
+    # fp32: B * H is the grid's y extent (at most 65535)
+    assert L.rf_attn_fwd(0, p, p, p, p, 256, 256, 1, 1, 64, 0.125, 0, None) == rf.RF_ERR_INVALID_ARG
     # explicit evaluation order: unknown mode, two-pass beyond 256 keys or in fp32
     X = L.rf_attn_fwd_ex
     assert X(1, p, p, p, p, 1, 1, 64, 64, 64, 0.125, 0, 3, None) == rf.RF_ERR_INVALID_ARG
