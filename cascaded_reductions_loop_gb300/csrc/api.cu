@@ -379,6 +379,10 @@ rf_status rf_moe_gate_topk_softmax_ex(const void* X, const void* Wg, int T, int 
   if (D % 8 != 0) return RF_ERR_INVALID_ARG;   // 16-byte row pitch for TMA
   if (w_layout != RF_GATE_W_ED && w_layout != RF_GATE_W_DE) return RF_ERR_INVALID_ARG;
   if (E > 256 || k > 8) return RF_ERR_UNSUPPORTED;
+  // the tiles lie along the grid's y extent (at most 65535); the host plan
+  // makes at most T / 128 + (SMs per cluster wave) of them, within that limit
+  // for T <= 65535 * 120
+  if (T > 65535 * 120) return RF_ERR_UNSUPPORTED;
   if (w_layout == RF_GATE_W_DE && E % 64 != 0) return RF_ERR_UNSUPPORTED;
   unsigned* err = device_error_word();
   if (!err) return RF_ERR_CUDA;

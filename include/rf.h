@@ -301,11 +301,14 @@ rf_status rf_mla_decode(const void* Q, const void* CKV, void* O, int B, int Hq, 
  *   idx    [T][k] int32 out: selected experts by descending score, equal
  *          scores by ascending expert index.
  *   w      [T][k] fp32 out: softmax of the selected scores (same order).
- *   Sizes  T >= 1; D >= 1 with D % 8 == 0; 1 <= E <= 256; 1 <= k <= min(8, E).
+ *   Sizes  1 <= T <= 7864200 (65535 x 120: tiles of up to 128 tokens are
+ *          the grid's y extent); D >= 1 with D % 8 == 0; 1 <= E <= 256;
+ *          1 <= k <= min(8, E).
  * Scores are accumulated in fp32 on the tensor cores (exact when every
  * partial sum is an integer below 2^24, e.g. small-integer inputs).
  * Errors: RF_ERR_INVALID_ARG (null/misaligned pointer, size < 1, k > E,
- * D % 8 != 0), RF_ERR_UNSUPPORTED (E > 256 or k > 8), RF_ERR_CUDA.
+ * D % 8 != 0), RF_ERR_UNSUPPORTED (E > 256, k > 8 or T > 7864200),
+ * RF_ERR_CUDA.
  */
 rf_status rf_moe_gate_topk_softmax(const void* X, const void* Wg, int T, int D, int E, int k,
                                    int32_t* idx, float* w, rf_stream_t stream);

@@ -135,6 +135,8 @@ def test_validation_rejects_bad_arguments_without_a_gpu(rf):
     assert L.rf_moe_gate_topk_softmax(p, p, 16, 128, 257, 2, p, p, None) == rf.RF_ERR_UNSUPPORTED
     assert L.rf_moe_gate_topk_softmax(p, p, 16, 128, 4, 5, p, p, None) == rf.RF_ERR_INVALID_ARG
     assert L.rf_moe_gate_topk_softmax(p, p, 16, 128, 64, 9, p, p, None) == rf.RF_ERR_UNSUPPORTED
+    assert L.rf_moe_gate_topk_softmax(p, p, 65535 * 120 + 1, 128, 64, 2, p, p, None) == \
+        rf.RF_ERR_UNSUPPORTED
     # W_gate layout: an unknown layout, and [D][E] with E not a multiple of 64
     Mx = L.rf_moe_gate_topk_softmax_ex
     assert Mx(p, p, 16, 128, 64, 2, 2, p, p, None) == rf.RF_ERR_INVALID_ARG
