@@ -27,7 +27,7 @@ __all__ = [
     "rf_mla_decode_workspace_size", "rf_moe_gate_topk_softmax", "rf_moe_gate_topk_softmax_ex",
     "rf_absmax_fp8_gemm", "rf_absmax_fp8_gemm_workspace_size", "rf_absmax_quant_fp8",
     "rf_selftest_wait_timeout", "rf_selftest_bounds", "rf_selftest_decode_plan",
-    "rf_selftest_fp8_schedule",
+    "rf_selftest_fp8_schedule", "rf_selftest_moe_plan",
     "RF_OK", "RF_ERR_INVALID_ARG", "RF_ERR_UNSUPPORTED", "RF_ERR_WORKSPACE", "RF_ERR_CUDA",
     "RF_ERR_DEVICE_TIMEOUT", "RF_ERR_DEVICE_INPUT", "RF_ERR_DEVICE_LAYOUT", "RF_ERR_DEVICE_BOUNDS",
     "RF_F32", "RF_BF16",
@@ -81,6 +81,7 @@ _SIGS = {
     "rf_selftest_bounds": (_I, [_P]),
     "rf_selftest_decode_plan": (_I, [_I, _I, _I, _I, _I]),
     "rf_selftest_fp8_schedule": (_I, [_I, _I, _I]),
+    "rf_selftest_moe_plan": (_I, [_I, _I, _I, _I]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -364,3 +365,10 @@ def rf_selftest_fp8_schedule(M: int, N: int, clusters: int) -> int:
     when every block of the M x N output is computed once by the pairs'
     tiles, -1 for refused sizes, else the number of the first failed check."""
     return lib.rf_selftest_fp8_schedule(int(M), int(N), int(clusters))
+
+
+def rf_selftest_moe_plan(T: int, D: int, E: int, sms: int) -> int:
+    """Host-side check of the MoE gate's tile plan (no GPU needed): 0 when it
+    is consistent, -1 for refused sizes, else the number of the first failed
+    check."""
+    return lib.rf_selftest_moe_plan(int(T), int(D), int(E), int(sms))

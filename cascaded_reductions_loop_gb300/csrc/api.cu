@@ -444,6 +444,10 @@ int rf_selftest_fp8_schedule(int M, int N, int clusters) {
   return fp8_schedule_selfcheck(M, N, clusters);
 }
 
+int rf_selftest_moe_plan(int T, int D, int E, int sms) {
+  return moe_plan_selfcheck(T, D, E, sms);
+}
+
 rf_status rf_selftest_bounds(rf_stream_t stream) {
 #ifdef RF_DEBUG_BOUNDS
   unsigned* err = device_error_word();

@@ -440,29 +440,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Host side: tensor maps, the cluster split and the launch for one width.
-template <int NE, bool DE>
-cudaError_t launch_ne(const void* X, const void* Wg, int T, int D, int E, int k, int32_t* idx,
-                      float* w, unsigned* err, cudaStream_t s) {
-  using C = GateCfg<NE>;
-  CUtensorMap tmX, tmW;
-  // Tile shape: a cluster of cs CTAs (one per SM) splits the D reduction of
-  // a tile of bm token rows.  For each cs in {1, 2, 4, 8}, bm is the multiple
-  // of 8 (<= 128) that spreads the tokens evenly over whole waves of clusters.
-  // Cost = waves x (k-blocks per CTA x time per k-block + a fixed per-CTA cost
-  // of about three k-blocks, plus one for the cluster reduction when cs > 1),
-  // in units of the HBM time of a 128-row k-block at an even share of the
-  // bandwidth.  Time per k-block = max(bm / 128, MMA time) + a fixed 0.35 for
-  // the stage's barrier round trip and its W tile (fitted to a sweep of cs and
-  // bm on GB300 at T = 8192, D = 4096, E in {8, 64, 256}: halving the rows
-  // per CTA does not halve the k-block time).  The MMA always covers 128
-  // rows; at an even HBM share (~24 B/clk per SM) its N = NE product takes
-  // about NE * 3 / 1024 of the unit.
+// The tile plan of a launch on `sms` SMs.
+// Tile shape: a cluster of cs CTAs (one per SM) splits the D reduction of
+// a tile of bm token rows.  For each cs in {1, 2, 4, 8}, bm is the multiple
+// of 8 (<= 128) that spreads the tokens evenly over whole waves of clusters.
+// Cost = waves x (k-blocks per CTA x time per k-block + a fixed per-CTA cost
+// of about three k-blocks, plus one for the cluster reduction when cs > 1),
+// in units of the HBM time of a 128-row k-block at an even share of the
+// bandwidth.  Time per k-block = max(bm / 128, MMA time) + a fixed 0.35 for
+// the stage's barrier round trip and its W tile (fitted to a sweep of cs and
+// bm on GB300 at T = 8192, D = 4096, E in {8, 64, 256}: halving the rows
+// per CTA does not halve the k-block time).  The MMA always covers 128
+// rows; at an even HBM share (~24 B/clk per SM) its N = NE product takes
+// about NE * 3 / 1024 of the unit.
+struct GatePlan {
+  int cs;      // CTAs per cluster (split of D)
+  int bm;      // token rows per tile (a multiple of 8, <= 128)
+  int tiles;   // clusters: ceil(T / bm)
+};
+template <int NE>
+GatePlan gate_plan(int T, int D, int sms) {
   constexpr double kMmaPerKb = NE * 3.0 / 1024.0;
   constexpr double kStageFixed = 0.35;
-  const int nkb = (D + C::KB - 1) / C::KB;
-  const int sms = sm_count();
-  if (sms <= 0) return cudaErrorInvalidValue;
+  const int nkb = (D + GateCfg<NE>::KB - 1) / GateCfg<NE>::KB;
   int cs = 1, bm = BM;
   double best = -1.0;
   for (int c = 1; c <= 8; c *= 2) {
@@ -481,7 +481,24 @@ cudaError_t launch_ne(const void* X, const void* Wg, int T, int D, int E, int k,
       bm = b;
     }
   }
-  const int tiles = (T + bm - 1) / bm;
+  GatePlan gp;
+  gp.cs = cs;
+  gp.bm = bm;
+  gp.tiles = (int)(((int64_t)T + bm - 1) / bm);
+  return gp;
+}
+
+// Host side: tensor maps, the cluster split and the launch for one width.
+template <int NE, bool DE>
+cudaError_t launch_ne(const void* X, const void* Wg, int T, int D, int E, int k, int32_t* idx,
+                      float* w, unsigned* err, cudaStream_t s) {
+  using C = GateCfg<NE>;
+  CUtensorMap tmX, tmW;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidValue;
+  const GatePlan gp = gate_plan<NE>(T, D, sms);
+  const int cs = gp.cs, bm = gp.bm;
+  const int tiles = gp.tiles;
   if (tiles > 65535) return cudaErrorInvalidValue;
   if (!encode_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)D, (uint64_t)T,
                       (uint64_t)D * 2, BK, (uint32_t)bm, true) ||
@@ -524,6 +541,50 @@ cudaError_t launch_moe_gate(const void* X, const void* Wg, int T, int D, int E, 
   if (E <= 128) return launch_ne<128, false>(X, Wg, T, D, E, k, idx, w, err, s);
   if (E <= 256) return launch_ne<256, false>(X, Wg, T, D, E, k, idx, w, err, s);
   return cudaErrorInvalidValue;
+}
+
+// Host-side check of the tile plan (gate_plan, with the width the launcher
+// picks for E) for T tokens of D dims on `sms` SMs.  Returns 0 when it
+// holds, -1 for sizes the call refuses, else the number of the first check
+// that fails:
+//   1 the cluster size is 1, 2, 4 or 8 and at most the k-blocks and the SMs;
+//   2 the tile height is a multiple of 8 in 8..128;
+//   3 the tiles hold every token once and none is empty;
+//   4 the tiles fit the grid's y extent (65535) whenever T <= 65535 * 120;
+//   5 the cluster's CTAs share the k-blocks with none left out or idle;
+//   6 the epilogue's rows (ceil(bm / cs) per CTA) cover the tile.
+int moe_plan_selfcheck(int T, int D, int E, int sms) {
+  if (T < 1 || D < 1 || D % 8 != 0 || E < 1 || E > 256 || sms < 1) return -1;
+  GatePlan gp;
+  int kb;
+  if (E <= 32) {
+    gp = gate_plan<32>(T, D, sms);
+    kb = GateCfg<32>::KB;
+  } else if (E <= 64) {
+    gp = gate_plan<64>(T, D, sms);
+    kb = GateCfg<64>::KB;
+  } else if (E <= 128) {
+    gp = gate_plan<128>(T, D, sms);
+    kb = GateCfg<128>::KB;
+  } else {
+    gp = gate_plan<256>(T, D, sms);
+    kb = GateCfg<256>::KB;
+  }
+  const int nkb = (D + kb - 1) / kb;
+  const int cs = gp.cs, bm = gp.bm;
+  if ((cs != 1 && cs != 2 && cs != 4 && cs != 8) || cs > nkb || cs > sms) return 1;
+  if (bm % 8 != 0 || bm < 8 || bm > BM) return 2;
+  if ((int64_t)gp.tiles * bm < T || (int64_t)(gp.tiles - 1) * bm >= T) return 3;
+  if (T <= 65535 * 120 && gp.tiles > 65535) return 4;
+  int shared = 0;
+  for (int r = 0; r < cs; ++r) {
+    const int nk = nkb > r ? (nkb - r + cs - 1) / cs : 0;
+    if (nk < 1) return 5;
+    shared += nk;
+  }
+  if (shared != nkb) return 5;
+  if (((bm + cs - 1) / cs) * cs < bm) return 6;
+  return 0;
 }
 
 }  // namespace rf

@@ -73,6 +73,8 @@ int decode_num_splits(int B, int Hq, int Hkv, int Lk, int d, int requested);
 int decode_plan_selfcheck(int P, int Lk, int S, int sms);
 // host only: 0 when the FP8 GEMM's tile schedule covers an M x N output once
 int fp8_schedule_selfcheck(int M, int N, int clusters);
+// host only: 0 when the MoE gate's tile plan is consistent
+int moe_plan_selfcheck(int T, int D, int E, int sms);
 size_t decode_workspace_bytes(int B, int Hq, int Hkv, int Lk, int d, int requested);
 cudaError_t launch_decode_splitkv(const void* Q, const void* K, const void* V, void* O, int B,
                                   int Hq, int Hkv, int Lk, int d, float scale, int requested,

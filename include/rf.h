@@ -430,6 +430,20 @@ int rf_selftest_decode_plan(int B, int Hkv, int Lk, int num_splits, int sms);
  */
 int rf_selftest_fp8_schedule(int M, int N, int clusters);
 
+/*
+ * Host-side check of the tile plan of rf_moe_gate_topk_softmax (no
+ * counterpart in the paper; no GPU needed, no CUDA call made).  For T tokens
+ * of D dims, E experts and a device of `sms` SMs it checks that the chosen
+ * cluster size (1, 2, 4 or 8 CTAs splitting D) and tile height (a multiple
+ * of 8 up to 128 tokens) are valid, that the tiles hold every token once and
+ * fit the grid (for T <= 7864200), that the cluster's CTAs share the
+ * k-blocks with none idle, and that the epilogue's rows cover each tile.
+ * Returns 0 when all of that holds, -1 for refused sizes (T, D, E < 1,
+ * D % 8 != 0, E > 256, sms < 1), else the number (1..6) of the first check
+ * that fails.
+ */
+int rf_selftest_moe_plan(int T, int D, int E, int sms);
+
 #ifdef __cplusplus
 }
 #endif

@@ -5,7 +5,9 @@ self-checks that need no GPU:
   sequences' keys into pieces, the CTA that takes each piece, the workspace
   slot of each partial state and the order in which the merge reads them;
 * the FP8 GEMM (rf_selftest_fp8_schedule): the tiles of the output, whole
-  and in column halves, over the CTA pairs."""
+  and in column halves, over the CTA pairs;
+* the MoE gate (rf_selftest_moe_plan): the cluster split of D and the token
+  tiles chosen by the host's cost model."""
 import random
 
 import pytest
@@ -91,3 +93,29 @@ def test_fp8_schedule_random_shapes(rf):
 def test_fp8_schedule_refused(rf):
     for args in [(0, 1, 1), (1, 0, 1), (1, 1, 0), (1, 1, 4097), (1 << 20, 1 << 20, 76)]:
         assert rf.rf_selftest_fp8_schedule(*args) == -1, args
+
+
+# ------------------------------------------------------ MoE gate tile plan
+
+
+@pytest.mark.parametrize("E", [1, 8, 32, 64, 100, 128, 192, 256])
+@pytest.mark.parametrize("T,D", [(8192, 4096), (1, 8), (7, 64), (1000, 128), (65536, 1024),
+                                 (65535 * 120, 4096)])
+@pytest.mark.parametrize("sms", [1, 2, 148, 152, 1000])
+def test_moe_plan(rf, T, D, E, sms):
+    assert rf.rf_selftest_moe_plan(T, D, E, sms) == 0
+
+
+def test_moe_plan_random_shapes(rf):
+    rng = random.Random(4242)
+    for _ in range(3000):
+        T = rng.choice([rng.randint(1, 300), rng.randint(1, 100000), rng.randint(1, 65535 * 120)])
+        D = 8 * rng.randint(1, 1024)
+        E, sms = rng.randint(1, 256), rng.choice([1, 3, 8, 132, 148, 152, rng.randint(1, 2000)])
+        assert rf.rf_selftest_moe_plan(T, D, E, sms) == 0, (T, D, E, sms)
+
+
+def test_moe_plan_refused(rf):
+    for args in [(0, 8, 64, 152), (1, 0, 64, 152), (1, 12, 64, 152), (1, 8, 0, 152),
+                 (1, 8, 257, 152), (1, 8, 64, 0)]:
+        assert rf.rf_selftest_moe_plan(*args) == -1, args
